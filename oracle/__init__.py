@@ -1,0 +1,137 @@
+"""fp64 CPU oracle for tree-causal attention and greedy tree verification.
+
+TEST INFRASTRUCTURE. Only ``tests/``, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline leg may import this package. The product path
+(``tree_masked_attention_causal_gb300``) never does, and this package
+imports nothing from it.
+
+The arithmetic lives in ``oracle.c`` (plain C, OpenMP over rows). This module
+compiles it with gcc on first use and wraps it with ctypes and numpy.
+
+Parity pins: see the header of ``oracle.c``. Every function here is pinned
+by a test under ``tests/test_oracle_pins.py`` that checks it against
+something other than itself.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so next to it (gcc, -O2, OpenMP)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.run(["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-fopenmp",
+                        "-o", tmp, _SRC, "-lm"], check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P = ctypes.c_void_p
+            i32, i64, f64 = ctypes.c_int32, ctypes.c_int64, ctypes.c_double
+            lib.oracle_tree_attention_f64.argtypes = [P, P, P, P, P, P, P, P, i32, i32, i32, i32,
+                                                      i32, i32, f64, P, i64, P]
+            lib.oracle_tree_attention_f64.restype = None
+            lib.oracle_argmax_rows.argtypes = [P, i64, i64, P]
+            lib.oracle_argmax_rows.restype = None
+            lib.oracle_tree_verify.argtypes = [P, P, P, P, i32, i32, i64, i32, P, P, P]
+            lib.oracle_tree_verify.restype = None
+            lib.oracle_tree_is_valid.argtypes = [P, i32, i32]
+            lib.oracle_tree_is_valid.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _u16(t) -> np.ndarray:
+    """Raw bf16 bits of a CPU torch bf16 tensor (or a uint16 ndarray)."""
+    if isinstance(t, np.ndarray):
+        assert t.dtype == np.uint16
+        return np.ascontiguousarray(t)
+    import torch
+    assert t.dtype == torch.bfloat16
+    return np.ascontiguousarray(t.contiguous().view(torch.int16).numpy().view(np.uint16))
+
+
+def _i32(t) -> np.ndarray:
+    a = t if isinstance(t, np.ndarray) else t.numpy()
+    return np.ascontiguousarray(a, dtype=np.int32)
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def num_threads() -> int:
+    """OpenMP threads the oracle uses (OMP_NUM_THREADS, else all cores)."""
+    env = os.environ.get("OMP_NUM_THREADS")
+    return int(env) if env else (os.cpu_count() or 1)
+
+
+def tree_attention(q, k_cache, v_cache, prefix_lens, tree_k, tree_v, parents, n_nodes,
+                   scale: float = 0.0, sel=None, out: np.ndarray | None = None) -> np.ndarray:
+    """fp64 tree attention. Returns out [B, Nmax, Hq, d] (float64); rows
+    not computed (padded nodes, or rows outside ``sel``) stay NaN unless an
+    ``out`` buffer is passed. ``sel`` is an (n, 2) array of (b, i) pairs."""
+    lib = _load()
+    B, N, Hq, d = q.shape
+    Hkv, Pcap = k_cache.shape[1], k_cache.shape[2]
+    qa, kc, vc = _u16(q), _u16(k_cache), _u16(v_cache)
+    tk, tv = _u16(tree_k), _u16(tree_v)
+    pl, par, nn = _i32(prefix_lens), _i32(parents), _i32(n_nodes)
+    if out is None:
+        out = np.full((B, N, Hq, d), np.nan, dtype=np.float64)
+    sel_a = None if sel is None else np.ascontiguousarray(np.asarray(sel, dtype=np.int32).reshape(-1, 2))
+    lib.oracle_tree_attention_f64(_ptr(qa), _ptr(kc), _ptr(vc), _ptr(pl), _ptr(tk), _ptr(tv),
+                                  _ptr(par), _ptr(nn), B, N, Hq, Hkv, d, Pcap, float(scale),
+                                  None if sel_a is None else _ptr(sel_a),
+                                  0 if sel_a is None else sel_a.shape[0], _ptr(out))
+    return out
+
+
+def argmax_rows(logits) -> np.ndarray:
+    """First-max argmax of each row of a [..., V] bf16 tensor (int32)."""
+    lib = _load()
+    a = _u16(logits)
+    V = a.shape[-1]
+    rows = a.size // V
+    out = np.empty(rows, dtype=np.int32)
+    lib.oracle_argmax_rows(_ptr(a), rows, V, _ptr(out))
+    return out.reshape(a.shape[:-1])
+
+
+def tree_verify(logits, tokens, parents, n_nodes, max_depth: int):
+    """Greedy verification. Returns (accept_len [B], accept_path [B, max_depth+1],
+    argmax [B, Nmax]) as int32 arrays."""
+    lib = _load()
+    lg = _u16(logits)
+    B, N, V = lg.shape
+    tok, par, nn = _i32(tokens), _i32(parents), _i32(n_nodes)
+    alen = np.empty(B, dtype=np.int32)
+    path = np.empty((B, max_depth + 1), dtype=np.int32)
+    am = np.empty((B, N), dtype=np.int32)
+    lib.oracle_tree_verify(_ptr(lg), _ptr(tok), _ptr(par), _ptr(nn), B, N, V, max_depth,
+                           _ptr(alen), _ptr(path), _ptr(am))
+    return alen, path, am
+
+
+def tree_is_valid(parents_row, n: int, max_nodes: int) -> bool:
+    lib = _load()
+    p = _i32(np.asarray(parents_row))
+    return bool(lib.oracle_tree_is_valid(_ptr(p), int(n), int(max_nodes)))

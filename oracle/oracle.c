@@ -1,0 +1,243 @@
+/*
+ * oracle.c - plain, slow, fp64 CPU oracle for tree-causal attention and
+ * greedy tree verification.
+ *
+ * TEST INFRASTRUCTURE. Only the test suite, the package's smoke check and
+ * the benchmark's CPU-baseline leg load this library. The product path
+ * (the CUDA library and its Python binding) never calls it, and the two
+ * share no code, headers, tables or constants.
+ *
+ * Sources (the method is JetFlow, arXiv 2606.18394; JetSpec on some pages):
+ *  [blog]  "JetFlow: Scaling Speculative Decoding with Parallel Tree
+ *          Drafting" (james.trappett.org), section "What JetFlow Does
+ *          Differently". A tree node attends to the original prefix and to
+ *          its own ancestors, never to siblings or descendants. A path's
+ *          probability is a product of conditionals, each on the concrete
+ *          ancestor tokens of that branch.
+ *  [paper] Chinese translation of the paper (bittide.aicompass.dev),
+ *          section 2.1 "Background". The target model verifies the N
+ *          drafted tokens in parallel and accepts the longest prefix that
+ *          agrees with its own predictions.
+ *
+ * Readings where the pages say nothing:
+ *  - scale = 1/sqrt(head_dim) unless the caller passes another;
+ *  - query head h uses KV head floor(h / (Hq/Hkv));
+ *  - node 0 is the root (the last committed token); its own token is never
+ *    checked; the logits of node u predict the children of u;
+ *  - accept length counts path nodes including the root;
+ *  - among accepted nodes of equal depth the lowest index wins;
+ *  - argmax: ties go to the lowest index, +0 and -0 are equal, and NaN
+ *    ranks above every number (the first NaN wins).
+ *
+ * Pins (tests/test_oracle_pins.py): torch fp64 scaled_dot_product_attention
+ * with an independently built boolean mask; the chain tree equals textbook
+ * causal attention; with q = 0 the output is the plain mean of the visible
+ * values (closed form); relabelling or deleting non-ancestor nodes leaves a
+ * node's output bit-identical; torch.argmax; brute-force path enumeration
+ * on every tree with up to 6 nodes; hand-worked walk cases in
+ * tests/golden/walk_cases.txt.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* Exact bf16 -> double: a bf16 is the top half of an IEEE binary32. */
+static double bf16_to_double(uint16_t bits)
+{
+    uint32_t u = (uint32_t)bits << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* A sequence's tree is well formed iff 1 <= n <= max_nodes, parents[0] = -1
+ * and 0 <= parents[i] < i for 0 < i < n (topological order). */
+int oracle_tree_is_valid(const int32_t *parents_b, int32_t n, int32_t max_nodes)
+{
+    if (n < 1 || n > max_nodes) return 0;
+    if (parents_b[0] != -1) return 0;
+    for (int32_t i = 1; i < n; ++i)
+        if (parents_b[i] < 0 || parents_b[i] >= i) return 0;
+    return 1;
+}
+
+/* Root-to-i ancestor chain (i included) of a well-formed tree; returns its
+ * length. [blog] "each node can attend to the original prefix and its
+ * ancestors in the tree". */
+static int32_t ancestor_chain(const int32_t *parents_b, int32_t i, int32_t *chain)
+{
+    int32_t len = 0;
+    for (int32_t j = i; j >= 0; j = parents_b[j]) chain[len++] = j;
+    for (int32_t a = 0, z = len - 1; a < z; ++a, --z) {
+        int32_t t = chain[a];
+        chain[a] = chain[z];
+        chain[z] = t;
+    }
+    return len;
+}
+
+/*
+ * Tree attention, literally: for node i of sequence b the key/value sequence
+ * is prefix[0 .. P_b) followed by the tree rows of i's ancestors, root first,
+ * ending with i itself. Node i is the last query of ordinary causal attention
+ * over that sequence ([blog]: the draft distribution along a branch is a
+ * product of conditionals on that branch's concrete ancestors).
+ *
+ * q, out [B, Nmax, Hq, d]; k_cache, v_cache [B, Hkv, Pcap, d];
+ * tree_k, tree_v [B, Nmax, Hkv, d]. All bf16 inputs are raw uint16 bits.
+ * scale <= 0 selects 1/sqrt(d).
+ * sel: n_sel (b, i) pairs to compute, or NULL for every (b, i) with
+ *      i < n_nodes[b]. Rows not computed are left untouched.
+ * A sequence whose tree or prefix length is malformed gets NaN in every
+ * selected row.
+ */
+void oracle_tree_attention_f64(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                               const int32_t *prefix_lens, const uint16_t *tree_k,
+                               const uint16_t *tree_v, const int32_t *parents,
+                               const int32_t *n_nodes, int32_t B, int32_t Nmax, int32_t Hq,
+                               int32_t Hkv, int32_t d, int32_t Pcap, double scale,
+                               const int32_t *sel, int64_t n_sel, double *out)
+{
+    const int32_t G = Hq / Hkv;
+    if (scale <= 0.0) scale = 1.0 / sqrt((double)d);
+    int64_t n_rows = sel ? n_sel : (int64_t)B * Nmax;
+
+#pragma omp parallel
+    {
+        double *s = (double *)malloc(sizeof(double) * ((size_t)Pcap + (size_t)Nmax));
+        double *acc = (double *)malloc(sizeof(double) * (size_t)d);
+        int32_t *chain = (int32_t *)malloc(sizeof(int32_t) * (size_t)Nmax);
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t r = 0; r < n_rows; ++r) {
+            int32_t b = sel ? sel[2 * r] : (int32_t)(r / Nmax);
+            int32_t i = sel ? sel[2 * r + 1] : (int32_t)(r % Nmax);
+            const int32_t *par = parents + (int64_t)b * Nmax;
+            int32_t n = n_nodes[b];
+            int32_t P = prefix_lens[b];
+            int ok = oracle_tree_is_valid(par, n, Nmax) && P >= 0 && P <= Pcap;
+            if (ok && i >= n) continue; /* padded node: not an output row */
+            for (int32_t h = 0; h < Hq; ++h) {
+                double *o = out + (((int64_t)b * Nmax + i) * Hq + h) * d;
+                if (!ok) {
+                    for (int32_t c = 0; c < d; ++c) o[c] = NAN;
+                    continue;
+                }
+                int32_t kh = h / G;
+                int32_t len = ancestor_chain(par, i, chain);
+                const uint16_t *qv = q + (((int64_t)b * Nmax + i) * Hq + h) * d;
+                const uint16_t *kc = k_cache + ((int64_t)b * Hkv + kh) * Pcap * d;
+                const uint16_t *vc = v_cache + ((int64_t)b * Hkv + kh) * Pcap * d;
+                int32_t L = P + len;
+                /* scores s_j = scale * <q, k_j> over the causal sequence */
+                for (int32_t j = 0; j < L; ++j) {
+                    const uint16_t *kv = j < P ? kc + (int64_t)j * d
+                                               : tree_k + (((int64_t)b * Nmax + chain[j - P]) * Hkv + kh) * d;
+                    double dot = 0.0;
+                    for (int32_t c = 0; c < d; ++c) dot += bf16_to_double(qv[c]) * bf16_to_double(kv[c]);
+                    s[j] = scale * dot;
+                }
+                /* softmax over the sequence, then the weighted sum of values */
+                double m = -INFINITY;
+                for (int32_t j = 0; j < L; ++j) if (s[j] > m) m = s[j];
+                double z = 0.0;
+                for (int32_t c = 0; c < d; ++c) acc[c] = 0.0;
+                for (int32_t j = 0; j < L; ++j) {
+                    double w = exp(s[j] - m);
+                    z += w;
+                    const uint16_t *vv = j < P ? vc + (int64_t)j * d
+                                               : tree_v + (((int64_t)b * Nmax + chain[j - P]) * Hkv + kh) * d;
+                    for (int32_t c = 0; c < d; ++c) acc[c] += w * bf16_to_double(vv[c]);
+                }
+                for (int32_t c = 0; c < d; ++c) o[c] = acc[c] / z;
+            }
+        }
+        free(s);
+        free(acc);
+        free(chain);
+    }
+}
+
+/* First index of the maximum of one bf16 row: strict '>' keeps the first
+ * of equal values (+0 == -0); a NaN ranks above every number, so the first
+ * NaN is returned as soon as it is met. */
+int32_t oracle_argmax_row(const uint16_t *row, int64_t V)
+{
+    double best = bf16_to_double(row[0]);
+    int64_t arg = 0;
+    if (isnan(best)) return 0;
+    for (int64_t v = 1; v < V; ++v) {
+        double x = bf16_to_double(row[v]);
+        if (isnan(x)) return (int32_t)v;
+        if (x > best) {
+            best = x;
+            arg = v;
+        }
+    }
+    return (int32_t)arg;
+}
+
+/* argmax of n_rows rows of length V (row r at logits + r * V). */
+void oracle_argmax_rows(const uint16_t *logits, int64_t n_rows, int64_t V, int32_t *out)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < n_rows; ++r) out[r] = oracle_argmax_row(logits + r * V, V);
+}
+
+/* Naive recursion from the root: a child c of an accepted node u is accepted
+ * iff tokens[c] equals the target's greedy prediction at u ([paper] 2.1). */
+static void accept_from(int32_t u, int32_t depth, const int32_t *par, const int32_t *tok,
+                        const int32_t *am, int32_t n, int32_t *best, int32_t *best_depth)
+{
+    if (depth > *best_depth || (depth == *best_depth && u < *best)) {
+        *best = u;
+        *best_depth = depth;
+    }
+    for (int32_t c = 0; c < n; ++c)
+        if (par[c] == u && c != u && tok[c] == am[u])
+            accept_from(c, depth + 1, par, tok, am, n, best, best_depth);
+}
+
+/*
+ * Greedy tree verification for B sequences.
+ * am[b, i] = argmax of logits row (b, i) for i < n_nodes[b]. The accepted
+ * node is the deepest node whose every edge on the root path agrees
+ * (lowest index on ties). The path runs root first, and accept_len counts
+ * its nodes, root included. At most max_depth + 1 nodes are reported: a
+ * deeper accepted path is cut to its first max_depth + 1 nodes. Unused
+ * path slots hold -1. A malformed tree gives accept_len 0 and an all -1
+ * path. argmax_out (may be NULL) gets -1 on padded rows and on every row
+ * of a sequence whose n_nodes is out of range.
+ */
+void oracle_tree_verify(const uint16_t *logits, const int32_t *tokens, const int32_t *parents,
+                        const int32_t *n_nodes, int32_t B, int32_t Nmax, int64_t V,
+                        int32_t max_depth, int32_t *accept_len, int32_t *accept_path,
+                        int32_t *argmax_out)
+{
+    int32_t *am = (int32_t *)malloc(sizeof(int32_t) * (size_t)Nmax);
+    int32_t *chain = (int32_t *)malloc(sizeof(int32_t) * (size_t)Nmax);
+    for (int32_t b = 0; b < B; ++b) {
+        const int32_t *par = parents + (int64_t)b * Nmax;
+        const int32_t *tok = tokens + (int64_t)b * Nmax;
+        int32_t n = n_nodes[b];
+        int n_ok = n >= 1 && n <= Nmax;
+        for (int32_t i = 0; i < Nmax; ++i) am[i] = -1;
+        if (n_ok) oracle_argmax_rows(logits + (int64_t)b * Nmax * V, n, V, am);
+        if (argmax_out)
+            for (int32_t i = 0; i < Nmax; ++i) argmax_out[(int64_t)b * Nmax + i] = am[i];
+        int32_t *path = accept_path + (int64_t)b * (max_depth + 1);
+        for (int32_t k = 0; k <= max_depth; ++k) path[k] = -1;
+        if (!oracle_tree_is_valid(par, n, Nmax)) {
+            accept_len[b] = 0;
+            continue;
+        }
+        int32_t best = 0, best_depth = 0;
+        accept_from(0, 0, par, tok, am, n, &best, &best_depth);
+        int32_t len = ancestor_chain(par, best, chain);
+        if (len > max_depth + 1) len = max_depth + 1;
+        for (int32_t k = 0; k < len; ++k) path[k] = chain[k];
+        accept_len[b] = len;
+    }
+    free(am);
+    free(chain);
+}
