@@ -1,0 +1,395 @@
+"""Benchmark of the tree-attention + greedy-verification hot path on GB300.
+
+One step = one jf_tree_attention call plus one jf_tree_verify call over one
+batch of seeded synthetic inputs: the Qwen3-8B attention shape (32 query
+heads, 8 KV heads, head_dim 128), prefix 4096, a 256-node draft tree, and
+256 x 151936 bf16 logits with a planted accepted path of length 10.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+
+Prints one JSON line (rank 0). Under torchrun each rank runs an independent
+replica on its own GPU (the path has no exchange step). Timing is the max
+over ranks between barriers.
+
+Timed region: the K steps are captured once into CUDA graphs and replayed,
+with events on the launch stream before and after. The inputs rotate over
+enough device copies that each step's data (105 MB) was evicted from the
+126 MB L2 by the steps in between. The dominant kernel's duration comes
+from events the library records around each of its kernels inside the
+same graphs. e2e times the public calls eagerly on inputs in pinned host
+memory: each step copies them to the device and reads the results back.
+`--impl reference` times the fp64 CPU oracle on the host cores.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "qwen3_8b_tree256"
+METRIC = "tree-attn µs/step & % roofline (TFLOP/s | HBM GB/s); verify nodes/s"
+L2_BYTES = 126 * 2 ** 20
+MAX_DEPTH = 16
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        rows = []
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(f[1]), smax=float(f[2]), power=float(f[3]),
+                                 hw=f[5], hwt=f[6], swt=f[7], swp=f[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        loaded = [r for r in rows if r["power"] > 0.25 * max(x["power"] for x in rows)] or rows
+        reasons = set()
+        for r in loaded:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("swp", "sw_power_cap")):
+                if r[key].lower() in ("active", "1", "yes"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in loaded), "sm_max_mhz": max(r["smax"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(loaded)}
+
+
+def kernel_source_hash() -> str:
+    """Hash of the sources that define the attention kernel, to tie a stored
+    ncu traffic figure to the exact code it was measured on."""
+    h = hashlib.sha256()
+    for f in ("jf_attn.cu", "jf_common.cuh"):
+        h.update(open(os.path.join(ROOT, "tree_masked_attention_causal_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def stored_traffic():
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    ent = d.get("tree_attention")
+    if not ent or ent.get("source_hash") != kernel_source_hash():
+        return None
+    return ent
+
+
+# ------------------------------------------------------------ CPU oracle leg
+
+def time_oracle(inp, target_s: float = 8.0):
+    """Time the oracle on a bounded sample of one step and scale it to a full
+    step. Returns (us_per_step, sample_description, threads)."""
+    import numpy as np
+    import oracle
+    B, N = inp["parents"].shape
+    # calibrate on 2 nodes, then take as many as fit the budget
+    t0 = time.perf_counter()
+    oracle.tree_attention(inp["q"], inp["k_cache"], inp["v_cache"], inp["prefix_lens"], inp["tree_k"],
+                          inp["tree_v"], inp["parents"], inp["n_nodes"], sel=[(0, 0), (0, N - 1)])
+    per_node = (time.perf_counter() - t0) / 2
+    n_attn = int(max(2, min(N, 0.7 * target_s / max(per_node, 1e-6))))
+    sel = [(0, int(i)) for i in np.linspace(0, N - 1, n_attn).round().astype(int)]
+    t0 = time.perf_counter()
+    oracle.tree_attention(inp["q"], inp["k_cache"], inp["v_cache"], inp["prefix_lens"], inp["tree_k"],
+                          inp["tree_v"], inp["parents"], inp["n_nodes"], sel=sel)
+    t_attn = time.perf_counter() - t0
+    n_rows = min(B * N, 64)
+    lg = inp["logits"].reshape(B * N, -1)[:n_rows]
+    t0 = time.perf_counter()
+    oracle.argmax_rows(lg)
+    t_arg = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    oracle.tree_verify(inp["logits"][:1, :1], inp["tokens"][:1, :1], inp["parents"][:1, :1],
+                       inp["n_nodes"][:1].clamp(max=1), MAX_DEPTH)
+    t_walk_fixed = time.perf_counter() - t0
+    total_nodes = int(inp["n_nodes"].sum())
+    us = 1e6 * (t_attn * total_nodes / len(sel) + t_arg * total_nodes / n_rows + t_walk_fixed)
+    desc = (f"attention for {len(sel)} of {total_nodes} nodes (all heads) and argmax of {n_rows} of "
+            f"{total_nodes} logits rows, scaled to a full step")
+    return us, desc, oracle.num_threads(), t_attn + t_arg
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    from tree_masked_attention_causal_gb300 import synth
+    w = synth.WORKLOADS[args.workload]
+    inp = synth.make_inputs(w)
+    times = []
+    desc, threads = "", 0
+    n = max(1, min(args.steps, 3))
+    for _ in range(n):
+        us, desc, threads, _ = time_oracle(inp, target_s=min(20.0, 60.0 / n))
+        times.append(us)
+    us = statistics.median(times)
+    line = {"impl": "reference", "metric": METRIC, "value": us, "unit": "us/step", "n_gpus": world,
+            "steps": n, "warmup": 0, "ms_per_step": us / 1e3, "higher_is_better": False, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_of(w, None),
+            "cpu_baseline": {"value": us, "unit": "us/step", "cores": threads, "kind": "oracle", "sample": desc},
+            "e2e": {"value": us, "unit": "us/step", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def config_of(w, extra):
+    c = {"workload": f"{w.name}: batch {w.batch}, {w.n_q_heads}q/{w.n_kv_heads}kv heads, head_dim {w.head_dim}, "
+                     f"prefix {w.prefix_min}" + (f"-{w.prefix_max}" if w.prefix_max != w.prefix_min else "") +
+                     f", tree {w.max_nodes} nodes, vocab {w.vocab}",
+         "batch": w.batch, "tree_nodes": w.max_nodes, "prefix": w.prefix_max, "vocab": w.vocab}
+    if extra:
+        c.update(extra)
+    return c
+
+
+# ---------------------------------------------------------------- GPU leg
+
+def run_gpu(args, rank, world, local):
+    import torch
+    import torch.distributed as dist
+    from tree_masked_attention_causal_gb300 import _build, binding as jb, synth
+
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0:
+        _build.build()
+    if world > 1:
+        dist.barrier()
+    jb.load()
+
+    w = synth.WORKLOADS[args.workload]
+    inp = synth.make_inputs(w)
+    B, N, Hq, d = inp["q"].shape
+    Hkv, Pcap, V = inp["k_cache"].shape[1], inp["k_cache"].shape[2], inp["logits"].shape[-1]
+    shape = jb.make_shape(B, Hq, Hkv, d, N, Pcap, V)
+    names = ["q", "k_cache", "v_cache", "prefix_lens", "tree_k", "tree_v", "parents", "n_nodes", "tokens", "logits"]
+    step_bytes = sum(inp[k].numel() * inp[k].element_size() for k in names)
+    R = max(2, math.ceil(3 * L2_BYTES / step_bytes))
+    copies = [{k: inp[k].to(dev) for k in names} for _ in range(R)]
+    ws = torch.empty(jb.jf_workspace_bytes(shape), dtype=torch.uint8, device=dev)
+    out = torch.empty_like(copies[0]["q"])
+    alen = torch.empty(B, dtype=torch.int32, device=dev)
+    path = torch.empty(B, MAX_DEPTH + 1, dtype=torch.int32, device=dev)
+    am = torch.empty(B, N, dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def step(c):
+        jb.jf_tree_attention(c["q"], c["k_cache"], c["v_cache"], c["prefix_lens"], c["tree_k"], c["tree_v"],
+                             c["parents"], c["n_nodes"], out, shape, ws, status=status)
+        jb.jf_tree_verify(c["logits"], c["tokens"], c["parents"], c["n_nodes"], alen, path, am, shape, MAX_DEPTH, ws,
+                          status=status)
+
+    # warm-up (eager) and a correctness check of the planted path
+    for i in range(max(3, args.warmup)):
+        step(copies[i % R])
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, "device status flag raised"
+    assert int(alen[0].item()) == int(inp["planted_len"][0]), "planted accept length not recovered"
+
+    # graphs of G steps each; K = G * M
+    K = args.steps
+    G = max(g for g in range(1, min(K, 250) + 1) if K % g == 0)
+    M = K // G
+    kernels_per_step = 5
+    events = [torch.cuda.Event(enable_timing=True) for _ in range(2 * kernels_per_step * G)]
+    graph = torch.cuda.CUDAGraph()
+    launches0 = jb.jf_kernel_launch_count()
+    jb.jf_trace_kernels(events, kernels_per_step * G)
+    with torch.cuda.graph(graph):
+        for i in range(G):
+            step(copies[i % R])
+    n_traced = jb.jf_trace_count()
+    trace_names = [jb.jf_trace_name(k) for k in range(n_traced)]
+    jb.jf_trace_kernels(None, 0)
+    launches_per_step = (jb.jf_kernel_launch_count() - launches0) / G
+    graph.replay()                                   # untimed
+    torch.cuda.synchronize()
+
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        start.record()
+        for _ in range(M):
+            graph.replay()
+        end.record()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+    total_ms = start.elapsed_time(end)
+    clocks = clk.summary()
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    # per-kernel durations of the last replay
+    per = {}
+    for k, name in enumerate(trace_names):
+        per.setdefault(name, []).append(events[2 * k].elapsed_time(events[2 * k + 1]))
+    avg = {n: statistics.mean(v) for n, v in per.items()}
+    attn_ms = sum(avg.get(n, 0.0) for n in ("tree_prep", "tree_attention", "split_combine"))
+    verify_ms = sum(avg.get(n, 0.0) for n in ("argmax_chunk", "accept_walk"))
+
+    # e2e through the public calls: pinned host inputs, H2D every step, D2H results
+    host = {k: inp[k].pin_memory() for k in names}
+    dev_in = {k: torch.empty_like(copies[0][k]) for k in names}
+    h_alen = torch.empty(B, dtype=torch.int32).pin_memory()
+    h_path = torch.empty(B, MAX_DEPTH + 1, dtype=torch.int32).pin_memory()
+    h_am = torch.empty(B, N, dtype=torch.int32).pin_memory()
+    K_e2e = max(3, min(K, 50))
+
+    def e2e_step():
+        for k in names:
+            dev_in[k].copy_(host[k], non_blocking=True)
+        step(dev_in)
+        h_alen.copy_(alen, non_blocking=True)
+        h_path.copy_(path, non_blocking=True)
+        h_am.copy_(am, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(K_e2e):
+        e2e_step()
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    assert int(h_alen[0]) == int(inp["planted_len"][0])
+
+    flops = synth.attention_flops(inp["parents"], inp["n_nodes"], inp["prefix_lens"], Hq, d)
+    abytes = synth.attention_bytes(inp["prefix_lens"], inp["n_nodes"], Hq, Hkv, d)
+    vbytes = synth.verify_bytes(inp["n_nodes"], V)
+    pk, pk_src = peaks()
+    attn_kernel_ms = avg.get("tree_attention", float("nan"))
+    achieved = flops / (attn_kernel_ms * 1e-3) / 1e12
+    traffic = stored_traffic()
+    nodes = int(inp["n_nodes"].sum())
+
+    if rank == 0:
+        us_step = total_ms * 1e3 / (K * world)
+        cpu_us, cpu_desc, cpu_threads, _ = time_oracle(inp, target_s=args.cpu_seconds)
+        line = {
+            "metric": METRIC, "value": us_step, "unit": "us/step", "n_gpus": world, "steps": K,
+            "warmup": max(3, args.warmup), "ms_per_step": total_ms / K, "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": config_of(w, {"l2": f"inputs rotate over {R} device copies ({R * step_bytes / 2**20:.0f} MB "
+                                          f"> L2)", "graph_steps": G, "parallelism": f"replicas x{world}"}),
+            "attn_us": attn_ms * 1e3, "verify_us": verify_ms * 1e3,
+            "kernel_us": {n: v * 1e3 for n, v in avg.items()},
+            "attn_tflops": flops / (attn_ms * 1e-3) / 1e12,
+            "attn_roofline_frac": max(flops / (pk["bf16_tflops"] * 1e12), abytes / (pk["hbm_gbs"] * 1e9))
+            / (attn_ms * 1e-3),
+            "verify_gbs": vbytes / (verify_ms * 1e-3) / 1e9,
+            "verify_nodes_per_s": nodes / (verify_ms * 1e-3),
+            "roofline": {"bound": "tensor", "kernel": "tree_attention", "achieved": achieved,
+                         "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"],
+                         "peak_source": f"{pk_src} bf16 burst",
+                         "traffic": None if traffic is None else traffic["bytes_per_launch"],
+                         "algorithmic": flops},
+            "argmax_roofline": {"bound": "hbm", "kernel": "argmax_chunk",
+                                "achieved": vbytes / (avg.get("argmax_chunk", float("nan")) * 1e-3) / 1e9,
+                                "peak": pk["hbm_gbs"], "unit": "GB/s",
+                                "frac": vbytes / (avg.get("argmax_chunk", float("nan")) * 1e-3) / 1e9 / pk["hbm_gbs"]},
+            "cpu_baseline": {"value": cpu_us, "unit": "us/step", "cores": cpu_threads, "kind": "oracle",
+                             "sample": cpu_desc},
+            "e2e": {"value": e2e_ms * 1e3 / (K_e2e * world), "unit": "us/step",
+                    "h2d_bytes_per_step": step_bytes, "d2h_bytes_per_step": 4 * (B + B * (MAX_DEPTH + 1) + B * N)},
+            "gpu_launches": int(round(launches_per_step * K)),
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--cpu-seconds", type=float, default=8.0)
+    args = ap.parse_args()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_gpu(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,209 @@
+/*
+ * jf_tree.h - C ABI of the GB300 (sm_103a) tree-attention and greedy
+ * tree-verification library (libjf_tree.so).
+ *
+ * The method (JetFlow, arXiv 2606.18394; JetSpec on some pages) drafts a
+ * tree of candidate tokens under the accepted prefix. The target model
+ * verifies the whole tree in one parallel forward pass, then greedily
+ * accepts the longest root path that its own predictions agree with.
+ * This library provides the data-parallel hot path of that pass:
+ *
+ *   jf_tree_attention  one forward pass of tree-causal attention over the
+ *                      whole tree ("JetFlow: Scaling Speculative Decoding
+ *                      with Parallel Tree Drafting", blog, section "What
+ *                      JetFlow Does Differently": every node attends to the
+ *                      original prefix and to its own ancestors, never to
+ *                      siblings or descendants; all nodes are computed in
+ *                      one pass).
+ *   jf_tree_verify     per-node vocabulary argmax, then the longest
+ *                      accepted root path (the paper's section 2.1
+ *                      "Background": the target verifies the N drafted
+ *                      tokens in parallel and accepts the longest prefix
+ *                      that agrees with its own predictions).
+ *
+ * Conventions shared by every entry point
+ *  - Every tensor pointer is a CUDA device pointer on the current device.
+ *    The caller owns every buffer, the workspace and the stream.
+ *  - bf16 is IEEE bfloat16 (__nv_bfloat16) passed as raw 16-bit values.
+ *  - Tensors are dense and row-major, in the layouts stated per argument.
+ *  - Calls are asynchronous and ordered on `stream`, and they allocate no
+ *    device memory. The return value reports only problems the host can
+ *    see. Problems found on the device are OR-ed into `*status` (a device
+ *    int32, may be NULL), which the caller reads after synchronising.
+ *    The caller must zero it before the first call.
+ *  - One workspace may serve a jf_tree_attention call and a jf_tree_verify
+ *    call at the same time (the two use disjoint regions), but not two
+ *    calls of the same entry point that overlap on the GPU.
+ *
+ * Tree encoding: parents[b][i] is the parent of node i of sequence b.
+ * parents[b][0] = -1 (the root, i.e. the last committed token), and
+ * 0 <= parents[b][i] < i for 0 < i < n_nodes[b] (topological order). Nodes
+ * i >= n_nodes[b] are padding: they are neither read as tree nodes nor
+ * written.
+ */
+#ifndef JF_TREE_H
+#define JF_TREE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define JF_API __attribute__((visibility("default")))
+#else
+#define JF_API
+#endif
+
+/* Opaque CUDA handles (cudaStream_t / cudaEvent_t). */
+typedef struct CUstream_st *jf_stream_t;
+typedef struct CUevent_st *jf_event_t;
+
+/* Host return codes. */
+enum {
+    JF_OK = 0,
+    JF_ERR_NULL = 1,      /* a required pointer is NULL */
+    JF_ERR_SHAPE = 2,     /* a size is out of the supported range (see jf_shape) */
+    JF_ERR_ALIGN = 3,     /* a tensor pointer is not 16-byte aligned */
+    JF_ERR_WORKSPACE = 4, /* workspace_bytes < jf_workspace_bytes(shape) */
+    JF_ERR_CUDA = 5       /* a CUDA runtime/driver call or kernel launch failed */
+};
+
+/* Device status flags, OR-ed into *status. */
+enum {
+    JF_STATUS_BAD_TREE = 1,  /* a sequence had n_nodes outside [1, max_nodes], a
+                                parent breaking the encoding above, or (for
+                                attention) prefix_lens outside [0, prefix_cap] */
+    JF_STATUS_TIMEOUT = 2    /* a kernel's bounded wait expired; outputs of the
+                                call are undefined (never expected) */
+};
+
+/*
+ * Problem sizes.
+ *   batch       B >= 1 sequences
+ *   n_q_heads   Hq; n_kv_heads Hkv; Hq % Hkv == 0 and G = Hq / Hkv must be a
+ *               power of two <= 128. Query head h reads KV head h / G.
+ *   head_dim    d, 64 or 128
+ *   max_nodes   Nmax, 1..256 tree slots per sequence
+ *   prefix_cap  Pcap >= 1 rows per (sequence, KV head) in the KV cache
+ *   vocab       V >= 1 and a multiple of 8 (jf_tree_verify only)
+ *   scale       softmax scale; 0 selects 1/sqrt(d)
+ */
+typedef struct {
+    int32_t batch;
+    int32_t n_q_heads;
+    int32_t n_kv_heads;
+    int32_t head_dim;
+    int32_t max_nodes;
+    int32_t prefix_cap;
+    int32_t vocab;
+    float scale;
+} jf_shape;
+
+/*
+ * Bytes of workspace that jf_tree_attention and jf_tree_verify need for
+ * `shape` (one buffer serves both). Host-only, and needs no GPU. Returns 0
+ * when the shape is outside the supported range. The size does not depend
+ * on the prefix lengths or the trees, only on the shape.
+ */
+JF_API size_t jf_workspace_bytes(const jf_shape *shape);
+
+/*
+ * Tree-causal attention: one forward pass over every node of every tree.
+ *
+ * For node i of sequence b and query head h, with G = Hq / Hkv and kv = h / G:
+ *   out[b,i,h,:] = softmax_j(scale * q[b,i,h,:] . K_j) V_j
+ * over the keys j of the ordinary causal sequence that ends at node i:
+ * the prefix rows k_cache[b,kv,0 .. prefix_lens[b]) followed by the tree
+ * rows tree_k[b,a,kv,:] of every ancestor a of i and of i itself (the blog's
+ * "What JetFlow Does Differently": each node attends to the prefix and to
+ * its ancestors, never to siblings or descendants). V_j is the matching row
+ * of v_cache / tree_v. RoPE and positions are the caller's: q and tree_k
+ * arrive already rotated.
+ *
+ *   q            bf16 [B, Nmax, Hq, d]
+ *   k_cache      bf16 [B, Hkv, Pcap, d]; rows >= prefix_lens[b] are never
+ *   v_cache      bf16 [B, Hkv, Pcap, d]  used and may hold anything (NaN too)
+ *   prefix_lens  int32 [B], each in [0, Pcap]
+ *   tree_k       bf16 [B, Nmax, Hkv, d]; rows of padding nodes may hold anything
+ *   tree_v       bf16 [B, Nmax, Hkv, d]
+ *   parents      int32 [B, Nmax] (encoding above)
+ *   n_nodes      int32 [B], each in [1, Nmax]
+ *   out          bf16 [B, Nmax, Hq, d]; rows of padding nodes are not
+ *                written; every row of a sequence flagged BAD_TREE is
+ *                filled with NaN
+ *   workspace    device buffer of >= jf_workspace_bytes(shape) bytes,
+ *                256-byte aligned; its contents need no initialisation
+ *   status       device int32 or NULL
+ * Every bf16 pointer must be 16-byte aligned.
+ * Returns JF_OK, JF_ERR_NULL, JF_ERR_SHAPE, JF_ERR_ALIGN, JF_ERR_WORKSPACE
+ * or JF_ERR_CUDA.
+ */
+JF_API int32_t jf_tree_attention(const void *q, const void *k_cache, const void *v_cache,
+                                 const int32_t *prefix_lens, const void *tree_k,
+                                 const void *tree_v, const int32_t *parents,
+                                 const int32_t *n_nodes, void *out, const jf_shape *shape,
+                                 void *workspace, size_t workspace_bytes, int32_t *status,
+                                 jf_stream_t stream);
+
+/*
+ * Greedy tree verification.
+ *
+ * am[b,i] = argmax_v logits[b,i,v] for i < n_nodes[b], the lowest index on
+ * ties, +0 == -0, and a NaN ranks above every number (the first NaN wins).
+ * A non-root node c is accepted iff its parent p is accepted and
+ * tree_tokens[b,c] == am[b,p]; the root is always accepted (its token is
+ * not checked). The reported node is the deepest accepted node (lowest
+ * index on ties). Its root path, root first, goes to accept_path_out,
+ * and accept_len_out counts that path's nodes, root included (the paper's
+ * section 2.1 "Background": accept the longest prefix that agrees with the
+ * target's predictions). Only max_depth + 1 path slots exist, so a deeper
+ * accepted path is cut to its first max_depth + 1 nodes. The bonus token
+ * of greedy decoding is am at the last reported node (in argmax_out).
+ *
+ *   logits           bf16 [B, Nmax, V], 16-byte aligned
+ *   tree_tokens      int32 [B, Nmax]
+ *   parents, n_nodes as for jf_tree_attention
+ *   accept_len_out   int32 [B]; 0 for a sequence flagged BAD_TREE
+ *   accept_path_out  int32 [B, max_depth + 1]; unused slots -1
+ *   argmax_out       int32 [B, Nmax] or NULL; -1 on padding rows and on
+ *                    every row of a sequence whose n_nodes is out of range
+ *   max_depth        >= 0
+ * Returns as jf_tree_attention.
+ */
+JF_API int32_t jf_tree_verify(const void *logits, const int32_t *tree_tokens,
+                              const int32_t *parents, const int32_t *n_nodes,
+                              int32_t *accept_len_out, int32_t *accept_path_out,
+                              int32_t *argmax_out, const jf_shape *shape, int32_t max_depth,
+                              void *workspace, size_t workspace_bytes, int32_t *status,
+                              jf_stream_t stream);
+
+/* Static description of a return code or status flag. */
+JF_API const char *jf_status_string(int32_t code);
+
+/*
+ * Instrumentation (host-only bookkeeping; adds no device work).
+ *
+ * jf_kernel_launch_count: kernels this library has launched in this process.
+ *
+ * jf_trace_kernels: arm per-kernel timing. `events` holds 2 * capacity
+ * cudaEvent_t handles created by the caller with timing enabled. Each
+ * following kernel launch records events[2k] before and events[2k+1] after
+ * itself on the launch stream, for k = 0, 1, ... < capacity. A call with
+ * capacity 0 (or events NULL) disarms. The caller keeps `events` alive while
+ * armed.
+ * jf_trace_count: pairs recorded since the last arm.
+ * jf_trace_name: name of the kernel that recorded pair k (NULL if none).
+ */
+JF_API uint64_t jf_kernel_launch_count(void);
+JF_API int32_t jf_trace_kernels(jf_event_t *events, int32_t capacity);
+JF_API int32_t jf_trace_count(void);
+JF_API const char *jf_trace_name(int32_t k);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* JF_TREE_H */

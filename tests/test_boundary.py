@@ -1,0 +1,125 @@
+"""The C ABI boundary without a GPU.
+
+The library must load on a machine without a GPU and export every function
+that include/jf_tree.h declares. Every argument error that the host can
+detect is reported before the first CUDA call, so these tests pass fake
+(never dereferenced) pointers and never reach a kernel.
+"""
+
+import ctypes
+
+import pytest
+
+from tree_masked_attention_causal_gb300 import _build, binding as jb
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return jb.load()
+
+
+def test_exports_every_header_symbol(lib):
+    names = jb.header_symbols()
+    assert {"jf_tree_attention", "jf_tree_verify", "jf_workspace_bytes", "jf_status_string"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def good_shape(**kw):
+    d = dict(batch=2, n_q_heads=8, n_kv_heads=2, head_dim=128, max_nodes=64, prefix_cap=1000, vocab=4096)
+    d.update(kw)
+    return jb.make_shape(**d)
+
+
+def test_workspace_bytes(lib):
+    assert jb.jf_workspace_bytes(good_shape()) > 0
+    assert jb.jf_workspace_bytes(good_shape(batch=4)) > jb.jf_workspace_bytes(good_shape())
+    for bad in (dict(batch=0), dict(max_nodes=0), dict(max_nodes=257)):
+        assert jb.jf_workspace_bytes(good_shape(**bad)) == 0
+    # a verify-only shape (attention fields unset) still gets a workspace
+    assert jb.jf_workspace_bytes(jb.make_shape(3, 0, 0, 0, 16, 0, 1024)) > 0
+    # an attention-only shape (vocab unset) too
+    assert jb.jf_workspace_bytes(good_shape(vocab=0)) > 0
+    assert lib.jf_workspace_bytes(None) == 0
+
+
+A16 = 1 << 20            # fake 16-byte-aligned addresses: never dereferenced
+
+
+def attn(shape, ws_bytes=1 << 40, **over):
+    args = dict(q=A16, k_cache=A16, v_cache=A16, prefix_lens=A16, tree_k=A16, tree_v=A16, parents=A16,
+                n_nodes=A16, out=A16, workspace=A16)
+    args.update(over)
+    return jb.jf_tree_attention(args["q"], args["k_cache"], args["v_cache"], args["prefix_lens"], args["tree_k"],
+                                args["tree_v"], args["parents"], args["n_nodes"], args["out"], shape,
+                                args["workspace"], ws_bytes, status=None, stream=0, check=False)
+
+
+def verify(shape, ws_bytes=1 << 40, max_depth=16, **over):
+    args = dict(logits=A16, tokens=A16, parents=A16, n_nodes=A16, alen=A16, path=A16, workspace=A16)
+    args.update(over)
+    return jb.jf_tree_verify(args["logits"], args["tokens"], args["parents"], args["n_nodes"], args["alen"],
+                             args["path"], None, shape, max_depth, args["workspace"], ws_bytes, status=None,
+                             stream=0, check=False)
+
+
+@pytest.mark.parametrize("name", ["q", "k_cache", "v_cache", "prefix_lens", "tree_k", "tree_v", "parents",
+                                  "n_nodes", "out", "workspace"])
+def test_attention_null_pointer(lib, name):
+    assert attn(good_shape(), **{name: None}) == jb.JF_ERR_NULL
+
+
+@pytest.mark.parametrize("bad", [dict(batch=0), dict(n_q_heads=6, n_kv_heads=4), dict(n_q_heads=12, n_kv_heads=4),
+                                 dict(head_dim=96), dict(head_dim=256), dict(max_nodes=300), dict(prefix_cap=0),
+                                 dict(n_kv_heads=0), dict(scale=-1.0), dict(scale=float("nan")),
+                                 dict(n_q_heads=256, n_kv_heads=1)])
+def test_attention_bad_shape(lib, bad):
+    assert attn(good_shape(**bad)) == jb.JF_ERR_SHAPE
+
+
+@pytest.mark.parametrize("name", ["q", "k_cache", "v_cache", "tree_k", "tree_v", "out"])
+def test_attention_misaligned(lib, name):
+    assert attn(good_shape(), **{name: A16 + 8}) == jb.JF_ERR_ALIGN
+
+
+def test_attention_workspace(lib):
+    s = good_shape()
+    need = jb.jf_workspace_bytes(s)
+    assert attn(s, ws_bytes=need - 1) == jb.JF_ERR_WORKSPACE
+    assert attn(s, workspace=A16 + 128) == jb.JF_ERR_ALIGN
+
+
+def test_attention_null_shape(lib):
+    rc = lib.jf_tree_attention(A16, A16, A16, A16, A16, A16, A16, A16, A16, None, A16, 1 << 30, None, None)
+    assert rc == jb.JF_ERR_NULL
+
+
+@pytest.mark.parametrize("name", ["logits", "tokens", "parents", "n_nodes", "alen", "path", "workspace"])
+def test_verify_null_pointer(lib, name):
+    assert verify(good_shape(), **{name: None}) == jb.JF_ERR_NULL
+
+
+@pytest.mark.parametrize("bad", [dict(vocab=0), dict(vocab=1001), dict(max_nodes=257), dict(batch=0)])
+def test_verify_bad_shape(lib, bad):
+    assert verify(good_shape(**bad)) == jb.JF_ERR_SHAPE
+
+
+def test_verify_bad_depth_alignment_workspace(lib):
+    s = good_shape()
+    assert verify(s, max_depth=-1) == jb.JF_ERR_SHAPE
+    assert verify(s, logits=A16 + 2) == jb.JF_ERR_ALIGN
+    assert verify(s, ws_bytes=jb.jf_workspace_bytes(s) - 1) == jb.JF_ERR_WORKSPACE
+
+
+def test_status_strings(lib):
+    for code in range(6):
+        assert jb.jf_status_string(code)
+    assert "unknown" in jb.jf_status_string(99)
+
+
+def test_trace_arm_disarm_without_gpu(lib):
+    assert lib.jf_trace_kernels(None, 0) == jb.JF_OK
+    assert jb.jf_trace_count() == 0
+    assert jb.jf_trace_name(0) is None
+    assert jb.jf_kernel_launch_count() == 0   # nothing was launched on this machine

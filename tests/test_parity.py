@@ -1,0 +1,222 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Accept lengths, paths and argmax must match bit for bit. Attention outputs
+must be within max-abs 1e-2 and mean-abs 1e-3 of the fp64 oracle, on
+unit-variance bf16 inputs. Every call runs with guard zones around `out`,
+and padding rows must still hold the sentinel.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from tree_masked_attention_causal_gb300 import synth
+import oracle
+from helpers import (assert_attention_close, lib, oracle_attention, out_bits, out_f64, padding_untouched,
+                     run_attention, run_verify, shape_of, small_inputs, to_dev, valid_rows)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    lib()
+
+
+# The five workloads; the serving batch is checked on sampled rows.
+FULL = ["tiny", "qwen3_8b_tree16", "qwen3_8b_tree256", "qwen3_30b_a3b_tree256"]
+
+
+@pytest.mark.parametrize("name", FULL + ["serving_16x64"])
+def test_workload_attention(name):
+    inp = synth.make_inputs(synth.WORKLOADS[name])
+    dev = to_dev(inp)
+    shape = shape_of(inp)
+    out, status = run_attention(dev, shape)
+    assert status == 0
+    got = out_f64(out)
+    if name in FULL:
+        rows = valid_rows(inp)
+        ref = oracle_attention(inp)
+    else:
+        g = torch.Generator().manual_seed(5)
+        B, N = inp["parents"].shape
+        rows = sorted({(int(torch.randint(0, B, (1,), generator=g)), int(torch.randint(0, N, (1,), generator=g)))
+                       for _ in range(48)} | {(0, 0), (B - 1, N - 1)})
+        ref = oracle_attention(inp, sel=rows)
+    assert_attention_close(got, ref, rows, name)
+
+
+@pytest.mark.parametrize("name", FULL + ["serving_16x64"])
+def test_workload_verify(name):
+    inp = synth.make_inputs(synth.WORKLOADS[name])
+    dev = to_dev(inp)
+    alen, path, am, status = run_verify(dev, shape_of(inp), max_depth=16)
+    assert status == 0
+    r_len, r_path, r_am = oracle.tree_verify(inp["logits"], inp["tokens"], inp["parents"], inp["n_nodes"], 16)
+    np.testing.assert_array_equal(am, r_am)
+    np.testing.assert_array_equal(alen, r_len)
+    np.testing.assert_array_equal(path, r_path)
+    np.testing.assert_array_equal(alen, inp["planted_len"].numpy())
+
+
+def check_attention(inp, scale=0.0, rows=None):
+    dev = to_dev(inp)
+    shape = shape_of(inp, scale)
+    out, status = run_attention(dev, shape)
+    ref = oracle_attention(inp, scale=scale)
+    rows = rows if rows is not None else valid_rows(inp)
+    assert_attention_close(out_f64(out), ref, rows)
+    assert padding_untouched(out_bits(out), inp)
+    return out, status
+
+
+@pytest.mark.parametrize("G,d", [(1, 64), (2, 128), (4, 64), (8, 128), (16, 64), (32, 128)])
+def test_gqa_groups_and_head_dims(G, d):
+    Hkv = 2
+    inp = small_inputs(10 + G, B=2, N=40, Hq=G * Hkv, Hkv=Hkv, d=d, Pcap=300)
+    check_attention(inp)
+
+
+def test_single_node_tree():
+    inp = small_inputs(1, B=3, N=1, parents=torch.full((3, 1), -1, dtype=torch.int32), Pcap=333)
+    check_attention(inp)
+
+
+def test_chain_of_256():
+    chain = torch.tensor([[-1] + list(range(255))], dtype=torch.int32)
+    inp = small_inputs(2, B=1, N=256, Hq=4, Hkv=1, d=128, Pcap=129, parents=chain,
+                       prefixes=torch.tensor([129], dtype=torch.int32))
+    check_attention(inp)
+
+
+def test_star_tree_256():
+    star = torch.tensor([[-1] + [0] * 255], dtype=torch.int32)
+    inp = small_inputs(3, B=1, N=256, Hq=8, Hkv=8, d=64, Pcap=64, parents=star)
+    check_attention(inp)
+
+
+def test_prefix_zero_and_full():
+    inp = small_inputs(4, B=3, N=33, Pcap=256, prefixes=torch.tensor([0, 256, 128], dtype=torch.int32))
+    check_attention(inp)
+
+
+def test_ragged_n_nodes_leaves_padding_untouched():
+    inp = small_inputs(5, B=4, N=96, Hq=8, Hkv=2, d=128, Pcap=700,
+                       n_nodes=torch.tensor([96, 1, 37, 65], dtype=torch.int32))
+    for b in range(4):                                  # padding parents: anything
+        inp["parents"][b, int(inp["n_nodes"][b]):] = 12345
+    check_attention(inp)
+
+
+def test_nan_in_unused_cache_rows_and_padding_nodes():
+    inp = small_inputs(6, B=2, N=50, Pcap=390, prefixes=torch.tensor([77, 389], dtype=torch.int32),
+                       n_nodes=torch.tensor([50, 23], dtype=torch.int32), kv_fill=float("nan"))
+    inp["tree_k"][1, 23:] = float("nan")
+    inp["tree_v"][1, 23:] = float("nan")
+    inp["q"][1, 23:] = float("nan")
+    check_attention(inp)
+
+
+def test_custom_scale():
+    inp = small_inputs(7, B=1, N=30, Pcap=150)
+    check_attention(inp, scale=0.05)
+
+
+def test_long_ragged_prefixes_split_kv():
+    """Prefixes long enough that every query tile is split over CTAs."""
+    inp = small_inputs(8, B=3, N=24, Hq=32, Hkv=8, d=128, Pcap=9000,
+                       prefixes=torch.tensor([9000, 1, 4097], dtype=torch.int32))
+    check_attention(inp)
+
+
+def test_malformed_tree_flags_and_nans():
+    inp = small_inputs(9, B=3, N=16, Pcap=100)
+    inp["parents"][1, 5] = 7                           # parent not earlier
+    inp["n_nodes"][2] = 0                              # out of range
+    dev = to_dev(inp)
+    out, status = run_attention(dev, shape_of(inp))
+    assert status & 1
+    o = out.float().cpu()
+    assert torch.isnan(o[1]).all() and torch.isnan(o[2]).all()
+    ref = oracle_attention(inp)
+    assert_attention_close(out_f64(out), ref, [(0, i) for i in range(16)])
+
+
+def test_repeat_calls_are_deterministic_and_reuse_workspace():
+    inp = small_inputs(11, B=2, N=64, Hq=32, Hkv=8, d=128, Pcap=3000)
+    dev = to_dev(inp)
+    shape = shape_of(inp)
+    from helpers import new_workspace
+    ws = new_workspace(shape)
+    a, _ = run_attention(dev, shape, ws=ws)
+    b, _ = run_attention(dev, shape, ws=ws)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+# ------------------------------------------------------------------ verify
+
+def check_verify(inp, max_depth=16):
+    dev = to_dev(inp)
+    alen, path, am, status = run_verify(dev, shape_of(inp), max_depth=max_depth)
+    r_len, r_path, r_am = oracle.tree_verify(inp["logits"], inp["tokens"], inp["parents"], inp["n_nodes"], max_depth)
+    np.testing.assert_array_equal(am, r_am)
+    np.testing.assert_array_equal(alen, r_len)
+    np.testing.assert_array_equal(path, r_path)
+    return status
+
+
+def test_verify_ties_nan_and_signed_zero():
+    inp = small_inputs(20, B=2, N=8, vocab=40000)
+    lg = inp["logits"]
+    lg[0, 0] = 0.0
+    lg[0, 1, 20000] = 9.0
+    lg[0, 1, 35000] = 9.0                              # tie across chunks: lowest index
+    lg[0, 2, 5] = float("nan")
+    lg[0, 2, 30000] = float("nan")                     # first NaN wins
+    lg[0, 3] = -0.0
+    lg[0, 3, 17000] = 0.0                              # +0 == -0: index 0 wins
+    lg[0, 4] = float("-inf")
+    lg[0, 5, 39999] = float("inf")
+    lg[0, 6, 16383] = 10.0                             # chunk boundary
+    lg[0, 6, 16384] = 10.0
+    check_verify(inp)
+
+
+def test_verify_duplicate_sibling_tokens_and_cut_path():
+    N = 12
+    par = torch.tensor([[-1, 0, 0, 1, 2, 3, 4, 5, 6, 7, 8, 9]], dtype=torch.int32)
+    inp = small_inputs(21, B=1, N=N, parents=par, vocab=64)
+    top = torch.arange(N) % 7 + 3
+    lg = torch.zeros(1, N, 64)
+    lg[0, torch.arange(N), top] = 5.0
+    inp["logits"] = lg.to(torch.bfloat16)
+    tok = torch.zeros(1, N, dtype=torch.int32)
+    for c in range(1, N):
+        tok[0, c] = top[par[0, c]]
+    inp["tokens"] = tok
+    check_verify(inp, max_depth=16)
+    check_verify(inp, max_depth=3)
+    check_verify(inp, max_depth=0)
+
+
+def test_verify_ragged_and_malformed():
+    inp = small_inputs(22, B=4, N=40, vocab=1000, n_nodes=torch.tensor([40, 1, 17, 0], dtype=torch.int32))
+    inp["parents"][2, 17:] = 999
+    inp["parents"][0, 9] = 9
+    status = check_verify(inp)
+    assert status & 1
+
+
+def test_verify_random_trees_many_matches():
+    """Small vocabulary so that many edges agree and long paths form."""
+    for seed in range(3):
+        inp = small_inputs(30 + seed, B=8, N=64, vocab=8)
+        check_verify(inp, max_depth=63)
+
+
+def test_verify_all_chunks_vocab_151936():
+    inp = small_inputs(40, B=2, N=5, vocab=151936)
+    check_verify(inp)

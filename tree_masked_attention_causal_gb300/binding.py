@@ -1,0 +1,160 @@
+"""Thin ctypes binding of libjf_tree.so (include/jf_tree.h).
+
+Argument marshalling only: every step of the computation runs in the
+library's CUDA kernels. The functions keep the C names and argument order.
+Tensors are passed as ``data_ptr()``; the stream defaults to torch's current
+CUDA stream. If the library has not been built, loading raises. There is
+no fallback path.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+from typing import List, Optional
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libjf_tree.so")
+HEADER = os.path.join(os.path.dirname(PKG), "include", "jf_tree.h")
+
+JF_OK, JF_ERR_NULL, JF_ERR_SHAPE, JF_ERR_ALIGN, JF_ERR_WORKSPACE, JF_ERR_CUDA = range(6)
+JF_STATUS_BAD_TREE, JF_STATUS_TIMEOUT = 1, 2
+
+
+class JfShape(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("n_q_heads", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("max_nodes", ctypes.c_int32), ("prefix_cap", ctypes.c_int32),
+                ("vocab", ctypes.c_int32), ("scale", ctypes.c_float)]
+
+
+class JfError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn} returned {code}: {jf_status_string(code)}")
+        self.code = code
+
+
+_lib = None
+
+
+def load() -> ctypes.CDLL:
+    """Load libjf_tree.so from the package directory (built by _build.build())."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "tree_masked_attention_causal_gb300._build.build()")
+        lib = ctypes.CDLL(LIB_PATH)
+        P, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+        sp = ctypes.POINTER(JfShape)
+        lib.jf_workspace_bytes.argtypes = [sp]
+        lib.jf_workspace_bytes.restype = sz
+        lib.jf_tree_attention.argtypes = [P, P, P, P, P, P, P, P, P, sp, P, sz, P, P]
+        lib.jf_tree_attention.restype = i32
+        lib.jf_tree_verify.argtypes = [P, P, P, P, P, P, P, sp, i32, P, sz, P, P]
+        lib.jf_tree_verify.restype = i32
+        lib.jf_status_string.argtypes = [i32]
+        lib.jf_status_string.restype = ctypes.c_char_p
+        lib.jf_kernel_launch_count.argtypes = []
+        lib.jf_kernel_launch_count.restype = ctypes.c_uint64
+        lib.jf_trace_kernels.argtypes = [P, i32]
+        lib.jf_trace_kernels.restype = i32
+        lib.jf_trace_count.argtypes = []
+        lib.jf_trace_count.restype = i32
+        lib.jf_trace_name.argtypes = [i32]
+        lib.jf_trace_name.restype = ctypes.c_char_p
+        _lib = lib
+    return _lib
+
+
+def header_symbols() -> List[str]:
+    """Names of every function include/jf_tree.h declares with JF_API."""
+    text = open(HEADER).read()
+    return re.findall(r"JF_API\s+[\w\s\*]+?\b(jf_\w+)\s*\(", text)
+
+
+def make_shape(batch, n_q_heads, n_kv_heads, head_dim, max_nodes, prefix_cap, vocab, scale=0.0) -> JfShape:
+    return JfShape(batch, n_q_heads, n_kv_heads, head_dim, max_nodes, prefix_cap, vocab, scale)
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def jf_workspace_bytes(shape: JfShape) -> int:
+    return int(load().jf_workspace_bytes(ctypes.byref(shape)))
+
+
+def jf_status_string(code: int) -> str:
+    return load().jf_status_string(int(code)).decode()
+
+
+def jf_tree_attention(q, k_cache, v_cache, prefix_lens, tree_k, tree_v, parents, n_nodes, out,
+                      shape: JfShape, workspace, workspace_bytes: Optional[int] = None, status=None,
+                      stream=None, check: bool = True) -> int:
+    """Tree-causal attention over every node of every tree (see jf_tree.h)."""
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    rc = load().jf_tree_attention(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(prefix_lens), _ptr(tree_k),
+                                  _ptr(tree_v), _ptr(parents), _ptr(n_nodes), _ptr(out), ctypes.byref(shape),
+                                  _ptr(workspace), int(workspace_bytes), _ptr(status), _stream(stream))
+    if check and rc != JF_OK:
+        raise JfError("jf_tree_attention", rc)
+    return rc
+
+
+def jf_tree_verify(logits, tree_tokens, parents, n_nodes, accept_len_out, accept_path_out, argmax_out,
+                   shape: JfShape, max_depth: int, workspace, workspace_bytes: Optional[int] = None,
+                   status=None, stream=None, check: bool = True) -> int:
+    """Per-node argmax, then the longest accepted root path (see jf_tree.h)."""
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    rc = load().jf_tree_verify(_ptr(logits), _ptr(tree_tokens), _ptr(parents), _ptr(n_nodes),
+                               _ptr(accept_len_out), _ptr(accept_path_out), _ptr(argmax_out),
+                               ctypes.byref(shape), int(max_depth), _ptr(workspace), int(workspace_bytes),
+                               _ptr(status), _stream(stream))
+    if check and rc != JF_OK:
+        raise JfError("jf_tree_verify", rc)
+    return rc
+
+
+def jf_kernel_launch_count() -> int:
+    return int(load().jf_kernel_launch_count())
+
+
+def jf_trace_kernels(events, capacity: int) -> int:
+    """Arm per-kernel timing with a list of 2*capacity torch.cuda.Event
+    objects (enable_timing=True); pass None / 0 to disarm. The handle array
+    is kept alive by this module while armed."""
+    global _trace_keep
+    if not events or capacity <= 0:
+        _trace_keep = None
+        return load().jf_trace_kernels(None, 0)
+    arr = (ctypes.c_void_p * (2 * capacity))(*[e.cuda_event for e in events[: 2 * capacity]])
+    _trace_keep = arr
+    return load().jf_trace_kernels(ctypes.cast(arr, ctypes.c_void_p), capacity)
+
+
+_trace_keep = None
+
+
+def jf_trace_count() -> int:
+    return int(load().jf_trace_count())
+
+
+def jf_trace_name(k: int) -> Optional[str]:
+    r = load().jf_trace_name(int(k))
+    return None if r is None else r.decode()

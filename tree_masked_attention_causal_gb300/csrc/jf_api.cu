@@ -1,0 +1,264 @@
+// jf_api.cu - the C ABI (include/jf_tree.h): argument validation, workspace
+// layout, TMA tensor-map encoding and the stream-ordered kernel launches.
+//
+// Every check that needs no GPU runs before the first CUDA call, so bad
+// arguments are reported (and testable) on a machine without a GPU.
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "jf_common.cuh"
+
+namespace jf {
+
+// ------------------------------------------------------------- tracing
+namespace {
+std::atomic<uint64_t> g_launches{0};
+std::mutex g_trace_mu;
+jf_event_t *g_trace_events = nullptr;
+int32_t g_trace_capacity = 0;
+int32_t g_trace_count = 0;
+const char *g_trace_names[4096];
+thread_local bool t_open = false;
+
+// Inside stream capture a plain event record is only a dependency marker;
+// the external flag makes it a timing-capable event node of the graph.
+void record(jf_event_t ev, cudaStream_t s) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaStreamIsCapturing(s, &cs);
+    if (cs == cudaStreamCaptureStatusActive)
+        cudaEventRecordWithFlags(reinterpret_cast<cudaEvent_t>(ev), s, cudaEventRecordExternal);
+    else
+        cudaEventRecord(reinterpret_cast<cudaEvent_t>(ev), s);
+}
+}  // namespace
+
+void trace_begin(const char *name, cudaStream_t s) {
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    std::lock_guard<std::mutex> lk(g_trace_mu);
+    t_open = false;
+    if (g_trace_events && g_trace_count < g_trace_capacity) {
+        record(g_trace_events[2 * g_trace_count], s);
+        if (g_trace_count < 4096) g_trace_names[g_trace_count] = name;
+        t_open = true;
+    }
+}
+
+void trace_end(cudaStream_t s) {
+    std::lock_guard<std::mutex> lk(g_trace_mu);
+    if (t_open && g_trace_events && g_trace_count < g_trace_capacity) {
+        record(g_trace_events[2 * g_trace_count + 1], s);
+        ++g_trace_count;
+    }
+    t_open = false;
+}
+
+// -------------------------------------------------------- validation
+namespace {
+
+bool pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+
+// Shape checks shared by both entry points; `need_vocab` for verify.
+int32_t check_shape(const jf_shape *s, bool need_vocab, bool need_attn) {
+    if (!s) return JF_ERR_NULL;
+    if (s->batch < 1 || s->max_nodes < 1 || s->max_nodes > kMaxNodes) return JF_ERR_SHAPE;
+    if (need_attn) {
+        if (s->n_q_heads < 1 || s->n_kv_heads < 1 || s->n_q_heads % s->n_kv_heads) return JF_ERR_SHAPE;
+        const int G = s->n_q_heads / s->n_kv_heads;
+        if (!pow2(G) || G > kBM) return JF_ERR_SHAPE;
+        if (s->head_dim != 64 && s->head_dim != 128) return JF_ERR_SHAPE;
+        if (s->prefix_cap < 1) return JF_ERR_SHAPE;
+        if (!(s->scale >= 0.0f) || isinf(s->scale)) return JF_ERR_SHAPE;
+        // 32-bit index arithmetic in the kernels
+        if ((long long)s->batch * s->max_nodes * s->n_q_heads * s->head_dim > 0x7FFFFFFFll) return JF_ERR_SHAPE;
+        if ((long long)s->batch * s->n_kv_heads * s->prefix_cap > 0x7FFFFFFFll) return JF_ERR_SHAPE;
+    }
+    if (need_vocab) {
+        if (s->vocab < 8 || s->vocab % 8) return JF_ERR_SHAPE;
+        if ((long long)s->batch * s->max_nodes > 65535) return JF_ERR_SHAPE;   // grid.y
+    }
+    return JF_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Fully-defined shapes for the workspace: attention fields count only if
+// they are valid, vocab only if it is valid. Both entry points and
+// jf_workspace_bytes use this one layout, so their offsets always agree.
+bool attn_shape_ok(const jf_shape *s) { return check_shape(s, false, true) == JF_OK; }
+bool verify_shape_ok(const jf_shape *s) { return check_shape(s, true, false) == JF_OK; }
+
+Layout layout_of(const jf_shape *shape) {
+    jf_shape s = *shape;
+    if (!attn_shape_ok(&s)) { s.n_q_heads = 1; s.n_kv_heads = 1; s.head_dim = 64; s.prefix_cap = 1; }
+    if (!verify_shape_ok(&s)) s.vocab = 8;
+    return make_layout(s.batch, s.max_nodes, s.n_q_heads, s.n_kv_heads, s.head_dim, s.prefix_cap, s.vocab);
+}
+
+// ----------------------------------------------------- device queries
+int num_sms_cached(int dev) {
+    static int cache[64] = {0};
+    if (dev < 0 || dev >= 64) return 0;
+    if (cache[dev] == 0) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        cache[dev] = v;
+    }
+    return cache[dev];
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// 3-D bf16 map, 128-byte swizzle, zero fill out of bounds. dims/box are
+// innermost first; strides are the byte strides of dims 1 and 2.
+bool encode3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1, uint64_t s2,
+              uint32_t b0, uint32_t b1, uint32_t b2) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {d0, d1, d2};
+    const cuuint64_t strides[2] = {s1, s2};
+    const cuuint32_t box[3] = {b0, b1, b2};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+}  // namespace jf
+
+using namespace jf;
+
+extern "C" {
+
+JF_API size_t jf_workspace_bytes(const jf_shape *shape) {
+    if (!shape || (!attn_shape_ok(shape) && !verify_shape_ok(shape))) return 0;
+    return layout_of(shape).total;
+}
+
+JF_API const char *jf_status_string(int32_t code) {
+    switch (code) {
+        case JF_OK: return "ok";
+        case JF_ERR_NULL: return "a required pointer is NULL";
+        case JF_ERR_SHAPE: return "a size is outside the supported range";
+        case JF_ERR_ALIGN: return "a tensor pointer is not 16-byte aligned";
+        case JF_ERR_WORKSPACE: return "workspace too small";
+        case JF_ERR_CUDA: return "CUDA call or kernel launch failed";
+        default: break;
+    }
+    return "unknown status code";
+}
+
+JF_API int32_t jf_tree_attention(const void *q, const void *k_cache, const void *v_cache, const int32_t *prefix_lens,
+                                 const void *tree_k, const void *tree_v, const int32_t *parents,
+                                 const int32_t *n_nodes, void *out, const jf_shape *shape, void *workspace,
+                                 size_t workspace_bytes, int32_t *status, jf_stream_t stream) {
+    if (!q || !k_cache || !v_cache || !prefix_lens || !tree_k || !tree_v || !parents || !n_nodes || !out || !shape ||
+        !workspace)
+        return JF_ERR_NULL;
+    const int32_t sc = check_shape(shape, false, true);
+    if (sc != JF_OK) return sc;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(tree_k) || !aligned16(tree_v) ||
+        !aligned16(out) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return JF_ERR_ALIGN;
+    if (workspace_bytes < jf_workspace_bytes(shape)) return JF_ERR_WORKSPACE;
+
+    const Layout L = layout_of(shape);
+    const int B = shape->batch, N = shape->max_nodes, Hq = shape->n_q_heads, Hkv = shape->n_kv_heads;
+    const int D = shape->head_dim, Pcap = shape->prefix_cap;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return JF_ERR_CUDA;
+    const int sms = num_sms_cached(dev);
+    if (sms <= 0) return JF_ERR_CUDA;
+
+    AttnMaps maps;
+    const uint64_t e2 = 2;   // bytes per bf16
+    bool ok = encode3d(&maps.q, q, D, Hq, (uint64_t)B * N, e2 * D, e2 * D * Hq, 64, L.G, L.NB);
+    ok = ok && encode3d(&maps.k_cache, k_cache, D, Pcap, (uint64_t)B * Hkv, e2 * D, e2 * D * Pcap, 64, kBN, 1);
+    ok = ok && encode3d(&maps.v_cache, v_cache, D, Pcap, (uint64_t)B * Hkv, e2 * D, e2 * D * Pcap, 64, kBN, 1);
+    ok = ok && encode3d(&maps.tree_k, tree_k, D, Hkv, (uint64_t)B * N, e2 * D, e2 * D * Hkv, 64, 1, kBN);
+    ok = ok && encode3d(&maps.tree_v, tree_v, D, Hkv, (uint64_t)B * N, e2 * D, e2 * D * Hkv, 64, 1, kBN);
+    if (!ok) return JF_ERR_CUDA;
+
+    AttnArgs args;
+    args.prefix_lens = prefix_lens;
+    args.parents = parents;
+    args.n_nodes = n_nodes;
+    args.out = reinterpret_cast<__nv_bfloat16 *>(out);
+    args.ws = reinterpret_cast<uint8_t *>(workspace);
+    args.status = status;
+    const float scale = shape->scale > 0.f ? shape->scale : 1.0f / sqrtf((float)D);
+    args.scale_log2 = scale * 1.4426950408889634f;
+    args.num_ctas = sms < kMaxCtas ? sms : kMaxCtas;
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (launch_tree_prep(L, args, s) != cudaSuccess) return JF_ERR_CUDA;
+    if (launch_tree_attention(L, maps, args, s) != cudaSuccess) return JF_ERR_CUDA;
+    if (launch_split_combine(L, args, s) != cudaSuccess) return JF_ERR_CUDA;
+    return JF_OK;
+}
+
+JF_API int32_t jf_tree_verify(const void *logits, const int32_t *tree_tokens, const int32_t *parents,
+                              const int32_t *n_nodes, int32_t *accept_len_out, int32_t *accept_path_out,
+                              int32_t *argmax_out, const jf_shape *shape, int32_t max_depth, void *workspace,
+                              size_t workspace_bytes, int32_t *status, jf_stream_t stream) {
+    if (!logits || !tree_tokens || !parents || !n_nodes || !accept_len_out || !accept_path_out || !shape ||
+        !workspace)
+        return JF_ERR_NULL;
+    const int32_t sc = check_shape(shape, true, false);
+    if (sc != JF_OK) return sc;
+    if (max_depth < 0) return JF_ERR_SHAPE;
+    if (!aligned16(logits) || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return JF_ERR_ALIGN;
+    if (workspace_bytes < jf_workspace_bytes(shape)) return JF_ERR_WORKSPACE;
+    const Layout L = layout_of(shape);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t *ws = reinterpret_cast<uint8_t *>(workspace);
+    if (launch_argmax(L, reinterpret_cast<const __nv_bfloat16 *>(logits), n_nodes, ws, s) != cudaSuccess)
+        return JF_ERR_CUDA;
+    if (launch_accept_walk(L, tree_tokens, parents, n_nodes, accept_len_out, accept_path_out, argmax_out, max_depth,
+                           ws, status, s) != cudaSuccess)
+        return JF_ERR_CUDA;
+    return JF_OK;
+}
+
+JF_API uint64_t jf_kernel_launch_count(void) { return g_launches.load(); }
+
+JF_API int32_t jf_trace_kernels(jf_event_t *events, int32_t capacity) {
+    std::lock_guard<std::mutex> lk(g_trace_mu);
+    g_trace_events = (events && capacity > 0) ? events : nullptr;
+    g_trace_capacity = g_trace_events ? capacity : 0;
+    g_trace_count = 0;
+    return JF_OK;
+}
+
+JF_API int32_t jf_trace_count(void) {
+    std::lock_guard<std::mutex> lk(g_trace_mu);
+    return g_trace_count;
+}
+
+JF_API const char *jf_trace_name(int32_t k) {
+    std::lock_guard<std::mutex> lk(g_trace_mu);
+    if (k < 0 || k >= g_trace_count || k >= 4096) return nullptr;
+    return g_trace_names[k];
+}
+
+}  // extern "C"

@@ -1,0 +1,528 @@
+// jf_attn.cu - tree-causal attention forward on sm_103a (TMA + tcgen05/TMEM).
+//
+// What it computes ("JetFlow: Scaling Speculative Decoding with Parallel Tree
+// Drafting", blog, section "What JetFlow Does Differently"): all tree nodes in
+// one pass; node i attends to every prefix key and to the tree keys of its
+// ancestors and itself, never to siblings or descendants.
+//
+// Design
+//  * Query stacking (GQA). The G = Hq/Hkv query heads that share a KV head
+//    are stacked with the nodes into 128-row tiles: row r = node_local * G + g.
+//    One 3-D TMA box {64 d, G heads, 128/G nodes} loads such a tile straight
+//    from q[B, Nmax, Hq, d]. Each K/V tile in shared memory then serves all
+//    G heads at once.
+//  * Virtual key sequence. Per query tile, the keys are ceil(P/128) prefix
+//    tiles (from k_cache/v_cache) followed by ceil(n_hi/128) dense tree
+//    tiles (from tree_k/tree_v). Here n_hi is one past the highest node in
+//    the tile. Since parents[i] < i, no key of index > i is ever an ancestor.
+//    The ancestor bitmask (built by the prep kernel) masks the tree tiles in
+//    registers; a key-count bound masks the ragged last prefix tile.
+//  * Split-KV over a device-side plan. The prep kernel cuts each query tile's
+//    key tiles into splits of about total/num_CTAs tiles, and orders the
+//    items longest first. This persistent kernel pulls items from an atomic
+//    queue. A single-split tile is normalised and written as bf16 here; a
+//    split tile writes fp32 (O, m, l) partials that the combine kernel
+//    merges.
+//  * One CTA per SM, 6 warps:
+//      warp 4     TMA producer (Q once per item; K/V through rings of
+//                 NK / NV stages, 128-byte swizzle)
+//      warp 5     TMEM owner and MMA issuer: S = Q K^T (A and B from shared
+//                 memory) into one of two S buffers, then O += P V (A = P
+//                 from TMEM, B = V from shared memory, MN-major)
+//      warps 0-3  softmax: one thread per stacked row (TMEM lane); online
+//                 softmax in the exp2 domain with a lazy rescale of O only
+//                 when a row max grows by more than 2^8; P is written back
+//                 over its S buffer as bf16
+//    TMEM: S0 = columns [0,128), S1 = [128,256), O = [256, 256+d).
+//  * Rows of padding nodes are computed but never stored. V rows past the
+//    prefix length or past n_nodes are zeroed in shared memory before the
+//    PV MMA, so NaN in unused cache rows cannot reach an output.
+#include "jf_common.cuh"
+
+namespace jf {
+namespace {
+
+struct ItemInfo {
+    int32_t valid, skip, b, kh, qt, tb, te, t_pre, P, n, ns, slot;
+};
+
+template <int D>
+struct AttnCfg {
+    static constexpr int NK = D == 128 ? 3 : 4;             // K ring stages
+    static constexpr int NV = D == 128 ? 2 : 4;             // V ring stages
+    static constexpr int kBox = 64;                          // d per 128-byte swizzled box
+    static constexpr int kBoxes = D / kBox;
+    static constexpr uint32_t kQBytes = kBM * D * 2;
+    static constexpr uint32_t kTileBytes = kBN * D * 2;
+    static constexpr uint32_t q_off = 0;
+    static constexpr uint32_t k_off = q_off + kQBytes;
+    static constexpr uint32_t v_off = k_off + NK * kTileBytes;
+    static constexpr uint32_t bar_off = v_off + NV * kTileBytes;
+    // barrier indices
+    static constexpr int B_Q_FULL = 0, B_Q_EMPTY = 1, B_K_FULL = 2, B_K_EMPTY = B_K_FULL + NK,
+                         B_V_FULL = B_K_EMPTY + NK, B_V_EMPTY = B_V_FULL + NV, B_S_FULL = B_V_EMPTY + NV,
+                         B_P_FULL = B_S_FULL + 2, B_O_DONE = B_P_FULL + 2, B_ITEM_FULL = B_O_DONE + 1,
+                         B_ITEM_EMPTY = B_ITEM_FULL + 2, N_BARS = B_ITEM_EMPTY + 2;
+    static constexpr uint32_t item_off = bar_off + ((N_BARS * 8 + 15) / 16) * 16;
+    static constexpr uint32_t misc_off = item_off + 2 * sizeof(ItemInfo);
+    static constexpr uint32_t bytes = misc_off + 16;
+    static constexpr uint32_t smem_request = bytes + 1024;   // slack for 1024-byte alignment
+    static constexpr uint32_t kTmemCols = 512;
+    static constexpr uint32_t kColS0 = 0, kColO = 256;
+};
+
+constexpr int kThreads = 192;
+constexpr int kProducerWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr float kNegInf = -__builtin_huge_valf();
+
+// Wait that ignores the abort flag: used only to drain in-flight copies.
+__device__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
+    const unsigned long long t0 = globaltimer();
+    while (!mbar_try_wait(bar, parity))
+        if (globaltimer() - t0 > kTimeoutNs / 8) return false;
+    return true;
+}
+
+template <int D>
+__device__ __forceinline__ void producer_loop(const AttnMaps &maps, const Layout &L, const AttnArgs &a,
+                                              uint8_t *smem, uint32_t bars, ItemInfo *items_s,
+                                              volatile int *abort) {
+    using C = AttnCfg<D>;
+    const int lane = threadIdx.x & 31;
+    PlanHeader *hdr = reinterpret_cast<PlanHeader *>(a.ws + L.plan_off);
+    const Item *items = reinterpret_cast<const Item *>(a.ws + L.items_off);
+    const SeqInfo *seqs = reinterpret_cast<const SeqInfo *>(a.ws + L.seq_off);
+    const int2 *qtab = reinterpret_cast<const int2 *>(a.ws + L.qtab_off);
+    const uint32_t sbase = smem_u32(smem);
+    auto bar = [&](int i) { return bars + 8u * i; };
+    const int n_items = hdr->n_items;
+    int ic = 0, qc = 0, kc = 0, vc = 0;
+    bool ok = true;
+    while (ok) {
+        const int slot = ic & 1;
+        if (!mbar_wait(bar(C::B_ITEM_EMPTY + slot), ((ic >> 1) & 1) ^ 1, abort, a.status)) break;
+        int idx = 0;
+        if (lane == 0) idx = atomicAdd(&hdr->counter, 1);
+        idx = __shfl_sync(0xffffffffu, idx, 0);
+        ItemInfo info{};
+        if (idx < n_items) {
+            const Item it = items[idx];
+            const int per_b = L.Hkv * L.QT;
+            info.valid = 1;
+            info.b = it.qtile / per_b;
+            const int rem = it.qtile - info.b * per_b;
+            info.kh = rem / L.QT;
+            info.qt = rem - info.kh * L.QT;
+            info.tb = it.tile_begin;
+            info.te = it.tile_end;
+            const SeqInfo si = seqs[info.b];
+            info.skip = si.bad;
+            info.P = si.prefix_len;
+            info.n = si.n_nodes;
+            info.t_pre = ceil_div(si.prefix_len, kBN);
+            const int2 q = qtab[it.qtile];
+            info.ns = q.x;
+            info.slot = q.x > 1 ? q.y + it.split : -1;
+        }
+        if (lane == 0) {
+            items_s[slot] = info;
+            mbar_arrive(bar(C::B_ITEM_FULL + slot));
+        }
+        __syncwarp();
+        ++ic;
+        if (!info.valid) break;
+        if (info.skip) continue;
+        // Q tile: G heads x 128/G nodes, d in 64-wide swizzled boxes.
+        if (!mbar_wait(bar(C::B_Q_EMPTY), (qc & 1) ^ 1, abort, a.status)) break;
+        if (lane == 0) {
+            mbar_arrive_expect_tx(bar(C::B_Q_FULL), C::kQBytes);
+            for (int dc = 0; dc < C::kBoxes; ++dc)
+                tma_load_3d(sbase + C::q_off + dc * (kBM * 128), &maps.q, dc * 64, info.kh * L.G,
+                            info.b * L.Nmax + info.qt * L.NB, bar(C::B_Q_FULL));
+        }
+        ++qc;
+        for (int t = info.tb; t < info.te; ++t) {
+            const bool tree = t >= info.t_pre;
+            const int ks = kc % C::NK;
+            if (!mbar_wait(bar(C::B_K_EMPTY + ks), ((kc / C::NK) & 1) ^ 1, abort, a.status)) { ok = false; break; }
+            if (lane == 0) {
+                mbar_arrive_expect_tx(bar(C::B_K_FULL + ks), C::kTileBytes);
+                for (int dc = 0; dc < C::kBoxes; ++dc) {
+                    const uint32_t dst = sbase + C::k_off + ks * C::kTileBytes + dc * (kBN * 128);
+                    if (tree)
+                        tma_load_3d(dst, &maps.tree_k, dc * 64, info.kh, info.b * L.Nmax + (t - info.t_pre) * kBN,
+                                    bar(C::B_K_FULL + ks));
+                    else
+                        tma_load_3d(dst, &maps.k_cache, dc * 64, t * kBN, info.b * L.Hkv + info.kh,
+                                    bar(C::B_K_FULL + ks));
+                }
+            }
+            ++kc;
+            const int vs = vc % C::NV;
+            if (!mbar_wait(bar(C::B_V_EMPTY + vs), ((vc / C::NV) & 1) ^ 1, abort, a.status)) { ok = false; break; }
+            if (lane == 0) {
+                mbar_arrive_expect_tx(bar(C::B_V_FULL + vs), C::kTileBytes);
+                for (int dc = 0; dc < C::kBoxes; ++dc) {
+                    const uint32_t dst = sbase + C::v_off + vs * C::kTileBytes + dc * (kBN * 128);
+                    if (tree)
+                        tma_load_3d(dst, &maps.tree_v, dc * 64, info.kh, info.b * L.Nmax + (t - info.t_pre) * kBN,
+                                    bar(C::B_V_FULL + vs));
+                    else
+                        tma_load_3d(dst, &maps.v_cache, dc * 64, t * kBN, info.b * L.Hkv + info.kh,
+                                    bar(C::B_V_FULL + vs));
+                }
+            }
+            ++vc;
+        }
+    }
+    if (*abort && lane == 0) {
+        // Let every copy this warp started land before the CTA can exit.
+        if (qc > 0) mbar_wait_drain(bar(C::B_Q_FULL), (qc - 1) & 1);
+        for (int s = 0; s < C::NK; ++s)
+            if (kc > s) mbar_wait_drain(bar(C::B_K_FULL + s), (((kc - 1 - s) / C::NK)) & 1);
+        for (int s = 0; s < C::NV; ++s)
+            if (vc > s) mbar_wait_drain(bar(C::B_V_FULL + s), (((vc - 1 - s) / C::NV)) & 1);
+    }
+}
+
+template <int D>
+__device__ __forceinline__ void mma_loop(const Layout &L, const AttnArgs &a, uint8_t *smem, uint32_t bars,
+                                         const ItemInfo *items_s, uint32_t tmem, volatile int *abort) {
+    using C = AttnCfg<D>;
+    const int lane = threadIdx.x & 31;
+    const uint32_t sbase = smem_u32(smem);
+    auto bar = [&](int i) { return bars + 8u * i; };
+    constexpr uint32_t idesc_qk = idesc_bf16_f32(kBM, kBN, false, false);
+    constexpr uint32_t idesc_pv = idesc_bf16_f32(kBM, D, false, true);
+    int ic = 0, qc = 0, kc = 0, vc = 0, g = 0;
+
+    // O += P V for item-local tile jj whose S/P buffer is global tile index gj.
+    auto pv = [&](const ItemInfo &info, int jj, int gj) -> bool {
+        const int sb = gj & 1;
+        if (!mbar_wait(bar(C::B_P_FULL + sb), (gj >> 1) & 1, abort, a.status)) return false;
+        tc_fence_after();
+        const int vs = vc % C::NV;
+        if (!mbar_wait(bar(C::B_V_FULL + vs), (vc / C::NV) & 1, abort, a.status)) return false;
+        const uint32_t vtile = C::v_off + vs * C::kTileBytes;
+        // Rows past the prefix length / past n_nodes: zero them so that
+        // whatever the caller's memory holds there cannot reach O via 0 * NaN.
+        const int t = info.tb + jj;
+        int r0 = kBN;
+        if (t < info.t_pre) {
+            if (t == info.t_pre - 1 && (info.P % kBN) != 0) r0 = info.P % kBN;
+        } else {
+            const int left = info.n - (t - info.t_pre) * kBN;
+            r0 = left < 0 ? 0 : (left < kBN ? left : kBN);
+        }
+        if (r0 < kBN) {
+            const int chunks = (kBN - r0) * 8;            // 16-byte chunks per box
+            for (int dc = 0; dc < C::kBoxes; ++dc) {
+                uint4 *base = reinterpret_cast<uint4 *>(smem + vtile + dc * (kBN * 128) + r0 * 128);
+                for (int c = lane; c < chunks; c += 32) base[c] = make_uint4(0u, 0u, 0u, 0u);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+        }
+        if (lane == 0) {
+#pragma unroll
+            for (int kk = 0; kk < kBN / 16; ++kk) {
+                const uint64_t bdesc = sdesc_sw128(sbase + vtile + kk * 2048, kBN * 128, 1024);
+                mma_ts(tmem + C::kColO, tmem + C::kColS0 + sb * 128 + kk * 8, bdesc, idesc_pv,
+                       (jj > 0 || kk > 0) ? 1u : 0u);
+            }
+            mma_commit(bar(C::B_V_EMPTY + vs));
+            mma_commit(bar(C::B_O_DONE));
+        }
+        __syncwarp();
+        ++vc;
+        return true;
+    };
+
+    while (true) {
+        const int slot = ic & 1;
+        if (!mbar_wait(bar(C::B_ITEM_FULL + slot), (ic >> 1) & 1, abort, a.status)) break;
+        const ItemInfo info = items_s[slot];
+        ++ic;
+        if (!info.valid) break;
+        if (info.skip) {
+            if (lane == 0) mbar_arrive(bar(C::B_ITEM_EMPTY + slot));
+            continue;
+        }
+        if (!mbar_wait(bar(C::B_Q_FULL), qc & 1, abort, a.status)) break;
+        ++qc;
+        tc_fence_after();
+        const int nt = info.te - info.tb;
+        bool fail = false;
+        for (int j = 0; j < nt; ++j) {
+            const int ks = kc % C::NK;
+            if (!mbar_wait(bar(C::B_K_FULL + ks), (kc / C::NK) & 1, abort, a.status)) { fail = true; break; }
+            tc_fence_after();
+            const int sb = g & 1;
+            if (lane == 0) {
+                const uint32_t ktile = sbase + C::k_off + ks * C::kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint64_t adesc = sdesc_sw128(sbase + C::q_off + (kk >> 2) * (kBM * 128) + (kk & 3) * 32, 16, 1024);
+                    const uint64_t bdesc = sdesc_sw128(ktile + (kk >> 2) * (kBN * 128) + (kk & 3) * 32, 16, 1024);
+                    mma_ss(tmem + C::kColS0 + sb * 128, adesc, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(bar(C::B_S_FULL + sb));
+                mma_commit(bar(C::B_K_EMPTY + ks));
+                if (j == nt - 1) mma_commit(bar(C::B_Q_EMPTY));
+            }
+            __syncwarp();
+            ++kc;
+            ++g;
+            if (j > 0 && !pv(info, j - 1, g - 2)) { fail = true; break; }
+        }
+        if (fail || !pv(info, nt - 1, g - 1)) break;
+        if (lane == 0) mbar_arrive(bar(C::B_ITEM_EMPTY + slot));
+    }
+}
+
+template <int D>
+__device__ __forceinline__ void softmax_loop(const Layout &L, const AttnArgs &a, uint32_t bars,
+                                             const ItemInfo *items_s, uint32_t tmem, volatile int *abort) {
+    using C = AttnCfg<D>;
+    const int r = threadIdx.x;            // stacked row = TMEM lane
+    const int warp = r >> 5, lane = r & 31;
+    auto bar = [&](int i) { return bars + 8u * i; };
+    const uint32_t t_row = tmem + ((uint32_t)(warp * 32) << 16);
+    const uint32_t t_o = t_row + C::kColO;
+    const uint32_t *masks = reinterpret_cast<const uint32_t *>(a.ws + L.mask_off);
+    float *opart = reinterpret_cast<float *>(a.ws + L.opart_off);
+    float2 *mlpart = reinterpret_cast<float2 *>(a.ws + L.ml_off);
+    const float sl2 = a.scale_log2;
+    int ic = 0, g = 0;
+
+    while (true) {
+        const int slot = ic & 1;
+        if (!mbar_wait(bar(C::B_ITEM_FULL + slot), (ic >> 1) & 1, abort, a.status)) break;
+        const ItemInfo info = items_s[slot];
+        ++ic;
+        if (!info.valid) break;
+        if (info.skip) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(C::B_ITEM_EMPTY + slot));
+            continue;
+        }
+        const int node = info.qt * L.NB + r / L.G;
+        const int head = info.kh * L.G + r % L.G;
+        const bool row_valid = node < info.n;
+        const uint32_t *mrow = masks + ((size_t)info.b * L.Nmax + (row_valid ? node : 0)) * L.W4;
+        float m_run = kNegInf, l_run = 0.f;
+        const int nt = info.te - info.tb;
+        bool fail = false;
+        for (int j = 0; j < nt; ++j) {
+            const int t = info.tb + j;
+            const int sb = g & 1;
+            const bool tree = t >= info.t_pre;
+            uint4 mw = make_uint4(0u, 0u, 0u, 0u);
+            if (tree && row_valid) mw = *reinterpret_cast<const uint4 *>(mrow + 4 * (t - info.t_pre));
+            if (!mbar_wait(bar(C::B_S_FULL + sb), (g >> 1) & 1, abort, a.status)) { fail = true; break; }
+            tc_fence_after();
+            float s[kBN];
+#pragma unroll
+            for (int c = 0; c < kBN / 32; ++c) {
+                uint32_t v[32];
+                tmem_ld32(t_row + C::kColS0 + sb * 128 + c * 32, v);
+#pragma unroll
+                for (int k = 0; k < 32; ++k) s[c * 32 + k] = __uint_as_float(v[k]);
+            }
+            if (tree) {
+                const uint32_t w4[4] = {mw.x, mw.y, mw.z, mw.w};
+#pragma unroll
+                for (int c = 0; c < kBN; ++c)
+                    if (!((w4[c >> 5] >> (c & 31)) & 1u)) s[c] = kNegInf;
+            } else if (t == info.t_pre - 1) {
+                const int lim = info.P - t * kBN;        // valid keys in the last prefix tile
+                if (lim < kBN) {
+#pragma unroll
+                    for (int c = 0; c < kBN; ++c)
+                        if (c >= lim) s[c] = kNegInf;
+                }
+            }
+            float mx = s[0];
+#pragma unroll
+            for (int c = 1; c < kBN; ++c) mx = fmaxf(mx, s[c]);
+            const float mt = mx * sl2;
+            bool waited_o = false;
+            if (j == 0) {
+                m_run = mt;
+            } else {
+                const float m_new = fmaxf(m_run, mt);
+                const bool need = m_new > m_run + 8.0f;
+                if (__any_sync(0xffffffffu, need)) {
+                    // O holds PV of the previous tile: wait for it, then rescale.
+                    if (!mbar_wait(bar(C::B_O_DONE), (g - 1) & 1, abort, a.status)) { fail = true; break; }
+                    waited_o = true;
+                    tc_fence_after();
+                    const float alpha = need ? ex2_approx(m_run - m_new) : 1.0f;
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t v[32];
+                        tmem_ld32(t_o + c * 32, v);
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * alpha);
+                        tmem_st32(t_o + c * 32, v);
+                    }
+                    if (need) {
+                        l_run *= alpha;
+                        m_run = m_new;
+                    }
+                }
+            }
+            const float neg_m = (m_run == kNegInf) ? 0.f : -m_run;
+            float sum = 0.f;
+#pragma unroll
+            for (int c = 0; c < kBN; ++c) {
+                s[c] = ex2_approx(fmaf(s[c], sl2, neg_m));
+                sum += s[c];
+            }
+            l_run += sum;
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                uint32_t v[32];
+#pragma unroll
+                for (int k = 0; k < 32; ++k) v[k] = pack_bf16x2(s[c * 64 + 2 * k], s[c * 64 + 2 * k + 1]);
+                tmem_st32(t_row + C::kColS0 + sb * 128 + c * 32, v);
+            }
+            tmem_wait_st();
+            // Keep PV of the previous tile retired before P of this one is
+            // released: the epilogue's single o_done wait then stays within
+            // one phase of the barrier.
+            if (j > 0 && !waited_o) {
+                if (!mbar_wait(bar(C::B_O_DONE), (g - 1) & 1, abort, a.status)) { fail = true; break; }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(C::B_P_FULL + sb));
+            ++g;
+        }
+        if (fail) break;
+        // Epilogue: wait for the last PV of this item.
+        if (!mbar_wait(bar(C::B_O_DONE), (g - 1) & 1, abort, a.status)) break;
+        tc_fence_after();
+        if (info.ns <= 1) {
+            const float inv_l = 1.0f / l_run;
+            __nv_bfloat16 *dst = a.out + (((size_t)info.b * L.Nmax + node) * L.Hq + head) * D;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t v[32];
+                tmem_ld32(t_o + c * 32, v);
+                if (row_valid) {
+                    uint4 *d4 = reinterpret_cast<uint4 *>(dst + c * 32);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        uint4 w;
+                        w.x = pack_bf16x2(__uint_as_float(v[8 * k + 0]) * inv_l, __uint_as_float(v[8 * k + 1]) * inv_l);
+                        w.y = pack_bf16x2(__uint_as_float(v[8 * k + 2]) * inv_l, __uint_as_float(v[8 * k + 3]) * inv_l);
+                        w.z = pack_bf16x2(__uint_as_float(v[8 * k + 4]) * inv_l, __uint_as_float(v[8 * k + 5]) * inv_l);
+                        w.w = pack_bf16x2(__uint_as_float(v[8 * k + 6]) * inv_l, __uint_as_float(v[8 * k + 7]) * inv_l);
+                        d4[k] = w;
+                    }
+                }
+            }
+        } else {
+            float *dst = opart + ((size_t)info.slot * kBM + r) * D;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t v[32];
+                tmem_ld32(t_o + c * 32, v);
+                float4 *d4 = reinterpret_cast<float4 *>(dst + c * 32);
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    d4[k] = make_float4(__uint_as_float(v[4 * k]), __uint_as_float(v[4 * k + 1]),
+                                        __uint_as_float(v[4 * k + 2]), __uint_as_float(v[4 * k + 3]));
+            }
+            mlpart[(size_t)info.slot * kBM + r] = make_float2(m_run, l_run);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(C::B_ITEM_EMPTY + slot));
+    }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    tree_attention_kernel(const __grid_constant__ AttnMaps maps, const Layout L, const AttnArgs a) {
+    using C = AttnCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int warp = threadIdx.x >> 5;
+    const uint32_t bars = smem_u32(smem + C::bar_off);
+    ItemInfo *items_s = reinterpret_cast<ItemInfo *>(smem + C::item_off);
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + C::misc_off);
+    volatile int *abort = reinterpret_cast<volatile int *>(smem + C::misc_off + 4);
+
+    if (threadIdx.x == 0) {
+        auto init = [&](int i, uint32_t count) { mbar_init(bars + 8u * i, count); };
+        init(C::B_Q_FULL, 1);
+        init(C::B_Q_EMPTY, 1);
+        for (int s = 0; s < C::NK; ++s) { init(C::B_K_FULL + s, 1); init(C::B_K_EMPTY + s, 1); }
+        for (int s = 0; s < C::NV; ++s) { init(C::B_V_FULL + s, 1); init(C::B_V_EMPTY + s, 1); }
+        for (int s = 0; s < 2; ++s) {
+            init(C::B_S_FULL + s, 1);
+            init(C::B_P_FULL + s, 4);           // one arrival per softmax warp
+            init(C::B_ITEM_FULL + s, 1);
+            init(C::B_ITEM_EMPTY + s, 5);       // MMA warp + 4 softmax warps
+        }
+        init(C::B_O_DONE, 1);
+        *abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == kProducerWarp && (threadIdx.x & 31) == 0) {
+        tma_prefetch_map(&maps.q);
+        tma_prefetch_map(&maps.k_cache);
+        tma_prefetch_map(&maps.v_cache);
+        tma_prefetch_map(&maps.tree_k);
+        tma_prefetch_map(&maps.tree_v);
+    }
+    if (warp == kMmaWarp) tmem_alloc(smem_u32(tmem_holder), C::kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+
+    if (warp == kProducerWarp)
+        producer_loop<D>(maps, L, a, smem, bars, items_s, abort);
+    else if (warp == kMmaWarp)
+        mma_loop<D>(L, a, smem, bars, items_s, tmem, abort);
+    else
+        softmax_loop<D>(L, a, bars, items_s, tmem, abort);
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == kMmaWarp) tmem_dealloc(tmem, C::kTmemCols);
+}
+
+template <int D>
+cudaError_t launch_d(const Layout &L, const AttnMaps &m, const AttnArgs &a, cudaStream_t s) {
+    using C = AttnCfg<D>;
+    static_assert(C::smem_request <= 227 * 1024, "shared memory budget");
+    static int configured_device = -1;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (configured_device != dev) {
+        e = cudaFuncSetAttribute(tree_attention_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)C::smem_request);
+        if (e != cudaSuccess) return e;
+        configured_device = dev;
+    }
+    trace_begin("tree_attention", s);
+    tree_attention_kernel<D><<<a.num_ctas, kThreads, C::smem_request, s>>>(m, L, a);
+    e = cudaGetLastError();
+    trace_end(s);
+    return e;
+}
+
+}  // namespace
+
+cudaError_t launch_tree_attention(const Layout &L, const AttnMaps &m, const AttnArgs &a, cudaStream_t s) {
+    return L.D == 128 ? launch_d<128>(L, m, a, s) : launch_d<64>(L, m, a, s);
+}
+
+}  // namespace jf

@@ -1,0 +1,332 @@
+// jf_common.cuh - shared definitions of the sm_103a kernels: tile sizes, the
+// workspace layout, and inline-PTX wrappers for mbarrier, TMA (cp.async.bulk
+// .tensor) and the 5th-generation tensor core (tcgen05 + TMEM).
+//
+// The PTX wrappers follow the PTX ISA's descriptions of these instructions.
+// Every wait on an mbarrier is bounded: after kTimeoutNs it sets
+// JF_STATUS_TIMEOUT, raises the CTA's abort flag and returns false, so no
+// kernel can spin forever.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/jf_tree.h"
+
+namespace jf {
+
+// ---------------------------------------------------------------- tiling
+constexpr int kBM = 128;          // stacked query rows per tile (nodes x GQA group)
+constexpr int kBN = 128;          // keys per KV tile
+constexpr int kMaxNodes = 256;    // tree slots per sequence
+constexpr int kMaxCtas = 256;     // cap on the persistent attention grid
+constexpr int kMinTilesPerSplit = 2;
+constexpr int kArgmaxThreads = 256;
+constexpr int kArgmaxVecs = 8;    // 16-byte vectors per thread per chunk
+constexpr int kArgmaxChunk = kArgmaxThreads * kArgmaxVecs * 8;  // bf16 elements per CTA
+constexpr unsigned long long kTimeoutNs = 2000000000ull;        // 2 s per wait
+
+__host__ __device__ constexpr int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// One tree-attention work item: tiles [tile_begin, tile_end) of the virtual
+// key sequence (prefix tiles first, then tree tiles) for one query tile.
+struct Item {
+    int32_t qtile;       // (b * Hkv + kh) * QT + qt
+    int32_t tile_begin;
+    int32_t tile_end;
+    int32_t split;       // index of this split within the query tile
+};
+
+struct SeqInfo {         // per sequence, written by the prep kernel
+    int32_t prefix_len;
+    int32_t n_nodes;
+    int32_t bad;
+    int32_t pad;
+};
+
+struct PlanHeader {
+    int32_t n_items;
+    int32_t counter;     // dynamic work queue cursor
+    int32_t tiles_per_split;
+    int32_t total_tiles;
+};
+
+// Byte offsets of the workspace regions. Attention regions come first, then
+// the verify region; the two never overlap.
+struct Layout {
+    int32_t B, Nmax, Hq, Hkv, G, D, Pcap, V;
+    int32_t QT;          // query tiles per (sequence, kv head)
+    int32_t NB;          // nodes per query tile = kBM / G
+    int32_t W4;          // mask words per node (multiple of 4)
+    int32_t n_qtiles;    // B * Hkv * QT
+    int32_t max_items;
+    int32_t chunks;      // argmax chunks per logits row
+    size_t mask_off, seq_off, plan_off, qtab_off, items_off, ml_off, opart_off;
+    size_t amp_off;
+    size_t total;
+};
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// The layout depends only on the shape (never on prefix lengths or trees).
+inline Layout make_layout(int B, int Nmax, int Hq, int Hkv, int D, int Pcap, int V) {
+    Layout L{};
+    L.B = B; L.Nmax = Nmax; L.Hq = Hq; L.Hkv = Hkv; L.G = Hq / Hkv; L.D = D; L.Pcap = Pcap; L.V = V;
+    L.NB = kBM / L.G;
+    L.QT = ceil_div(Nmax, L.NB);
+    L.W4 = 4 * ceil_div(Nmax, kBN);
+    L.n_qtiles = B * Hkv * L.QT;
+    L.max_items = L.n_qtiles + kMaxCtas;
+    L.chunks = V > 0 ? ceil_div(V, kArgmaxChunk) : 1;
+    size_t off = 0;
+    auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 256); return o; };
+    L.mask_off = take(sizeof(uint32_t) * (size_t)B * Nmax * L.W4);
+    L.seq_off = take(sizeof(SeqInfo) * (size_t)B);
+    L.plan_off = take(sizeof(PlanHeader));
+    L.qtab_off = take(sizeof(int2) * (size_t)L.n_qtiles);
+    L.items_off = take(sizeof(Item) * (size_t)L.max_items);
+    L.ml_off = take(sizeof(float2) * (size_t)L.max_items * kBM);
+    L.opart_off = take(sizeof(float) * (size_t)L.max_items * kBM * D);
+    L.amp_off = take(sizeof(int2) * (size_t)B * Nmax * L.chunks);
+    L.total = off;
+    return L;
+}
+
+// ------------------------------------------------------------- PTX: misc
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long globaltimer() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void set_status(int32_t *status, int32_t flag) {
+    if (status) atomicOr(status, flag);
+}
+
+// ------------------------------------------------------------ mbarrier
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for the phase of parity `parity` to complete. Returns false
+// (and raises *abort) if the CTA aborted or the wait ran past kTimeoutNs.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort,
+                                          int32_t *status) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort) return false;
+        if (globaltimer() - t0 > kTimeoutNs) {
+            *abort = 1;
+            set_status(status, JF_STATUS_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+// ----------------------------------------------------------------- TMA
+__device__ __forceinline__ void tma_prefetch_map(const void *map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
+}
+
+// 3-D tiled bulk tensor load global -> shared, completing on `bar`.
+// Coordinates are element indices, innermost first.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *map, int c0, int c1, int c2,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+        : "memory");
+}
+
+// Generic-proxy shared-memory writes -> visible to the async proxy (TMA/MMA).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// --------------------------------------------------- tcgen05 and TMEM
+__device__ __forceinline__ void tmem_alloc(uint32_t holder_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(holder_smem),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle (sm_100 family layout:
+// start>>4 in bits 0-13, leading byte offset>>4 in 16-29, stride byte
+// offset>>4 in 32-45, descriptor version 1 in 46-47, swizzle mode 2 =
+// 128B in 61-63).
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// Instruction descriptor for kind::f16 with bf16 A/B and fp32 accumulate:
+// D format bits 4-5 (1 = f32), A format 7-9 and B format 10-12 (1 = bf16),
+// A/B major bits 15/16 (0 = K-major, 1 = MN-major), N>>3 in 17-22,
+// M>>4 in 24-28.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn, bool b_mn) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
+           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, one CTA.
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                       uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem], one CTA.
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                       uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive once on `bar` when every tcgen05 operation this thread issued so
+// far has completed.
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+#define JF_R8(i) "=r"(v[i + 0]), "=r"(v[i + 1]), "=r"(v[i + 2]), "=r"(v[i + 3]), \
+                 "=r"(v[i + 4]), "=r"(v[i + 5]), "=r"(v[i + 6]), "=r"(v[i + 7])
+#define JF_W8(i) "r"(v[i + 0]), "r"(v[i + 1]), "r"(v[i + 2]), "r"(v[i + 3]), \
+                 "r"(v[i + 4]), "r"(v[i + 5]), "r"(v[i + 6]), "r"(v[i + 7])
+
+// Load 32 consecutive fp32 columns of this thread's TMEM lane (32x32b
+// shape: warp w of a warpgroup reads lanes 32w..32w+31) and wait for them.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : JF_R8(0), JF_R8(8), JF_R8(16), JF_R8(24)
+        : "r"(taddr)
+        : "memory");
+}
+
+// Store 32 consecutive 32-bit columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        JF_W8(0), JF_W8(8), JF_W8(16), JF_W8(24)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+#undef JF_R8
+#undef JF_W8
+
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);   // .x (low half) = lo
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// ------------------------------------------------------ kernel launchers
+// (defined in the .cu files, called by the C ABI in jf_api.cu)
+struct AttnMaps {
+    CUtensorMap q, k_cache, v_cache, tree_k, tree_v;
+};
+
+struct AttnArgs {
+    const int32_t *prefix_lens;
+    const int32_t *parents;
+    const int32_t *n_nodes;
+    __nv_bfloat16 *out;
+    uint8_t *ws;
+    int32_t *status;
+    float scale_log2;
+    int32_t num_ctas;    // persistent grid size of the attention kernel
+};
+
+cudaError_t launch_tree_prep(const Layout &L, const AttnArgs &a, cudaStream_t s);
+cudaError_t launch_tree_attention(const Layout &L, const AttnMaps &m, const AttnArgs &a,
+                                  cudaStream_t s);
+cudaError_t launch_split_combine(const Layout &L, const AttnArgs &a, cudaStream_t s);
+cudaError_t launch_argmax(const Layout &L, const __nv_bfloat16 *logits, const int32_t *n_nodes,
+                          uint8_t *ws, cudaStream_t s);
+cudaError_t launch_accept_walk(const Layout &L, const int32_t *tokens, const int32_t *parents,
+                               const int32_t *n_nodes, int32_t *accept_len, int32_t *accept_path,
+                               int32_t *argmax_out, int32_t max_depth, uint8_t *ws, int32_t *status,
+                               cudaStream_t s);
+
+// Host-side launch bookkeeping (jf_api.cu): counts launches and records the
+// armed trace events around each one.
+void trace_begin(const char *name, cudaStream_t s);
+void trace_end(cudaStream_t s);
+
+}  // namespace jf

@@ -1,0 +1,222 @@
+// jf_verify.cu - greedy tree verification on sm_103a.
+//
+// The paper's section 2.1 "Background": the target verifies the drafted
+// tokens in parallel and accepts the longest prefix that agrees with its own
+// predictions. In a tree, node c is accepted iff its parent p is accepted and
+// tokens[c] == argmax(logits[p]); the result is the deepest accepted node.
+//
+//  argmax_chunk_kernel  HBM-bound scan of the logits. Each CTA owns a chunk
+//                       of 16384 bf16 of one row: 8 independent 128-bit
+//                       loads per thread in flight, a packed bf16x2 max
+//                       (NaN-propagating) over them, a block max, then the
+//                       first position holding that max, found in registers
+//                       (no second pass over memory). The (max, index) pair
+//                       of every chunk goes to the workspace.
+//  accept_walk_kernel   one block per sequence, one thread per node: merges
+//                       the chunk results in index order (ties -> lowest
+//                       index, first NaN wins), checks each edge against the
+//                       parent's argmax, walks each node's root path, and
+//                       reduces (depth, -index) to the deepest accepted node.
+#include "jf_common.cuh"
+
+namespace jf {
+namespace {
+
+__device__ __forceinline__ bool is_nan_f(float x) { return x != x; }
+
+// Max that propagates NaN (a NaN beats every number).
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+    return is_nan_f(a) ? a : (is_nan_f(b) ? b : fmaxf(a, b));
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint32_t hmax2_nan(uint32_t a, uint32_t b) {
+    __nv_bfloat162 x = *reinterpret_cast<__nv_bfloat162 *>(&a);
+    __nv_bfloat162 y = *reinterpret_cast<__nv_bfloat162 *>(&b);
+    __nv_bfloat162 z = __hmax2_nan(x, y);
+    return *reinterpret_cast<uint32_t *>(&z);
+}
+
+__global__ void __launch_bounds__(kArgmaxThreads)
+    argmax_chunk_kernel(const __nv_bfloat16 *__restrict__ logits, const int32_t *__restrict__ n_nodes,
+                        int2 *__restrict__ part, int Nmax, int V, int chunks) {
+    const int row = blockIdx.y;
+    const int b = row / Nmax, i = row - b * Nmax;
+    const int n = n_nodes[b];
+    if (n < 1 || n > Nmax || i >= n) return;                 // padding row
+    const int tid = threadIdx.x;
+    const int e0 = blockIdx.x * kArgmaxChunk;
+    const int e1 = min(V, e0 + kArgmaxChunk);
+    const uint4 *src = reinterpret_cast<const uint4 *>(logits + (size_t)row * V + e0);
+    const int nvec = (e1 - e0) >> 3;                         // V % 8 == 0
+    uint4 v[kArgmaxVecs];
+#pragma unroll
+    for (int u = 0; u < kArgmaxVecs; ++u) {
+        const int k = tid + u * kArgmaxThreads;
+        v[u] = k < nvec ? ld_stream(src + k) : make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
+    }
+    uint32_t m2 = 0xFF80FF80u;                               // (-inf, -inf)
+#pragma unroll
+    for (int u = 0; u < kArgmaxVecs; ++u) {
+        m2 = hmax2_nan(m2, v[u].x);
+        m2 = hmax2_nan(m2, v[u].y);
+        m2 = hmax2_nan(m2, v[u].z);
+        m2 = hmax2_nan(m2, v[u].w);
+    }
+    float m = fmax_nan(bf16_lo(m2), bf16_hi(m2));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmax_nan(m, __shfl_xor_sync(0xffffffffu, m, o));
+    __shared__ float sm[kArgmaxThreads / 32];
+    __shared__ int si[kArgmaxThreads / 32];
+    const int warp = tid >> 5, lane = tid & 31;
+    if (lane == 0) sm[warp] = m;
+    __syncthreads();
+    float M = sm[0];
+#pragma unroll
+    for (int w = 1; w < kArgmaxThreads / 32; ++w) M = fmax_nan(M, sm[w]);
+    // first element equal to M (+0 == -0; NaN matches NaN), in element order
+    int first = 0x7FFFFFFF;
+    const bool M_nan = is_nan_f(M);
+    if (fmax_nan(bf16_lo(m2), bf16_hi(m2)) == M || (M_nan && is_nan_f(fmax_nan(bf16_lo(m2), bf16_hi(m2))))) {
+#pragma unroll
+        for (int u = 0; u < kArgmaxVecs; ++u) {
+            const int k = tid + u * kArgmaxThreads;
+            if (k >= nvec || first != 0x7FFFFFFF) continue;
+            const uint32_t w4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const float x = (q & 1) ? bf16_hi(w4[q >> 1]) : bf16_lo(w4[q >> 1]);
+                const bool hit = M_nan ? is_nan_f(x) : (x == M);
+                if (hit && first == 0x7FFFFFFF) first = e0 + 8 * k + q;
+            }
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) first = min(first, __shfl_xor_sync(0xffffffffu, first, o));
+    if (lane == 0) si[warp] = first;
+    __syncthreads();
+    if (tid == 0) {
+        int f = si[0];
+#pragma unroll
+        for (int w = 1; w < kArgmaxThreads / 32; ++w) f = min(f, si[w]);
+        part[(size_t)row * chunks + blockIdx.x] = make_int2(__float_as_int(M), f);
+    }
+}
+
+__global__ void __launch_bounds__(kMaxNodes)
+    accept_walk_kernel(const int2 *__restrict__ part, const int32_t *__restrict__ tokens,
+                       const int32_t *__restrict__ parents, const int32_t *__restrict__ n_nodes,
+                       int32_t *__restrict__ accept_len, int32_t *__restrict__ accept_path,
+                       int32_t *__restrict__ argmax_out, int Nmax, int chunks, int max_depth,
+                       int32_t *status) {
+    __shared__ int par[kMaxNodes];
+    __shared__ int am[kMaxNodes];
+    __shared__ unsigned char edge_ok[kMaxNodes];
+    __shared__ int red[kMaxNodes / 32];
+    const int b = blockIdx.x, i = threadIdx.x;
+    const int n = n_nodes[b];
+    const bool n_ok = n >= 1 && n <= Nmax;
+    // merge chunk results in chunk order
+    int a = -1;
+    if (n_ok && i < n) {
+        const int2 *pr = part + ((size_t)b * Nmax + i) * chunks;
+        float best = __int_as_float(pr[0].x);
+        a = pr[0].y;
+        for (int c = 1; c < chunks; ++c) {
+            if (is_nan_f(best)) break;
+            const float x = __int_as_float(pr[c].x);
+            if (is_nan_f(x) || x > best) {
+                best = x;
+                a = pr[c].y;
+            }
+        }
+    }
+    if (i < kMaxNodes) am[i] = a;
+    if (argmax_out && i < Nmax) argmax_out[(size_t)b * Nmax + i] = a;
+    int p = -1;
+    bool bad = !n_ok;
+    if (n_ok && i < n) {
+        p = parents[(size_t)b * Nmax + i];
+        bad = (i == 0) ? (p != -1) : (p < 0 || p >= i);
+    }
+    par[i] = p;
+    bad = __syncthreads_or(bad);
+    int32_t *path = accept_path + (size_t)b * (max_depth + 1);
+    if (bad) {
+        for (int k = i; k <= max_depth; k += blockDim.x) path[k] = -1;
+        if (i == 0) {
+            accept_len[b] = 0;
+            set_status(status, JF_STATUS_BAD_TREE);
+        }
+        return;
+    }
+    edge_ok[i] = (i < n) && (i == 0 || tokens[(size_t)b * Nmax + i] == am[p]);
+    __syncthreads();
+    // accepted iff every edge on the root path agrees
+    int key = -1;
+    if (i < n) {
+        bool acc = true;
+        int depth = 0;
+        for (int j = i; j > 0; j = par[j]) {
+            acc = acc && edge_ok[j];
+            ++depth;
+        }
+        if (acc) key = (depth << 16) | (0xFFFF - i);          // deepest, then lowest index
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) key = max(key, __shfl_xor_sync(0xffffffffu, key, o));
+    if ((i & 31) == 0) red[i >> 5] = key;
+    __syncthreads();
+    if (i == 0) {
+        int k = red[0];
+        for (int w = 1; w < (int)(blockDim.x >> 5); ++w) k = max(k, red[w]);
+        const int best = 0xFFFF - (k & 0xFFFF);
+        const int depth = k >> 16;
+        const int len = min(depth, max_depth) + 1;
+        for (int s = len; s <= max_depth; ++s) path[s] = -1;
+        int node = best;
+        for (int d = depth; d >= 0; --d) {
+            if (d < len) path[d] = node;
+            node = par[node];
+        }
+        accept_len[b] = len;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_argmax(const Layout &L, const __nv_bfloat16 *logits, const int32_t *n_nodes, uint8_t *ws,
+                          cudaStream_t s) {
+    trace_begin("argmax_chunk", s);
+    dim3 grid(L.chunks, L.B * L.Nmax);
+    argmax_chunk_kernel<<<grid, kArgmaxThreads, 0, s>>>(logits, n_nodes, reinterpret_cast<int2 *>(ws + L.amp_off),
+                                                        L.Nmax, L.V, L.chunks);
+    cudaError_t e = cudaGetLastError();
+    trace_end(s);
+    return e;
+}
+
+cudaError_t launch_accept_walk(const Layout &L, const int32_t *tokens, const int32_t *parents,
+                               const int32_t *n_nodes, int32_t *accept_len, int32_t *accept_path,
+                               int32_t *argmax_out, int32_t max_depth, uint8_t *ws, int32_t *status,
+                               cudaStream_t s) {
+    trace_begin("accept_walk", s);
+    accept_walk_kernel<<<L.B, kMaxNodes, 0, s>>>(reinterpret_cast<const int2 *>(ws + L.amp_off), tokens, parents,
+                                                 n_nodes, accept_len, accept_path, argmax_out, L.Nmax, L.chunks,
+                                                 max_depth, status);
+    cudaError_t e = cudaGetLastError();
+    trace_end(s);
+    return e;
+}
+
+}  // namespace jf
