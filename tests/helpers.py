@@ -87,13 +87,30 @@ def valid_rows(inp):
     return rows
 
 
-def assert_attention_close(got, ref, rows, what=""):
-    """Element-wise comparison on the given (b, i) rows (all heads, all d)."""
+def half_ulp_bf16(x):
+    """Half a bf16 ulp at |x|: the representation error of the bf16 output
+    format (7 stored mantissa bits), 2^(floor(log2|x|) - 8)."""
+    ax = np.maximum(np.abs(x), 2.0 ** -126)
+    return np.ldexp(1.0, np.floor(np.log2(ax)).astype(np.int64) - 8)
+
+
+def assert_attention_close(got, ref, rows, what="", strict=False):
+    """Element-wise comparison on the given (b, i) rows (all heads, all d).
+
+    The bound is max-abs 1e-2 and mean-abs 1e-3 against fp64. The output is
+    bf16 by contract, and a row that sees only a few keys can have outputs
+    above 1 in magnitude, where bf16's half-ulp alone is 0.004-0.016. So
+    unless `strict`, each element may also differ by half a bf16 ulp of its
+    reference value. The five workloads run strict.
+    """
     g = np.stack([got[b, i] for b, i in rows]).astype(np.float64)
     r = np.stack([ref[b, i] for b, i in rows])
     assert np.isfinite(g).all(), f"{what}: non-finite output"
     err = np.abs(g - r)
-    assert err.max() <= ATOL_MAX, f"{what}: max-abs {err.max():.3e} > {ATOL_MAX}"
+    bound = ATOL_MAX if strict else ATOL_MAX + half_ulp_bf16(r)
+    worst = np.unravel_index(np.argmax(err - bound), err.shape)
+    assert (err <= bound).all(), (f"{what}: |err| {err[worst]:.3e} > bound {np.broadcast_to(bound, err.shape)[worst]:.3e}"
+                                  f" at row {rows[worst[0]]}, head {worst[1]}, d {worst[2]} (ref {r[worst]:.4f})")
     assert err.mean() <= ATOL_MEAN, f"{what}: mean-abs {err.mean():.3e} > {ATOL_MEAN}"
     return float(err.max()), float(err.mean())
 

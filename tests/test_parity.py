@@ -46,7 +46,7 @@ def test_workload_attention(name):
         rows = sorted({(int(torch.randint(0, B, (1,), generator=g)), int(torch.randint(0, N, (1,), generator=g)))
                        for _ in range(48)} | {(0, 0), (B - 1, N - 1)})
         ref = oracle_attention(inp, sel=rows)
-    assert_attention_close(got, ref, rows, name)
+    assert_attention_close(got, ref, rows, name, strict=True)
 
 
 @pytest.mark.parametrize("name", FULL + ["serving_16x64"])

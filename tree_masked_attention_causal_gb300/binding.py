@@ -143,7 +143,14 @@ def jf_trace_kernels(events, capacity: int) -> int:
     if not events or capacity <= 0:
         _trace_keep = None
         return load().jf_trace_kernels(None, 0)
-    arr = (ctypes.c_void_p * (2 * capacity))(*[e.cuda_event for e in events[: 2 * capacity]])
+    evs = events[: 2 * capacity]
+    if any(not e.cuda_event for e in evs):
+        import torch
+        for e in evs:              # torch creates the CUDA event lazily, on first record
+            if not e.cuda_event:
+                e.record()
+        torch.cuda.synchronize()
+    arr = (ctypes.c_void_p * (2 * capacity))(*[e.cuda_event for e in evs])
     _trace_keep = arr
     return load().jf_trace_kernels(ctypes.cast(arr, ctypes.c_void_p), capacity)
 
