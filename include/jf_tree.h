@@ -180,6 +180,37 @@ JF_API int32_t jf_tree_verify(const void *logits, const int32_t *tree_tokens,
                               void *workspace, size_t workspace_bytes, int32_t *status,
                               jf_stream_t stream);
 
+/*
+ * Allocation-free variant of jf_tree_verify. The paper has no counterpart:
+ * this entry point exists for callers that cannot allocate device memory.
+ * Examples: code running inside a CUDA graph capture, a custom allocator
+ * that owns all of the device's memory, or an embedding that forbids
+ * cudaMalloc after start-up. Such callers cannot provide a workspace.
+ *
+ * It computes exactly what jf_tree_verify computes, with the same arguments
+ * minus the workspace. Its scratch (the per-chunk argmax partials) is a
+ * fixed array of JF_NOALLOC_SCRATCH_BYTES in the library's device memory.
+ * Every GPU that loads the library holds that array until the process
+ * exits. The call itself allocates nothing.
+ *  - Limit: batch * max_nodes * ceil(vocab / 16384) * 8 bytes must be <=
+ *    JF_NOALLOC_SCRATCH_BYTES (e.g. 13107 logits rows of vocab 151936).
+ *    Larger problems return JF_ERR_SHAPE and launch nothing.
+ *  - The first call on a device looks up the array's device address (with
+ *    that device current) and caches it. Make that first call before any
+ *    stream capture.
+ *  - All calls share the one array, and each call overwrites what it
+ *    reads. Calls that overlap on the GPU (on different streams, or on
+ *    different host threads without ordering) race on it, so serialise
+ *    them.
+ * Returns as jf_tree_verify; JF_ERR_CUDA if the address lookup fails.
+ */
+#define JF_NOALLOC_SCRATCH_BYTES (1u << 20)
+JF_API int32_t jf_tree_verify_noalloc(const void *logits, const int32_t *tree_tokens,
+                                      const int32_t *parents, const int32_t *n_nodes,
+                                      int32_t *accept_len_out, int32_t *accept_path_out,
+                                      int32_t *argmax_out, const jf_shape *shape,
+                                      int32_t max_depth, int32_t *status, jf_stream_t stream);
+
 /* Static description of a return code or status flag. */
 JF_API const char *jf_status_string(int32_t code);
 

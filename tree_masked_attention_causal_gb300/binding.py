@@ -165,3 +165,21 @@ def jf_trace_count() -> int:
 def jf_trace_name(k: int) -> Optional[str]:
     r = load().jf_trace_name(int(k))
     return None if r is None else r.decode()
+
+
+def jf_tree_verify_noalloc(logits, tree_tokens, parents, n_nodes, accept_len_out, accept_path_out, argmax_out,
+                           shape: JfShape, max_depth: int, status=None, stream=None, check: bool = True) -> int:
+    """jf_tree_verify without a workspace, for callers that cannot allocate
+    device memory: the scratch is a fixed array inside the library (see
+    jf_tree.h for its size limit and for when calls race)."""
+    fn = load().jf_tree_verify_noalloc
+    if fn.argtypes is None:
+        P = ctypes.c_void_p
+        fn.argtypes = [P, P, P, P, P, P, P, ctypes.POINTER(JfShape), ctypes.c_int32, P, P]
+        fn.restype = ctypes.c_int32
+    rc = fn(_ptr(logits), _ptr(tree_tokens), _ptr(parents), _ptr(n_nodes), _ptr(accept_len_out),
+            _ptr(accept_path_out), _ptr(argmax_out), ctypes.byref(shape), int(max_depth), _ptr(status),
+            _stream(stream))
+    if check and rc != JF_OK:
+        raise JfError("jf_tree_verify_noalloc", rc)
+    return rc

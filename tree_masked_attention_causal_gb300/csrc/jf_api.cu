@@ -240,6 +240,54 @@ JF_API int32_t jf_tree_verify(const void *logits, const int32_t *tree_tokens, co
     return JF_OK;
 }
 
+// ------------------------------------------------ allocation-free verify
+// Scratch for jf_tree_verify_noalloc: lives in the library's own device
+// memory, so the call needs no caller workspace and allocates nothing.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[JF_NOALLOC_SCRATCH_BYTES];
+
+// Device address of g_noalloc_scratch on the current device, looked up once
+// per device. In host code the symbol's name is only a host-side stand-in,
+// so the kernels must be given this address instead.
+static uint8_t *noalloc_scratch(int dev) {
+    static std::mutex mu;
+    static uint8_t *addr[64] = {nullptr};
+    if (dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lk(mu);
+    if (!addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+        addr[dev] = reinterpret_cast<uint8_t *>(p);
+    }
+    return addr[dev];
+}
+
+JF_API int32_t jf_tree_verify_noalloc(const void *logits, const int32_t *tree_tokens, const int32_t *parents,
+                                      const int32_t *n_nodes, int32_t *accept_len_out, int32_t *accept_path_out,
+                                      int32_t *argmax_out, const jf_shape *shape, int32_t max_depth,
+                                      int32_t *status, jf_stream_t stream) {
+    if (!logits || !tree_tokens || !parents || !n_nodes || !accept_len_out || !accept_path_out || !shape)
+        return JF_ERR_NULL;
+    const int32_t sc = check_shape(shape, true, false);
+    if (sc != JF_OK) return sc;
+    if (max_depth < 0) return JF_ERR_SHAPE;
+    if (!aligned16(logits)) return JF_ERR_ALIGN;
+    Layout L = layout_of(shape);
+    const size_t need = sizeof(int2) * (size_t)L.B * L.Nmax * L.chunks;
+    if (need > (size_t)JF_NOALLOC_SCRATCH_BYTES) return JF_ERR_SHAPE;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return JF_ERR_CUDA;
+    uint8_t *scratch = noalloc_scratch(dev);
+    if (!scratch) return JF_ERR_CUDA;
+    L.amp_off = 0;   // the verify region starts at the array's first byte
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (launch_argmax(L, reinterpret_cast<const __nv_bfloat16 *>(logits), n_nodes, scratch, s) != cudaSuccess)
+        return JF_ERR_CUDA;
+    if (launch_accept_walk(L, tree_tokens, parents, n_nodes, accept_len_out, accept_path_out, argmax_out, max_depth,
+                           scratch, status, s) != cudaSuccess)
+        return JF_ERR_CUDA;
+    return JF_OK;
+}
+
 JF_API uint64_t jf_kernel_launch_count(void) { return g_launches.load(); }
 
 JF_API int32_t jf_trace_kernels(jf_event_t *events, int32_t capacity) {
