@@ -192,8 +192,8 @@ JF_API int32_t jf_tree_verify(const void *logits, const int32_t *tree_tokens,
  * fixed array of JF_NOALLOC_SCRATCH_BYTES in the library's device memory.
  * Every GPU that loads the library holds that array until the process
  * exits. The call itself allocates nothing.
- *  - Limit: batch * max_nodes * ceil(vocab / 16384) * 8 bytes must be <=
- *    JF_NOALLOC_SCRATCH_BYTES (e.g. 13107 logits rows of vocab 151936).
+ *  - Limit: batch * max_nodes * ceil(vocab / 51200) * 8 bytes must be <=
+ *    JF_NOALLOC_SCRATCH_BYTES (e.g. 43690 logits rows of vocab 151936).
  *    Larger problems return JF_ERR_SHAPE and launch nothing.
  *  - The first call on a device looks up the array's device address (with
  *    that device current) and caches it. Make that first call before any

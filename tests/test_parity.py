@@ -169,19 +169,22 @@ def check_verify(inp, max_depth=16):
 
 
 def test_verify_ties_nan_and_signed_zero():
-    inp = small_inputs(20, B=2, N=8, vocab=40000)
+    inp = small_inputs(20, B=2, N=8, vocab=110000)     # three scan chunks of 51200 per row
     lg = inp["logits"]
     lg[0, 0] = 0.0
     lg[0, 1, 20000] = 9.0
-    lg[0, 1, 35000] = 9.0                              # tie across chunks: lowest index
+    lg[0, 1, 105000] = 9.0                             # tie across chunks: lowest index
     lg[0, 2, 5] = float("nan")
-    lg[0, 2, 30000] = float("nan")                     # first NaN wins
+    lg[0, 2, 60000] = float("nan")                     # first NaN wins
     lg[0, 3] = -0.0
-    lg[0, 3, 17000] = 0.0                              # +0 == -0: index 0 wins
+    lg[0, 3, 57000] = 0.0                              # +0 == -0: index 0 wins
     lg[0, 4] = float("-inf")
-    lg[0, 5, 39999] = float("inf")
-    lg[0, 6, 16383] = 10.0                             # chunk boundary
-    lg[0, 6, 16384] = 10.0
+    lg[0, 5, 109999] = float("inf")
+    lg[0, 6, 51199] = 10.0                             # chunk boundary
+    lg[0, 6, 51200] = 10.0
+    lg[0, 7, 51201] = float("nan")                     # NaN only in a later chunk
+    lg[1, 0, 3] = 10.0
+    lg[1, 0, 7] = 10.0                                 # tie inside one 8-element vector
     check_verify(inp)
 
 

@@ -68,9 +68,9 @@ int32_t check_shape(const jf_shape *s, bool need_vocab, bool need_attn) {
     if (need_attn) {
         if (s->n_q_heads < 1 || s->n_kv_heads < 1 || s->n_q_heads % s->n_kv_heads) return JF_ERR_SHAPE;
         const int G = s->n_q_heads / s->n_kv_heads;
-        if (!pow2(G) || G > kBM) return JF_ERR_SHAPE;
+        if (!pow2(G) || G > kBM) return JF_ERR_SHAPE;   // kRows / G >= 2 nodes per unit
         if (s->head_dim != 64 && s->head_dim != 128) return JF_ERR_SHAPE;
-        if (s->prefix_cap < 1) return JF_ERR_SHAPE;
+        if (s->prefix_cap < 1 || s->batch > kMaxBatch) return JF_ERR_SHAPE;
         if (!(s->scale >= 0.0f) || isinf(s->scale)) return JF_ERR_SHAPE;
         // 32-bit index arithmetic in the kernels
         if ((long long)s->batch * s->max_nodes * s->n_q_heads * s->head_dim > 0x7FFFFFFFll) return JF_ERR_SHAPE;

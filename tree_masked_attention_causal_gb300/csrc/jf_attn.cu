@@ -7,33 +7,44 @@
 //
 // Design
 //  * Query stacking (GQA). The G = Hq/Hkv query heads that share a KV head
-//    are stacked with the nodes into 128-row tiles: row r = node_local * G + g.
-//    One 3-D TMA box {64 d, G heads, 128/G nodes} loads such a tile straight
-//    from q[B, Nmax, Hq, d]. Each K/V tile in shared memory then serves all
-//    G heads at once.
-//  * Virtual key sequence. Per query tile, the keys are ceil(P/128) prefix
-//    tiles (from k_cache/v_cache) followed by ceil(n_hi/128) dense tree
-//    tiles (from tree_k/tree_v). Here n_hi is one past the highest node in
-//    the tile. Since parents[i] < i, no key of index > i is ever an ancestor.
-//    The ancestor bitmask (built by the prep kernel) masks the tree tiles in
+//    are stacked with the nodes into a work unit of 128 rows (one tcgen05
+//    MMA tile): row r = node_local * G + g. One 3-D TMA box
+//    {64 d, G heads, 128/G nodes} loads the unit straight from
+//    q[B, Nmax, Hq, d]. Each K/V tile in shared memory then serves all G
+//    heads.
+//  * Virtual key sequence. Per unit, the keys are ceil(P/128) prefix tiles
+//    (from k_cache/v_cache) followed by ceil(n_hi/128) dense tree tiles (from
+//    tree_k/tree_v). Here n_hi is one past the unit's highest node, and
+//    parents[i] < i means no key above a node is ever its ancestor. The
+//    ancestor bitmask (built by the prep kernel) masks the tree tiles in
 //    registers; a key-count bound masks the ragged last prefix tile.
-//  * Split-KV over a device-side plan. The prep kernel cuts each query tile's
-//    key tiles into splits of about total/num_CTAs tiles, and orders the
-//    items longest first. This persistent kernel pulls items from an atomic
-//    queue. A single-split tile is normalised and written as bf16 here; a
-//    split tile writes fp32 (O, m, l) partials that the combine kernel
-//    merges.
-//  * One CTA per SM, 6 warps:
-//      warp 4     TMA producer (Q once per item; K/V through rings of
-//                 NK / NV stages, 128-byte swizzle)
-//      warp 5     TMEM owner and MMA issuer: S = Q K^T (A and B from shared
-//                 memory) into one of two S buffers, then O += P V (A = P
-//                 from TMEM, B = V from shared memory, MN-major)
-//      warps 0-3  softmax: one thread per stacked row (TMEM lane); online
-//                 softmax in the exp2 domain with a lazy rescale of O only
-//                 when a row max grows by more than 2^8; P is written back
-//                 over its S buffer as bf16
-//    TMEM: S0 = columns [0,128), S1 = [128,256), O = [256, 256+d).
+//  * Split-KV over a device-side plan. The prep kernel cuts each unit's tiles
+//    into chunks of about total/num_CTAs tiles, longest first, and this
+//    persistent kernel pulls them from an atomic queue. A single-split unit
+//    is normalised and written as bf16 here. Every split of a split unit
+//    writes fp32 (O, m, l) partials, which the combine kernel merges.
+//  * One CTA per SM, 7 warps:
+//      warps 0-3  softmax (one thread per row = TMEM lane)
+//      warp 4     TMA producer (Q once per item; K/V rings of NK / NV stages)
+//      warp 5     QK^T issuer and TMEM owner: S(g) = Q K(g)^T into S buffer g % 3
+//      warp 6     PV issuer: O += P(g) V(g)
+//    A single thread can issue about one 128x128x16 tcgen05 MMA per 110-140
+//    cycles, about half the tensor core's rate at N = 128. Two issuing warps
+//    with independent accumulators run concurrently, and the tensor core
+//    overlaps them.
+//    TMEM: S buffers at columns 0, 128, 256; O at [384, 384+d). P is written
+//    back as bf16 over its own S. The three S buffers are a ring between the
+//    two issuers: QK^T may run two tiles ahead of the softmax, and a buffer
+//    returns to the QK issuer when the PV that read its P completes.
+//  * Softmax per tile: one 128-column TMEM load, 3-input max chains, ex2 on
+//    the MUFU pipe, bf16 packing, one 64-column TMEM store of P.
+//  * Online softmax in the exp2 domain, lazy rescale: O and l are rescaled
+//    only when a row max grows by more than 2^8. Before releasing P(g), the
+//    softmax makes sure PV(g-1) has completed. O is then stable whenever it
+//    is rescaled, and each o_done wait stays within one barrier phase.
+//  * Launched as a programmatic dependent of the prep kernel: barrier init,
+//    TMEM allocation and tensor-map prefetch overlap it, and every thread
+//    waits (griddepcontrol.wait) before reading the plan or the masks.
 //  * Rows of padding nodes are computed but never stored. V rows past the
 //    prefix length or past n_nodes are zeroed in shared memory before the
 //    PV MMA, so NaN in unused cache rows cannot reach an output.
@@ -43,37 +54,39 @@ namespace jf {
 namespace {
 
 struct ItemInfo {
-    int32_t valid, skip, b, kh, qt, tb, te, t_pre, P, n, ns, slot;
+    int32_t valid, skip, b, kh, qt, tb, te, t_pre, P, n, ns, slot, qtile, split, pad0, pad1;
 };
 
 template <int D>
 struct AttnCfg {
     static constexpr int NK = D == 128 ? 3 : 4;             // K ring stages
-    static constexpr int NV = D == 128 ? 2 : 4;             // V ring stages
-    static constexpr int kBox = 64;                          // d per 128-byte swizzled box
-    static constexpr int kBoxes = D / kBox;
-    static constexpr uint32_t kQBytes = kBM * D * 2;
+    static constexpr int NV = D == 128 ? 3 : 6;             // V ring stages
+    static constexpr int NS = 3;                            // S/P buffers in TMEM
+    static constexpr int kBoxes = D / 64;                   // 64-column (128-byte) swizzled boxes
+    static constexpr uint32_t kQBoxBytes = kRows * 128;     // one box: 128 rows x 128 B
+    static constexpr uint32_t kQBytes = kRows * D * 2;
     static constexpr uint32_t kTileBytes = kBN * D * 2;
     static constexpr uint32_t q_off = 0;
     static constexpr uint32_t k_off = q_off + kQBytes;
     static constexpr uint32_t v_off = k_off + NK * kTileBytes;
     static constexpr uint32_t bar_off = v_off + NV * kTileBytes;
-    // barrier indices
     static constexpr int B_Q_FULL = 0, B_Q_EMPTY = 1, B_K_FULL = 2, B_K_EMPTY = B_K_FULL + NK,
                          B_V_FULL = B_K_EMPTY + NK, B_V_EMPTY = B_V_FULL + NV, B_S_FULL = B_V_EMPTY + NV,
-                         B_P_FULL = B_S_FULL + 2, B_O_DONE = B_P_FULL + 2, B_ITEM_FULL = B_O_DONE + 1,
-                         B_ITEM_EMPTY = B_ITEM_FULL + 2, N_BARS = B_ITEM_EMPTY + 2;
+                         B_S_FREE = B_S_FULL + NS, B_P_FULL = B_S_FREE + NS, B_O_DONE = B_P_FULL + NS,
+                         B_ITEM_FULL = B_O_DONE + 1, B_ITEM_EMPTY = B_ITEM_FULL + 2, N_BARS = B_ITEM_EMPTY + 2;
     static constexpr uint32_t item_off = bar_off + ((N_BARS * 8 + 15) / 16) * 16;
     static constexpr uint32_t misc_off = item_off + 2 * sizeof(ItemInfo);
-    static constexpr uint32_t bytes = misc_off + 16;
+    static constexpr uint32_t bytes = misc_off + 16;         // tmem holder, abort flag
     static constexpr uint32_t smem_request = bytes + 1024;   // slack for 1024-byte alignment
     static constexpr uint32_t kTmemCols = 512;
-    static constexpr uint32_t kColS0 = 0, kColO = 256;
+    static constexpr uint32_t kColO = 384;                   // S buffer s at column 128 * s
 };
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;
 constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;
+constexpr int kQkWarp = 5;
+constexpr int kPvWarp = 6;
+constexpr int kSoftmaxWarps = 4;
 constexpr float kNegInf = -__builtin_huge_valf();
 
 // Wait that ignores the abort flag: used only to drain in-flight copies.
@@ -86,15 +99,14 @@ __device__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
 
 template <int D>
 __device__ __forceinline__ void producer_loop(const AttnMaps &maps, const Layout &L, const AttnArgs &a,
-                                              uint8_t *smem, uint32_t bars, ItemInfo *items_s,
+                                              uint32_t sbase, uint32_t bars, ItemInfo *items_s,
                                               volatile int *abort) {
     using C = AttnCfg<D>;
     const int lane = threadIdx.x & 31;
     PlanHeader *hdr = reinterpret_cast<PlanHeader *>(a.ws + L.plan_off);
     const Item *items = reinterpret_cast<const Item *>(a.ws + L.items_off);
     const SeqInfo *seqs = reinterpret_cast<const SeqInfo *>(a.ws + L.seq_off);
-    const int2 *qtab = reinterpret_cast<const int2 *>(a.ws + L.qtab_off);
-    const uint32_t sbase = smem_u32(smem);
+    const QTile *qtab = reinterpret_cast<const QTile *>(a.ws + L.qtab_off);
     auto bar = [&](int i) { return bars + 8u * i; };
     const int n_items = hdr->n_items;
     int ic = 0, qc = 0, kc = 0, vc = 0;
@@ -121,9 +133,11 @@ __device__ __forceinline__ void producer_loop(const AttnMaps &maps, const Layout
             info.P = si.prefix_len;
             info.n = si.n_nodes;
             info.t_pre = ceil_div(si.prefix_len, kBN);
-            const int2 q = qtab[it.qtile];
-            info.ns = q.x;
-            info.slot = q.x > 1 ? q.y + it.split : -1;
+            const QTile q = qtab[it.qtile];
+            info.ns = q.n_splits;
+            info.slot = q.n_splits > 1 ? q.slot_base + it.split : -1;
+            info.qtile = it.qtile;
+            info.split = it.split;
         }
         if (lane == 0) {
             items_s[slot] = info;
@@ -133,12 +147,12 @@ __device__ __forceinline__ void producer_loop(const AttnMaps &maps, const Layout
         ++ic;
         if (!info.valid) break;
         if (info.skip) continue;
-        // Q tile: G heads x 128/G nodes, d in 64-wide swizzled boxes.
+        // Q: 256 stacked rows (G heads x 256/G nodes), one box per 64 d.
         if (!mbar_wait(bar(C::B_Q_EMPTY), (qc & 1) ^ 1, abort, a.status)) break;
         if (lane == 0) {
             mbar_arrive_expect_tx(bar(C::B_Q_FULL), C::kQBytes);
             for (int dc = 0; dc < C::kBoxes; ++dc)
-                tma_load_3d(sbase + C::q_off + dc * (kBM * 128), &maps.q, dc * 64, info.kh * L.G,
+                tma_load_3d(sbase + C::q_off + dc * C::kQBoxBytes, &maps.q, dc * 64, info.kh * L.G,
                             info.b * L.Nmax + info.qt * L.NB, bar(C::B_Q_FULL));
         }
         ++qc;
@@ -186,97 +200,118 @@ __device__ __forceinline__ void producer_loop(const AttnMaps &maps, const Layout
     }
 }
 
+// Item hand-off shared by the two issuers: returns false at the end.
 template <int D>
-__device__ __forceinline__ void mma_loop(const Layout &L, const AttnArgs &a, uint8_t *smem, uint32_t bars,
-                                         const ItemInfo *items_s, uint32_t tmem, volatile int *abort) {
+__device__ __forceinline__ bool next_item(uint32_t bars, const ItemInfo *items_s, int &ic, ItemInfo &info,
+                                          volatile int *abort, int32_t *status) {
+    using C = AttnCfg<D>;
+    const int slot = ic & 1;
+    if (!mbar_wait(bars + 8u * (C::B_ITEM_FULL + slot), (ic >> 1) & 1, abort, status)) return false;
+    info = items_s[slot];
+    ++ic;
+    return info.valid != 0;
+}
+
+// QK^T issuer: S(g) = Q K(g)^T into S buffer g % 3, up to 2 tiles ahead.
+template <int D>
+__device__ __forceinline__ void qk_loop(const AttnArgs &a, uint32_t sbase, uint32_t bars, const ItemInfo *items_s,
+                                        uint32_t tmem, volatile int *abort) {
     using C = AttnCfg<D>;
     const int lane = threadIdx.x & 31;
-    const uint32_t sbase = smem_u32(smem);
     auto bar = [&](int i) { return bars + 8u * i; };
     constexpr uint32_t idesc_qk = idesc_bf16_f32(kBM, kBN, false, false);
-    constexpr uint32_t idesc_pv = idesc_bf16_f32(kBM, D, false, true);
-    int ic = 0, qc = 0, kc = 0, vc = 0, g = 0;
-
-    // O += P V for item-local tile jj whose S/P buffer is global tile index gj.
-    auto pv = [&](const ItemInfo &info, int jj, int gj) -> bool {
-        const int sb = gj & 1;
-        if (!mbar_wait(bar(C::B_P_FULL + sb), (gj >> 1) & 1, abort, a.status)) return false;
-        tc_fence_after();
-        const int vs = vc % C::NV;
-        if (!mbar_wait(bar(C::B_V_FULL + vs), (vc / C::NV) & 1, abort, a.status)) return false;
-        const uint32_t vtile = C::v_off + vs * C::kTileBytes;
-        // Rows past the prefix length / past n_nodes: zero them so that
-        // whatever the caller's memory holds there cannot reach O via 0 * NaN.
-        const int t = info.tb + jj;
-        int r0 = kBN;
-        if (t < info.t_pre) {
-            if (t == info.t_pre - 1 && (info.P % kBN) != 0) r0 = info.P % kBN;
-        } else {
-            const int left = info.n - (t - info.t_pre) * kBN;
-            r0 = left < 0 ? 0 : (left < kBN ? left : kBN);
-        }
-        if (r0 < kBN) {
-            const int chunks = (kBN - r0) * 8;            // 16-byte chunks per box
-            for (int dc = 0; dc < C::kBoxes; ++dc) {
-                uint4 *base = reinterpret_cast<uint4 *>(smem + vtile + dc * (kBN * 128) + r0 * 128);
-                for (int c = lane; c < chunks; c += 32) base[c] = make_uint4(0u, 0u, 0u, 0u);
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-        }
-        if (lane == 0) {
-#pragma unroll
-            for (int kk = 0; kk < kBN / 16; ++kk) {
-                const uint64_t bdesc = sdesc_sw128(sbase + vtile + kk * 2048, kBN * 128, 1024);
-                mma_ts(tmem + C::kColO, tmem + C::kColS0 + sb * 128 + kk * 8, bdesc, idesc_pv,
-                       (jj > 0 || kk > 0) ? 1u : 0u);
-            }
-            mma_commit(bar(C::B_V_EMPTY + vs));
-            mma_commit(bar(C::B_O_DONE));
-        }
-        __syncwarp();
-        ++vc;
-        return true;
-    };
-
-    while (true) {
-        const int slot = ic & 1;
-        if (!mbar_wait(bar(C::B_ITEM_FULL + slot), (ic >> 1) & 1, abort, a.status)) break;
-        const ItemInfo info = items_s[slot];
-        ++ic;
-        if (!info.valid) break;
+    // Descriptors are built once; the start-address field (address >> 4, in
+    // the low bits) is then advanced by adding byte offsets >> 4.
+    const uint64_t q_desc = sdesc_sw128(sbase + C::q_off, 16, 1024);
+    const uint64_t k_desc = sdesc_sw128(sbase + C::k_off, 16, 1024);
+    int ic = 0, qc = 0, kc = 0, g = 0;
+    ItemInfo info;
+    while (next_item<D>(bars, items_s, ic, info, abort, a.status)) {
+        const int slot = (ic - 1) & 1;
         if (info.skip) {
             if (lane == 0) mbar_arrive(bar(C::B_ITEM_EMPTY + slot));
             continue;
         }
-        if (!mbar_wait(bar(C::B_Q_FULL), qc & 1, abort, a.status)) break;
+        if (!mbar_wait(bar(C::B_Q_FULL), qc & 1, abort, a.status)) return;
         ++qc;
-        tc_fence_after();
         const int nt = info.te - info.tb;
-        bool fail = false;
-        for (int j = 0; j < nt; ++j) {
-            const int ks = kc % C::NK;
-            if (!mbar_wait(bar(C::B_K_FULL + ks), (kc / C::NK) & 1, abort, a.status)) { fail = true; break; }
+        for (int j = 0; j < nt; ++j, ++kc, ++g) {
+            const int ks = kc % C::NK, sb = g % C::NS;
+            if (!mbar_wait(bar(C::B_K_FULL + ks), (kc / C::NK) & 1, abort, a.status)) return;
+            if (!mbar_wait(bar(C::B_S_FREE + sb), ((g / C::NS) & 1) ^ 1, abort, a.status)) return;
             tc_fence_after();
-            const int sb = g & 1;
             if (lane == 0) {
-                const uint32_t ktile = sbase + C::k_off + ks * C::kTileBytes;
+                const uint64_t b0 = k_desc + ((ks * C::kTileBytes) >> 4);
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint64_t adesc = sdesc_sw128(sbase + C::q_off + (kk >> 2) * (kBM * 128) + (kk & 3) * 32, 16, 1024);
-                    const uint64_t bdesc = sdesc_sw128(ktile + (kk >> 2) * (kBN * 128) + (kk & 3) * 32, 16, 1024);
-                    mma_ss(tmem + C::kColS0 + sb * 128, adesc, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
-                }
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_ss(tmem + sb * 128, q_desc + (((kk >> 2) * C::kQBoxBytes + (kk & 3) * 32) >> 4),
+                           b0 + (((kk >> 2) * (kBN * 128) + (kk & 3) * 32) >> 4), idesc_qk, kk > 0 ? 1u : 0u);
                 mma_commit(bar(C::B_S_FULL + sb));
                 mma_commit(bar(C::B_K_EMPTY + ks));
                 if (j == nt - 1) mma_commit(bar(C::B_Q_EMPTY));
             }
             __syncwarp();
-            ++kc;
-            ++g;
-            if (j > 0 && !pv(info, j - 1, g - 2)) { fail = true; break; }
         }
-        if (fail || !pv(info, nt - 1, g - 1)) break;
+        if (lane == 0) mbar_arrive(bar(C::B_ITEM_EMPTY + slot));
+    }
+}
+
+// PV issuer: O (+)= P(g) V(g); a buffer's S/P slot returns to the QK issuer
+// when this PV completes.
+template <int D>
+__device__ __forceinline__ void pv_loop(const AttnArgs &a, uint8_t *smem, uint32_t sbase, uint32_t bars,
+                                        const ItemInfo *items_s, uint32_t tmem, volatile int *abort) {
+    using C = AttnCfg<D>;
+    const int lane = threadIdx.x & 31;
+    auto bar = [&](int i) { return bars + 8u * i; };
+    constexpr uint32_t idesc_pv = idesc_bf16_f32(kBM, D, false, true);
+    const uint64_t v_desc = sdesc_sw128(sbase + C::v_off, kBN * 128, 1024);
+    int ic = 0, vc = 0, g = 0;
+    ItemInfo info;
+    while (next_item<D>(bars, items_s, ic, info, abort, a.status)) {
+        const int slot = (ic - 1) & 1;
+        if (info.skip) {
+            if (lane == 0) mbar_arrive(bar(C::B_ITEM_EMPTY + slot));
+            continue;
+        }
+        const int nt = info.te - info.tb;
+        for (int j = 0; j < nt; ++j, ++vc, ++g) {
+            const int vs = vc % C::NV, sb = g % C::NS;
+            if (!mbar_wait(bar(C::B_P_FULL + sb), (g / C::NS) & 1, abort, a.status)) return;
+            if (!mbar_wait(bar(C::B_V_FULL + vs), (vc / C::NV) & 1, abort, a.status)) return;
+            // V rows past the prefix length / past n_nodes: zero them so that
+            // whatever the caller's memory holds there cannot reach O via 0 * NaN.
+            const int t = info.tb + j;
+            int r0 = kBN;
+            if (t < info.t_pre) {
+                if (t == info.t_pre - 1 && (info.P % kBN) != 0) r0 = info.P % kBN;
+            } else {
+                const int left = info.n - (t - info.t_pre) * kBN;
+                r0 = left < 0 ? 0 : (left < kBN ? left : kBN);
+            }
+            if (r0 < kBN) {
+                const int chunks = (kBN - r0) * 8;            // 16-byte chunks per box
+                for (int dc = 0; dc < C::kBoxes; ++dc) {
+                    uint4 *base = reinterpret_cast<uint4 *>(smem + C::v_off + vs * C::kTileBytes + dc * (kBN * 128) +
+                                                            r0 * 128);
+                    for (int c = lane; c < chunks; c += 32) base[c] = make_uint4(0u, 0u, 0u, 0u);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+            }
+            tc_fence_after();
+            if (lane == 0) {
+                const uint64_t b0 = v_desc + ((vs * C::kTileBytes) >> 4);
+#pragma unroll
+                for (int kk = 0; kk < kBN / 16; ++kk)
+                    mma_ts(tmem + C::kColO, tmem + sb * 128 + kk * 8, b0 + ((kk * 2048) >> 4), idesc_pv,
+                           (j > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(bar(C::B_S_FREE + sb));
+                mma_commit(bar(C::B_V_EMPTY + vs));
+                mma_commit(bar(C::B_O_DONE));
+            }
+            __syncwarp();
+        }
         if (lane == 0) mbar_arrive(bar(C::B_ITEM_EMPTY + slot));
     }
 }
@@ -285,10 +320,10 @@ template <int D>
 __device__ __forceinline__ void softmax_loop(const Layout &L, const AttnArgs &a, uint32_t bars,
                                              const ItemInfo *items_s, uint32_t tmem, volatile int *abort) {
     using C = AttnCfg<D>;
-    const int r = threadIdx.x;            // stacked row = TMEM lane
-    const int warp = r >> 5, lane = r & 31;
+    const int r = threadIdx.x;                      // stacked row = TMEM lane
+    const int wq = r >> 5, lane = r & 31;
     auto bar = [&](int i) { return bars + 8u * i; };
-    const uint32_t t_row = tmem + ((uint32_t)(warp * 32) << 16);
+    const uint32_t t_row = tmem + ((uint32_t)(wq * 32) << 16);
     const uint32_t t_o = t_row + C::kColO;
     const uint32_t *masks = reinterpret_cast<const uint32_t *>(a.ws + L.mask_off);
     float *opart = reinterpret_cast<float *>(a.ws + L.opart_off);
@@ -316,37 +351,41 @@ __device__ __forceinline__ void softmax_loop(const Layout &L, const AttnArgs &a,
         bool fail = false;
         for (int j = 0; j < nt; ++j) {
             const int t = info.tb + j;
-            const int sb = g & 1;
             const bool tree = t >= info.t_pre;
             uint4 mw = make_uint4(0u, 0u, 0u, 0u);
             if (tree && row_valid) mw = *reinterpret_cast<const uint4 *>(mrow + 4 * (t - info.t_pre));
-            if (!mbar_wait(bar(C::B_S_FULL + sb), (g >> 1) & 1, abort, a.status)) { fail = true; break; }
+            const int sb = g % C::NS;
+            const uint32_t t_s = t_row + sb * 128;
+            if (!mbar_wait(bar(C::B_S_FULL + sb), (g / C::NS) & 1, abort, a.status)) { fail = true; break; }
             tc_fence_after();
-            float s[kBN];
+            // One TMEM round trip for the whole 128-column row of S.
+            uint32_t sv[kBN];
+            tmem_ld128(t_s, sv);
+            float sr[kBN];
 #pragma unroll
-            for (int c = 0; c < kBN / 32; ++c) {
-                uint32_t v[32];
-                tmem_ld32(t_row + C::kColS0 + sb * 128 + c * 32, v);
-#pragma unroll
-                for (int k = 0; k < 32; ++k) s[c * 32 + k] = __uint_as_float(v[k]);
-            }
-            if (tree) {
+            for (int c = 0; c < kBN; ++c) sr[c] = __uint_as_float(sv[c]);
+            if (tree) {                                    // ancestors only (1-2 tiles per item)
                 const uint32_t w4[4] = {mw.x, mw.y, mw.z, mw.w};
 #pragma unroll
                 for (int c = 0; c < kBN; ++c)
-                    if (!((w4[c >> 5] >> (c & 31)) & 1u)) s[c] = kNegInf;
+                    if (!((w4[c >> 5] >> (c & 31)) & 1u)) sr[c] = kNegInf;
             } else if (t == info.t_pre - 1) {
-                const int lim = info.P - t * kBN;        // valid keys in the last prefix tile
+                const int lim = info.P - t * kBN;          // valid keys of the last prefix tile
                 if (lim < kBN) {
 #pragma unroll
                     for (int c = 0; c < kBN; ++c)
-                        if (c >= lim) s[c] = kNegInf;
+                        if (c >= lim) sr[c] = kNegInf;
                 }
             }
-            float mx = s[0];
+            // row max: 8 independent chains of 3-input max
+            float m8[8];
 #pragma unroll
-            for (int c = 1; c < kBN; ++c) mx = fmaxf(mx, s[c]);
-            const float mt = mx * sl2;
+            for (int k = 0; k < 8; ++k) m8[k] = sr[k];
+#pragma unroll
+            for (int c = 8; c < kBN; c += 16)
+#pragma unroll
+                for (int k = 0; k < 8; ++k) m8[k] = max3f(m8[k], sr[c + k], sr[c + 8 + k]);
+            const float mt = max3f(max3f(m8[0], m8[1], m8[2]), max3f(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7])) * sl2;
             bool waited_o = false;
             if (j == 0) {
                 m_run = mt;
@@ -354,7 +393,8 @@ __device__ __forceinline__ void softmax_loop(const Layout &L, const AttnArgs &a,
                 const float m_new = fmaxf(m_run, mt);
                 const bool need = m_new > m_run + 8.0f;
                 if (__any_sync(0xffffffffu, need)) {
-                    // O holds PV of the previous tile: wait for it, then rescale.
+                    // O holds PV of the previous tile: wait for it, then
+                    // rescale in place.
                     if (!mbar_wait(bar(C::B_O_DONE), (g - 1) & 1, abort, a.status)) { fail = true; break; }
                     waited_o = true;
                     tc_fence_after();
@@ -374,24 +414,24 @@ __device__ __forceinline__ void softmax_loop(const Layout &L, const AttnArgs &a,
                 }
             }
             const float neg_m = (m_run == kNegInf) ? 0.f : -m_run;
-            float sum = 0.f;
+            float sum8[8];
 #pragma unroll
-            for (int c = 0; c < kBN; ++c) {
-                s[c] = ex2_approx(fmaf(s[c], sl2, neg_m));
-                sum += s[c];
+            for (int k = 0; k < 8; ++k) sum8[k] = 0.f;
+            uint32_t pv[kBN / 2];
+#pragma unroll
+            for (int c = 0; c < kBN; c += 2) {
+                const float p0 = ex2_approx(fmaf(sr[c], sl2, neg_m));
+                const float p1 = ex2_approx(fmaf(sr[c + 1], sl2, neg_m));
+                sum8[c & 7] += p0;
+                sum8[(c + 1) & 7] += p1;
+                pv[c >> 1] = pack_bf16x2(p0, p1);
             }
-            l_run += sum;
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                uint32_t v[32];
-#pragma unroll
-                for (int k = 0; k < 32; ++k) v[k] = pack_bf16x2(s[c * 64 + 2 * k], s[c * 64 + 2 * k + 1]);
-                tmem_st32(t_row + C::kColS0 + sb * 128 + c * 32, v);
-            }
+            tmem_st64(t_s, pv);                            // P (bf16 pairs) over S columns 0-63
+            l_run += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
             tmem_wait_st();
-            // Keep PV of the previous tile retired before P of this one is
-            // released: the epilogue's single o_done wait then stays within
-            // one phase of the barrier.
+            // PV(g-1) must be complete before P(g) is released: O is then
+            // stable for any rescale, and each o_done wait stays within one
+            // phase of its barrier.
             if (j > 0 && !waited_o) {
                 if (!mbar_wait(bar(C::B_O_DONE), (g - 1) & 1, abort, a.status)) { fail = true; break; }
             }
@@ -401,42 +441,38 @@ __device__ __forceinline__ void softmax_loop(const Layout &L, const AttnArgs &a,
             ++g;
         }
         if (fail) break;
-        // Epilogue: wait for the last PV of this item.
+        // Epilogue: the last PV of this item is the last o_done phase.
         if (!mbar_wait(bar(C::B_O_DONE), (g - 1) & 1, abort, a.status)) break;
         tc_fence_after();
         if (info.ns <= 1) {
-            const float inv_l = 1.0f / l_run;
             __nv_bfloat16 *dst = a.out + (((size_t)info.b * L.Nmax + node) * L.Hq + head) * D;
+            const float inv_l = 1.0f / l_run;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t v[32];
                 tmem_ld32(t_o + c * 32, v);
                 if (row_valid) {
                     uint4 *d4 = reinterpret_cast<uint4 *>(dst + c * 32);
+                    auto f = [&](int e) { return __uint_as_float(v[e]) * inv_l; };
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        uint4 w;
-                        w.x = pack_bf16x2(__uint_as_float(v[8 * k + 0]) * inv_l, __uint_as_float(v[8 * k + 1]) * inv_l);
-                        w.y = pack_bf16x2(__uint_as_float(v[8 * k + 2]) * inv_l, __uint_as_float(v[8 * k + 3]) * inv_l);
-                        w.z = pack_bf16x2(__uint_as_float(v[8 * k + 4]) * inv_l, __uint_as_float(v[8 * k + 5]) * inv_l);
-                        w.w = pack_bf16x2(__uint_as_float(v[8 * k + 6]) * inv_l, __uint_as_float(v[8 * k + 7]) * inv_l);
-                        d4[k] = w;
-                    }
+                    for (int k = 0; k < 4; ++k)
+                        d4[k] = make_uint4(pack_bf16x2(f(8 * k), f(8 * k + 1)), pack_bf16x2(f(8 * k + 2), f(8 * k + 3)),
+                                           pack_bf16x2(f(8 * k + 4), f(8 * k + 5)),
+                                           pack_bf16x2(f(8 * k + 6), f(8 * k + 7)));
                 }
             }
         } else {
-            float *dst = opart + ((size_t)info.slot * kBM + r) * D;
+            float4 *d4 = reinterpret_cast<float4 *>(opart + ((size_t)info.slot * kRows + r) * D);
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t v[32];
                 tmem_ld32(t_o + c * 32, v);
-                float4 *d4 = reinterpret_cast<float4 *>(dst + c * 32);
 #pragma unroll
                 for (int k = 0; k < 8; ++k)
-                    d4[k] = make_float4(__uint_as_float(v[4 * k]), __uint_as_float(v[4 * k + 1]),
-                                        __uint_as_float(v[4 * k + 2]), __uint_as_float(v[4 * k + 3]));
+                    d4[8 * c + k] = make_float4(__uint_as_float(v[4 * k]), __uint_as_float(v[4 * k + 1]),
+                                                __uint_as_float(v[4 * k + 2]), __uint_as_float(v[4 * k + 3]));
             }
-            mlpart[(size_t)info.slot * kBM + r] = make_float2(m_run, l_run);
+            mlpart[(size_t)info.slot * kRows + r] = make_float2(m_run, l_run);
         }
         tc_fence_before();
         __syncwarp();
@@ -451,7 +487,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5;
-    const uint32_t bars = smem_u32(smem + C::bar_off);
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t bars = sbase + C::bar_off;
     ItemInfo *items_s = reinterpret_cast<ItemInfo *>(smem + C::item_off);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + C::misc_off);
     volatile int *abort = reinterpret_cast<volatile int *>(smem + C::misc_off + 4);
@@ -462,13 +499,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         init(C::B_Q_EMPTY, 1);
         for (int s = 0; s < C::NK; ++s) { init(C::B_K_FULL + s, 1); init(C::B_K_EMPTY + s, 1); }
         for (int s = 0; s < C::NV; ++s) { init(C::B_V_FULL + s, 1); init(C::B_V_EMPTY + s, 1); }
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < C::NS; ++s) {
             init(C::B_S_FULL + s, 1);
-            init(C::B_P_FULL + s, 4);           // one arrival per softmax warp
-            init(C::B_ITEM_FULL + s, 1);
-            init(C::B_ITEM_EMPTY + s, 5);       // MMA warp + 4 softmax warps
+            init(C::B_S_FREE + s, 1);
+            init(C::B_P_FULL + s, kSoftmaxWarps);          // one arrival per softmax warp
         }
         init(C::B_O_DONE, 1);
+        for (int s = 0; s < 2; ++s) {
+            init(C::B_ITEM_FULL + s, 1);
+            init(C::B_ITEM_EMPTY + s, 2 + kSoftmaxWarps);  // both issuers + every softmax warp
+        }
         *abort = 0;
         fence_mbar_init();
     }
@@ -479,23 +519,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_map(&maps.tree_k);
         tma_prefetch_map(&maps.tree_v);
     }
-    if (warp == kMmaWarp) tmem_alloc(smem_u32(tmem_holder), C::kTmemCols);
+    if (warp == kQkWarp) tmem_alloc(smem_u32(tmem_holder), C::kTmemCols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
+    // Everything above overlapped the prep kernel; the plan and the masks it
+    // writes are read only after this point. The combine kernel may launch
+    // now: it waits for this grid before it reads any partial.
+    pdl_wait_prior_grid();
+    pdl_launch_dependents();
 
     if (warp == kProducerWarp)
-        producer_loop<D>(maps, L, a, smem, bars, items_s, abort);
-    else if (warp == kMmaWarp)
-        mma_loop<D>(L, a, smem, bars, items_s, tmem, abort);
+        producer_loop<D>(maps, L, a, sbase, bars, items_s, abort);
+    else if (warp == kQkWarp)
+        qk_loop<D>(a, sbase, bars, items_s, tmem, abort);
+    else if (warp == kPvWarp)
+        pv_loop<D>(a, smem, sbase, bars, items_s, tmem, abort);
     else
         softmax_loop<D>(L, a, bars, items_s, tmem, abort);
 
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == kMmaWarp) tmem_dealloc(tmem, C::kTmemCols);
+    if (warp == kQkWarp) tmem_dealloc(tmem, C::kTmemCols);
 }
 
 template <int D>
@@ -512,9 +559,19 @@ cudaError_t launch_d(const Layout &L, const AttnMaps &m, const AttnArgs &a, cuda
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.num_ctas);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = C::smem_request;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     trace_begin("tree_attention", s);
-    tree_attention_kernel<D><<<a.num_ctas, kThreads, C::smem_request, s>>>(m, L, a);
-    e = cudaGetLastError();
+    e = cudaLaunchKernelEx(&cfg, tree_attention_kernel<D>, m, L, a);
+    if (e == cudaSuccess) e = cudaGetLastError();
     trace_end(s);
     return e;
 }

@@ -18,22 +18,25 @@
 namespace jf {
 
 // ---------------------------------------------------------------- tiling
-constexpr int kBM = 128;          // stacked query rows per tile (nodes x GQA group)
+constexpr int kBM = 128;          // rows of one tcgen05 MMA tile (= TMEM lanes)
+constexpr int kRows = 128;        // stacked query rows per work unit (one MMA tile)
 constexpr int kBN = 128;          // keys per KV tile
 constexpr int kMaxNodes = 256;    // tree slots per sequence
 constexpr int kMaxCtas = 256;     // cap on the persistent attention grid
 constexpr int kMinTilesPerSplit = 2;
+constexpr int kMaxBatch = 1024;   // sequences per jf_tree_attention call (plan staging)
 constexpr int kArgmaxThreads = 256;
-constexpr int kArgmaxVecs = 8;    // 16-byte vectors per thread per chunk
-constexpr int kArgmaxChunk = kArgmaxThreads * kArgmaxVecs * 8;  // bf16 elements per CTA
+constexpr int kArgmaxVecs = 4;    // 16-byte loads in flight per thread
+constexpr int kArgmaxChunk = 51200;  // bf16 elements of one logits row per CTA (100 KB)
 constexpr unsigned long long kTimeoutNs = 2000000000ull;        // 2 s per wait
 
 __host__ __device__ constexpr int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
 // One tree-attention work item: tiles [tile_begin, tile_end) of the virtual
-// key sequence (prefix tiles first, then tree tiles) for one query tile.
+// key sequence (prefix tiles first, then tree tiles) for one work unit of
+// kRows stacked query rows.
 struct Item {
-    int32_t qtile;       // (b * Hkv + kh) * QT + qt
+    int32_t qtile;       // unit id (b * Hkv + kh) * QT + qt
     int32_t tile_begin;
     int32_t tile_end;
     int32_t split;       // index of this split within the query tile
@@ -44,6 +47,14 @@ struct SeqInfo {         // per sequence, written by the prep kernel
     int32_t n_nodes;
     int32_t bad;
     int32_t pad;
+};
+
+// Per work unit: number of splits and the first partial slot.
+struct QTile {
+    int32_t n_splits;
+    int32_t slot_base;
+    int32_t pad0;
+    int32_t pad1;
 };
 
 struct PlanHeader {
@@ -57,10 +68,10 @@ struct PlanHeader {
 // the verify region; the two never overlap.
 struct Layout {
     int32_t B, Nmax, Hq, Hkv, G, D, Pcap, V;
-    int32_t QT;          // query tiles per (sequence, kv head)
-    int32_t NB;          // nodes per query tile = kBM / G
+    int32_t QT;          // work units per (sequence, kv head)
+    int32_t NB;          // nodes per work unit = kRows / G
     int32_t W4;          // mask words per node (multiple of 4)
-    int32_t n_qtiles;    // B * Hkv * QT
+    int32_t n_qtiles;    // work units: B * Hkv * QT
     int32_t max_items;
     int32_t chunks;      // argmax chunks per logits row
     size_t mask_off, seq_off, plan_off, qtab_off, items_off, ml_off, opart_off;
@@ -74,7 +85,7 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 inline Layout make_layout(int B, int Nmax, int Hq, int Hkv, int D, int Pcap, int V) {
     Layout L{};
     L.B = B; L.Nmax = Nmax; L.Hq = Hq; L.Hkv = Hkv; L.G = Hq / Hkv; L.D = D; L.Pcap = Pcap; L.V = V;
-    L.NB = kBM / L.G;
+    L.NB = kRows / L.G;
     L.QT = ceil_div(Nmax, L.NB);
     L.W4 = 4 * ceil_div(Nmax, kBN);
     L.n_qtiles = B * Hkv * L.QT;
@@ -85,10 +96,10 @@ inline Layout make_layout(int B, int Nmax, int Hq, int Hkv, int D, int Pcap, int
     L.mask_off = take(sizeof(uint32_t) * (size_t)B * Nmax * L.W4);
     L.seq_off = take(sizeof(SeqInfo) * (size_t)B);
     L.plan_off = take(sizeof(PlanHeader));
-    L.qtab_off = take(sizeof(int2) * (size_t)L.n_qtiles);
+    L.qtab_off = take(sizeof(QTile) * (size_t)L.n_qtiles);
     L.items_off = take(sizeof(Item) * (size_t)L.max_items);
-    L.ml_off = take(sizeof(float2) * (size_t)L.max_items * kBM);
-    L.opart_off = take(sizeof(float) * (size_t)L.max_items * kBM * D);
+    L.ml_off = take(sizeof(float2) * (size_t)L.max_items * kRows);
+    L.opart_off = take(sizeof(float) * (size_t)L.max_items * kRows * D);
     L.amp_off = take(sizeof(int2) * (size_t)B * Nmax * L.chunks);
     L.total = off;
     return L;
@@ -284,6 +295,56 @@ __device__ __forceinline__ void tmem_wait_st() {
 
 #undef JF_R8
 #undef JF_W8
+
+// Load 128 consecutive fp32 columns of this thread's TMEM lane and wait for
+// them in the same statement (so no use can be scheduled before the wait).
+__device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&v)[128]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x128.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63, %64, %65, %66, %67, %68, %69, %70, %71, %72, %73, %74, %75, %76, %77, %78, %79, %80, %81, %82, %83, %84, %85, %86, %87, %88, %89, %90, %91, %92, %93, %94, %95, %96, %97, %98, %99, %100, %101, %102, %103, %104, %105, %106, %107, %108, %109, %110, %111, %112, %113, %114, %115, %116, %117, %118, %119, %120, %121, %122, %123, %124, %125, %126, %127}, [%128];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31]), "=r"(v[32]), "=r"(v[33]), "=r"(v[34]), "=r"(v[35]), "=r"(v[36]), "=r"(v[37]), "=r"(v[38]), "=r"(v[39]), "=r"(v[40]), "=r"(v[41]), "=r"(v[42]), "=r"(v[43]), "=r"(v[44]), "=r"(v[45]), "=r"(v[46]), "=r"(v[47]), "=r"(v[48]), "=r"(v[49]), "=r"(v[50]), "=r"(v[51]), "=r"(v[52]), "=r"(v[53]), "=r"(v[54]), "=r"(v[55]), "=r"(v[56]), "=r"(v[57]), "=r"(v[58]), "=r"(v[59]), "=r"(v[60]), "=r"(v[61]), "=r"(v[62]), "=r"(v[63]), "=r"(v[64]), "=r"(v[65]), "=r"(v[66]), "=r"(v[67]), "=r"(v[68]), "=r"(v[69]), "=r"(v[70]), "=r"(v[71]), "=r"(v[72]), "=r"(v[73]), "=r"(v[74]), "=r"(v[75]), "=r"(v[76]), "=r"(v[77]), "=r"(v[78]), "=r"(v[79]), "=r"(v[80]), "=r"(v[81]), "=r"(v[82]), "=r"(v[83]), "=r"(v[84]), "=r"(v[85]), "=r"(v[86]), "=r"(v[87]), "=r"(v[88]), "=r"(v[89]), "=r"(v[90]), "=r"(v[91]), "=r"(v[92]), "=r"(v[93]), "=r"(v[94]), "=r"(v[95]), "=r"(v[96]), "=r"(v[97]), "=r"(v[98]), "=r"(v[99]), "=r"(v[100]), "=r"(v[101]), "=r"(v[102]), "=r"(v[103]), "=r"(v[104]), "=r"(v[105]), "=r"(v[106]), "=r"(v[107]), "=r"(v[108]), "=r"(v[109]), "=r"(v[110]), "=r"(v[111]), "=r"(v[112]), "=r"(v[113]), "=r"(v[114]), "=r"(v[115]), "=r"(v[116]), "=r"(v[117]), "=r"(v[118]), "=r"(v[119]), "=r"(v[120]), "=r"(v[121]), "=r"(v[122]), "=r"(v[123]), "=r"(v[124]), "=r"(v[125]), "=r"(v[126]), "=r"(v[127])
+        : "r"(taddr)
+        : "memory");
+}
+
+// Load 64 consecutive fp32 columns of this thread's TMEM lane (+ wait).
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&v)[64]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%64];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31]), "=r"(v[32]), "=r"(v[33]), "=r"(v[34]), "=r"(v[35]), "=r"(v[36]), "=r"(v[37]), "=r"(v[38]), "=r"(v[39]), "=r"(v[40]), "=r"(v[41]), "=r"(v[42]), "=r"(v[43]), "=r"(v[44]), "=r"(v[45]), "=r"(v[46]), "=r"(v[47]), "=r"(v[48]), "=r"(v[49]), "=r"(v[50]), "=r"(v[51]), "=r"(v[52]), "=r"(v[53]), "=r"(v[54]), "=r"(v[55]), "=r"(v[56]), "=r"(v[57]), "=r"(v[58]), "=r"(v[59]), "=r"(v[60]), "=r"(v[61]), "=r"(v[62]), "=r"(v[63])
+        : "r"(taddr)
+        : "memory");
+}
+
+// Store 64 consecutive 32-bit columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_st64(uint32_t taddr, const uint32_t (&v)[64]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x64.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63, %64};"
+        :: "r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31]), "r"(v[32]), "r"(v[33]), "r"(v[34]), "r"(v[35]), "r"(v[36]), "r"(v[37]), "r"(v[38]), "r"(v[39]), "r"(v[40]), "r"(v[41]), "r"(v[42]), "r"(v[43]), "r"(v[44]), "r"(v[45]), "r"(v[46]), "r"(v[47]), "r"(v[48]), "r"(v[49]), "r"(v[50]), "r"(v[51]), "r"(v[52]), "r"(v[53]), "r"(v[54]), "r"(v[55]), "r"(v[56]), "r"(v[57]), "r"(v[58]), "r"(v[59]), "r"(v[60]), "r"(v[61]), "r"(v[62]), "r"(v[63])
+        : "memory");
+}
+
+// Programmatic dependent launch: let the next kernel in the stream start its
+// prologue now / wait here until the previous kernel's results are visible.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_wait_prior_grid() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Named barrier over the first `count` threads of the CTA.
+__device__ __forceinline__ void named_barrier(uint32_t id, uint32_t count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
 
 __device__ __forceinline__ float ex2_approx(float x) {
     float y;

@@ -6,17 +6,21 @@
 // tokens[c] == argmax(logits[p]); the result is the deepest accepted node.
 //
 //  argmax_chunk_kernel  HBM-bound scan of the logits. Each CTA owns a chunk
-//                       of 16384 bf16 of one row: 8 independent 128-bit
-//                       loads per thread in flight, a packed bf16x2 max
-//                       (NaN-propagating) over them, a block max, then the
-//                       first position holding that max, found in registers
-//                       (no second pass over memory). The (max, index) pair
-//                       of every chunk goes to the workspace.
+//                       of up to 51200 bf16 of one row (one wave of CTAs for
+//                       a 256 x 151936 batch at 6 CTAs per SM). Every thread
+//                       streams 128-bit loads, 4 in flight, and keeps a
+//                       running maximum over its vectors: a packed bf16x2
+//                       NaN-propagating max per
+//                       vector, plus the index of the first vector that
+//                       reached it. At the end it re-reads that one vector
+//                       for the exact first position. A block reduction on
+//                       (value, index) writes the chunk's result.
 //  accept_walk_kernel   one block per sequence, one thread per node: merges
-//                       the chunk results in index order (ties -> lowest
-//                       index, first NaN wins), checks each edge against the
-//                       parent's argmax, walks each node's root path, and
-//                       reduces (depth, -index) to the deepest accepted node.
+//                       the chunk results (ties -> lowest index, the first
+//                       NaN wins), checks each edge against the parent's
+//                       argmax, walks each node's root path, and reduces
+//                       (depth, -index) to the deepest accepted node.
+//                       Launched as a programmatic dependent of the scan.
 #include "jf_common.cuh"
 
 namespace jf {
@@ -47,69 +51,96 @@ __device__ __forceinline__ uint32_t hmax2_nan(uint32_t a, uint32_t b) {
     return *reinterpret_cast<uint32_t *>(&z);
 }
 
-__global__ void __launch_bounds__(kArgmaxThreads)
+// Largest of the 8 bf16 of a vector, as fp32 (exact), NaN if any is NaN.
+__device__ __forceinline__ float vec_max(const uint4 &v) {
+    const uint32_t m2 = hmax2_nan(hmax2_nan(v.x, v.y), hmax2_nan(v.z, v.w));
+    return fmax_nan(bf16_lo(m2), bf16_hi(m2));
+}
+
+// (a, ia) ranks before (b, ib): a NaN first, then the larger value, then
+// the lower index (+0 == -0 compare equal).
+__device__ __forceinline__ bool ranks_before(float a, int ia, float b, int ib) {
+    const bool an = is_nan_f(a), bn = is_nan_f(b);
+    if (an != bn) return an;
+    if (!an && a != b) return a > b;
+    return ia < ib;
+}
+
+__global__ void __launch_bounds__(kArgmaxThreads, 6)
     argmax_chunk_kernel(const __nv_bfloat16 *__restrict__ logits, const int32_t *__restrict__ n_nodes,
                         int2 *__restrict__ part, int Nmax, int V, int chunks) {
     const int row = blockIdx.y;
     const int b = row / Nmax, i = row - b * Nmax;
     const int n = n_nodes[b];
-    if (n < 1 || n > Nmax || i >= n) return;                 // padding row
+    if (n < 1 || n > Nmax || i >= n) {                       // padding row
+        pdl_launch_dependents();
+        return;
+    }
     const int tid = threadIdx.x;
     const int e0 = blockIdx.x * kArgmaxChunk;
-    const int e1 = min(V, e0 + kArgmaxChunk);
+    const int nvec = (min(V, e0 + kArgmaxChunk) - e0) >> 3;  // V % 8 == 0
     const uint4 *src = reinterpret_cast<const uint4 *>(logits + (size_t)row * V + e0);
-    const int nvec = (e1 - e0) >> 3;                         // V % 8 == 0
-    uint4 v[kArgmaxVecs];
-#pragma unroll
-    for (int u = 0; u < kArgmaxVecs; ++u) {
-        const int k = tid + u * kArgmaxThreads;
-        v[u] = k < nvec ? ld_stream(src + k) : make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
-    }
-    uint32_t m2 = 0xFF80FF80u;                               // (-inf, -inf)
-#pragma unroll
-    for (int u = 0; u < kArgmaxVecs; ++u) {
-        m2 = hmax2_nan(m2, v[u].x);
-        m2 = hmax2_nan(m2, v[u].y);
-        m2 = hmax2_nan(m2, v[u].z);
-        m2 = hmax2_nan(m2, v[u].w);
-    }
-    float m = fmax_nan(bf16_lo(m2), bf16_hi(m2));
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmax_nan(m, __shfl_xor_sync(0xffffffffu, m, o));
-    __shared__ float sm[kArgmaxThreads / 32];
-    __shared__ int si[kArgmaxThreads / 32];
-    const int warp = tid >> 5, lane = tid & 31;
-    if (lane == 0) sm[warp] = m;
-    __syncthreads();
-    float M = sm[0];
-#pragma unroll
-    for (int w = 1; w < kArgmaxThreads / 32; ++w) M = fmax_nan(M, sm[w]);
-    // first element equal to M (+0 == -0; NaN matches NaN), in element order
-    int first = 0x7FFFFFFF;
-    const bool M_nan = is_nan_f(M);
-    if (fmax_nan(bf16_lo(m2), bf16_hi(m2)) == M || (M_nan && is_nan_f(fmax_nan(bf16_lo(m2), bf16_hi(m2))))) {
+    float best = -__int_as_float(0x7f800000);
+    int best_k = -1;
+    for (int k0 = tid; k0 < nvec; k0 += kArgmaxThreads * kArgmaxVecs) {
+        uint4 v[kArgmaxVecs];
 #pragma unroll
         for (int u = 0; u < kArgmaxVecs; ++u) {
-            const int k = tid + u * kArgmaxThreads;
-            if (k >= nvec || first != 0x7FFFFFFF) continue;
-            const uint32_t w4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+            const int k = k0 + u * kArgmaxThreads;
+            if (k < nvec) v[u] = ld_stream(src + k);
+        }
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const float x = (q & 1) ? bf16_hi(w4[q >> 1]) : bf16_lo(w4[q >> 1]);
-                const bool hit = M_nan ? is_nan_f(x) : (x == M);
-                if (hit && first == 0x7FFFFFFF) first = e0 + 8 * k + q;
+        for (int u = 0; u < kArgmaxVecs; ++u) {
+            const int k = k0 + u * kArgmaxThreads;
+            if (k < nvec) {
+                const float m = vec_max(v[u]);
+                // strict: the first vector that reaches the maximum is kept;
+                // a NaN replaces any number and is never replaced
+                if (best_k < 0 || m > best || (is_nan_f(m) && !is_nan_f(best))) {
+                    best = m;
+                    best_k = k;
+                }
             }
         }
     }
+    pdl_launch_dependents();
+    // first element of the winning vector that equals the maximum
+    int idx = 0x7FFFFFFF;
+    if (best_k >= 0) {
+        const uint4 v = src[best_k];
+        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+        const bool want_nan = is_nan_f(best);
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) first = min(first, __shfl_xor_sync(0xffffffffu, first, o));
-    if (lane == 0) si[warp] = first;
+        for (int q = 7; q >= 0; --q) {
+            const float x = (q & 1) ? bf16_hi(w4[q >> 1]) : bf16_lo(w4[q >> 1]);
+            if (want_nan ? is_nan_f(x) : (x == best)) idx = e0 + 8 * best_k + q;
+        }
+    }
+    // block reduction on (value, index)
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float ob = __shfl_xor_sync(0xffffffffu, best, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, idx, o);
+        if (ranks_before(ob, oi, best, idx)) {
+            best = ob;
+            idx = oi;
+        }
+    }
+    __shared__ float sv[kArgmaxThreads / 32];
+    __shared__ int si[kArgmaxThreads / 32];
+    const int warp = tid >> 5, lane = tid & 31;
+    if (lane == 0) {
+        sv[warp] = best;
+        si[warp] = idx;
+    }
     __syncthreads();
     if (tid == 0) {
-        int f = si[0];
-#pragma unroll
-        for (int w = 1; w < kArgmaxThreads / 32; ++w) f = min(f, si[w]);
-        part[(size_t)row * chunks + blockIdx.x] = make_int2(__float_as_int(M), f);
+        for (int w = 1; w < kArgmaxThreads / 32; ++w)
+            if (ranks_before(sv[w], si[w], best, idx)) {
+                best = sv[w];
+                idx = si[w];
+            }
+        part[(size_t)row * chunks + blockIdx.x] = make_int2(__float_as_int(best), idx);
     }
 }
 
@@ -124,31 +155,33 @@ __global__ void __launch_bounds__(kMaxNodes)
     __shared__ unsigned char edge_ok[kMaxNodes];
     __shared__ int red[kMaxNodes / 32];
     const int b = blockIdx.x, i = threadIdx.x;
+    // inputs that the scan does not write: read them before waiting on it
     const int n = n_nodes[b];
     const bool n_ok = n >= 1 && n <= Nmax;
-    // merge chunk results in chunk order
+    int p = -1, tok = 0;
+    if (n_ok && i < n) {
+        p = parents[(size_t)b * Nmax + i];
+        tok = tokens[(size_t)b * Nmax + i];
+    }
+    pdl_wait_prior_grid();
+    // merge the chunk results (all loads independent)
     int a = -1;
     if (n_ok && i < n) {
         const int2 *pr = part + ((size_t)b * Nmax + i) * chunks;
         float best = __int_as_float(pr[0].x);
         a = pr[0].y;
         for (int c = 1; c < chunks; ++c) {
-            if (is_nan_f(best)) break;
-            const float x = __int_as_float(pr[c].x);
-            if (is_nan_f(x) || x > best) {
-                best = x;
-                a = pr[c].y;
+            const int2 x = __ldcg(pr + c);
+            if (ranks_before(__int_as_float(x.x), x.y, best, a)) {
+                best = __int_as_float(x.x);
+                a = x.y;
             }
         }
     }
-    if (i < kMaxNodes) am[i] = a;
+    am[i] = a;
     if (argmax_out && i < Nmax) argmax_out[(size_t)b * Nmax + i] = a;
-    int p = -1;
     bool bad = !n_ok;
-    if (n_ok && i < n) {
-        p = parents[(size_t)b * Nmax + i];
-        bad = (i == 0) ? (p != -1) : (p < 0 || p >= i);
-    }
+    if (n_ok && i < n) bad = (i == 0) ? (p != -1) : (p < 0 || p >= i);
     par[i] = p;
     bad = __syncthreads_or(bad);
     int32_t *path = accept_path + (size_t)b * (max_depth + 1);
@@ -160,7 +193,7 @@ __global__ void __launch_bounds__(kMaxNodes)
         }
         return;
     }
-    edge_ok[i] = (i < n) && (i == 0 || tokens[(size_t)b * Nmax + i] == am[p]);
+    edge_ok[i] = (i < n) && (i == 0 || tok == am[p]);
     __syncthreads();
     // accepted iff every edge on the root path agrees
     int key = -1;
@@ -210,11 +243,20 @@ cudaError_t launch_accept_walk(const Layout &L, const int32_t *tokens, const int
                                const int32_t *n_nodes, int32_t *accept_len, int32_t *accept_path,
                                int32_t *argmax_out, int32_t max_depth, uint8_t *ws, int32_t *status,
                                cudaStream_t s) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(L.B);
+    cfg.blockDim = dim3(kMaxNodes);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     trace_begin("accept_walk", s);
-    accept_walk_kernel<<<L.B, kMaxNodes, 0, s>>>(reinterpret_cast<const int2 *>(ws + L.amp_off), tokens, parents,
-                                                 n_nodes, accept_len, accept_path, argmax_out, L.Nmax, L.chunks,
-                                                 max_depth, status);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = cudaLaunchKernelEx(&cfg, accept_walk_kernel, reinterpret_cast<const int2 *>(ws + L.amp_off),
+                                       tokens, parents, n_nodes, accept_len, accept_path, argmax_out, L.Nmax,
+                                       L.chunks, max_depth, status);
+    if (e == cudaSuccess) e = cudaGetLastError();
     trace_end(s);
     return e;
 }
