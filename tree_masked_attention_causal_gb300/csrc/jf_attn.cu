@@ -18,16 +18,20 @@
 //    parents[i] < i means no key above a node is ever its ancestor. The
 //    ancestor bitmask (built by the prep kernel) masks the tree tiles in
 //    registers; a key-count bound masks the ragged last prefix tile.
-//  * Split-KV over a device-side plan. The prep kernel cuts each unit's tiles
-//    into chunks of about total/num_CTAs tiles, longest first, and this
-//    persistent kernel pulls them from an atomic queue. A single-split unit
-//    is normalised and written as bf16 here. Every split of a split unit
-//    writes fp32 (O, m, l) partials, which the combine kernel merges.
-//  * One CTA per SM, 7 warps:
-//      warps 0-3  softmax (one thread per row = TMEM lane)
-//      warp 4     TMA producer (Q once per item; K/V rings of NK / NV stages)
-//      warp 5     QK^T issuer and TMEM owner: S(g) = Q K(g)^T into S buffer g % 3
-//      warp 6     PV issuer: O += P(g) V(g)
+//  * Stream-K split of the keys. The prep kernel concatenates every unit's
+//    key tiles and gives each CTA an equal contiguous range. A CTA walks its
+//    range as one or a few items (one per unit it touches). A unit covered
+//    by a single range is normalised and written as bf16 here. Every piece of
+//    a unit covered by several ranges writes fp32 (O, m, l) partials, which
+//    the combine kernel merges.
+//  * One CTA per SM, 11 warps:
+//      warps 0-7  softmax: warp w owns TMEM lanes 32 (w % 4).. (rows) and S
+//                 columns 64 (w / 4)..; two warps per row quadrant hide
+//                 each other's latencies
+//      warp 8     TMA producer (Q per item, double-buffered; K/V rings of
+//                 NK / NV stages)
+//      warp 9     QK^T issuer and TMEM owner: S(g) = Q K(g)^T into S buffer g % 3
+//      warp 10    PV issuer: O += P(g) V(g)
 //    A single thread can issue about one 128x128x16 tcgen05 MMA per 110-140
 //    cycles, about half the tensor core's rate at N = 128. Two issuing warps
 //    with independent accumulators run concurrently, and the tensor core
@@ -36,8 +40,9 @@
 //    back as bf16 over its own S. The three S buffers are a ring between the
 //    two issuers: QK^T may run two tiles ahead of the softmax, and a buffer
 //    returns to the QK issuer when the PV that read its P completes.
-//  * Softmax per tile: one 128-column TMEM load, 3-input max chains, ex2 on
-//    the MUFU pipe, bf16 packing, one 64-column TMEM store of P.
+//  * Softmax per tile and warp: one 64-column TMEM load, 3-input max chains,
+//    a row-max exchange with the partner warp, ex2 on the MUFU pipe, bf16
+//    packing, one 32-column TMEM store of P.
 //  * Online softmax in the exp2 domain, lazy rescale: O and l are rescaled
 //    only when a row max grows by more than 2^8. Before releasing P(g), the
 //    softmax makes sure PV(g-1) has completed. O is then stable whenever it
@@ -59,7 +64,8 @@ struct ItemInfo {
 
 template <int D>
 struct AttnCfg {
-    static constexpr int NK = D == 128 ? 3 : 4;             // K ring stages
+    static constexpr int NQ = 2;                            // Q buffers: the next unit's Q loads early
+    static constexpr int NK = D == 128 ? 2 : 4;             // K ring stages (released right after QK^T)
     static constexpr int NV = D == 128 ? 3 : 6;             // V ring stages
     static constexpr int NS = 3;                            // S/P buffers in TMEM
     static constexpr int kBoxes = D / 64;                   // 64-column (128-byte) swizzled boxes
@@ -67,26 +73,30 @@ struct AttnCfg {
     static constexpr uint32_t kQBytes = kRows * D * 2;
     static constexpr uint32_t kTileBytes = kBN * D * 2;
     static constexpr uint32_t q_off = 0;
-    static constexpr uint32_t k_off = q_off + kQBytes;
+    static constexpr uint32_t k_off = q_off + NQ * kQBytes;
     static constexpr uint32_t v_off = k_off + NK * kTileBytes;
     static constexpr uint32_t bar_off = v_off + NV * kTileBytes;
-    static constexpr int B_Q_FULL = 0, B_Q_EMPTY = 1, B_K_FULL = 2, B_K_EMPTY = B_K_FULL + NK,
+    static constexpr int B_Q_FULL = 0, B_Q_EMPTY = B_Q_FULL + NQ, B_K_FULL = B_Q_EMPTY + NQ, B_K_EMPTY = B_K_FULL + NK,
                          B_V_FULL = B_K_EMPTY + NK, B_V_EMPTY = B_V_FULL + NV, B_S_FULL = B_V_EMPTY + NV,
                          B_S_FREE = B_S_FULL + NS, B_P_FULL = B_S_FREE + NS, B_O_DONE = B_P_FULL + NS,
-                         B_ITEM_FULL = B_O_DONE + 1, B_ITEM_EMPTY = B_ITEM_FULL + 2, N_BARS = B_ITEM_EMPTY + 2;
+                         B_ITEM_FULL = B_O_DONE + 1, B_ITEM_EMPTY = B_ITEM_FULL + 2, B_PAIR = B_ITEM_EMPTY + 2,
+                         N_BARS = B_PAIR + 4;
     static constexpr uint32_t item_off = bar_off + ((N_BARS * 8 + 15) / 16) * 16;
-    static constexpr uint32_t misc_off = item_off + 2 * sizeof(ItemInfo);
+    static constexpr uint32_t xchg_off = item_off + 2 * sizeof(ItemInfo);   // float [2 parity][2 half][128 rows]
+    static constexpr uint32_t misc_off = xchg_off + 2 * 2 * kRows * sizeof(float);
     static constexpr uint32_t bytes = misc_off + 16;         // tmem holder, abort flag
-    static constexpr uint32_t smem_request = bytes + 1024;   // slack for 1024-byte alignment
+    // The dynamic shared-memory window starts 1024-byte aligned (no static
+    // shared memory precedes it); the kernel checks this and aborts if not.
+    static constexpr uint32_t smem_request = bytes;
     static constexpr uint32_t kTmemCols = 512;
     static constexpr uint32_t kColO = 384;                   // S buffer s at column 128 * s
 };
 
-constexpr int kThreads = 224;
-constexpr int kProducerWarp = 4;
-constexpr int kQkWarp = 5;
-constexpr int kPvWarp = 6;
-constexpr int kSoftmaxWarps = 4;
+constexpr int kThreads = 352;
+constexpr int kSoftmaxWarps = 8;    // warp w: TMEM lanes 32 * (w % 4), S columns 64 * (w / 4)
+constexpr int kProducerWarp = 8;
+constexpr int kQkWarp = 9;
+constexpr int kPvWarp = 10;
 constexpr float kNegInf = -__builtin_huge_valf();
 
 // Wait that ignores the abort flag: used only to drain in-flight copies.
@@ -103,41 +113,47 @@ __device__ __forceinline__ void producer_loop(const AttnMaps &maps, const Layout
                                               volatile int *abort) {
     using C = AttnCfg<D>;
     const int lane = threadIdx.x & 31;
-    PlanHeader *hdr = reinterpret_cast<PlanHeader *>(a.ws + L.plan_off);
-    const Item *items = reinterpret_cast<const Item *>(a.ws + L.items_off);
+    const PlanHeader hdr = *reinterpret_cast<const PlanHeader *>(a.ws + L.plan_off);
     const SeqInfo *seqs = reinterpret_cast<const SeqInfo *>(a.ws + L.seq_off);
     const QTile *qtab = reinterpret_cast<const QTile *>(a.ws + L.qtab_off);
     auto bar = [&](int i) { return bars + 8u * i; };
-    const int n_items = hdr->n_items;
+    // This CTA's stream-K range of the concatenated unit tiles.
+    const int c = blockIdx.x, n_ctas = hdr.n_ctas, total = hdr.total_tiles;
+    long long lo = c < n_ctas ? (long long)c * total / n_ctas : 0;
+    const long long hi = c < n_ctas ? (long long)(c + 1) * total / n_ctas : 0;
+    int u = lo < hi ? reinterpret_cast<const int32_t *>(a.ws + L.first_off)[c] : 0;
     int ic = 0, qc = 0, kc = 0, vc = 0;
     bool ok = true;
     while (ok) {
         const int slot = ic & 1;
         if (!mbar_wait(bar(C::B_ITEM_EMPTY + slot), ((ic >> 1) & 1) ^ 1, abort, a.status)) break;
-        int idx = 0;
-        if (lane == 0) idx = atomicAdd(&hdr->counter, 1);
-        idx = __shfl_sync(0xffffffffu, idx, 0);
         ItemInfo info{};
-        if (idx < n_items) {
-            const Item it = items[idx];
+        QTile q{};
+        if (lo < hi) {
+            q = qtab[u];
+            while (q.tiles == 0) q = qtab[++u];          // units without work
+        }
+        if (lo < hi) {
             const int per_b = L.Hkv * L.QT;
             info.valid = 1;
-            info.b = it.qtile / per_b;
-            const int rem = it.qtile - info.b * per_b;
+            info.qtile = u;
+            info.b = u / per_b;
+            const int rem = u - info.b * per_b;
             info.kh = rem / L.QT;
             info.qt = rem - info.kh * L.QT;
-            info.tb = it.tile_begin;
-            info.te = it.tile_end;
+            info.tb = (int)(lo - q.tile_start);
+            info.te = (int)(min(hi, (long long)q.tile_start + q.tiles) - q.tile_start);
             const SeqInfo si = seqs[info.b];
             info.skip = si.bad;
             info.P = si.prefix_len;
             info.n = si.n_nodes;
             info.t_pre = ceil_div(si.prefix_len, kBN);
-            const QTile q = qtab[it.qtile];
             info.ns = q.n_splits;
-            info.slot = q.n_splits > 1 ? q.slot_base + it.split : -1;
-            info.qtile = it.qtile;
-            info.split = it.split;
+            const int c_first = (int)(((long long)(q.tile_start + 1) * n_ctas - 1) / total);
+            info.split = c - c_first;
+            info.slot = q.n_splits > 1 ? q.slot_base + info.split : -1;
+            lo = (long long)q.tile_start + info.te;
+            ++u;
         }
         if (lane == 0) {
             items_s[slot] = info;
@@ -147,13 +163,15 @@ __device__ __forceinline__ void producer_loop(const AttnMaps &maps, const Layout
         ++ic;
         if (!info.valid) break;
         if (info.skip) continue;
-        // Q: 256 stacked rows (G heads x 256/G nodes), one box per 64 d.
-        if (!mbar_wait(bar(C::B_Q_EMPTY), (qc & 1) ^ 1, abort, a.status)) break;
+        // Q: 128 stacked rows (G heads x 128/G nodes), one box per 64 d, into
+        // buffer qc % NQ so that it can land while the previous unit runs.
+        const int qb = qc % C::NQ;
+        if (!mbar_wait(bar(C::B_Q_EMPTY + qb), ((qc / C::NQ) & 1) ^ 1, abort, a.status)) break;
         if (lane == 0) {
-            mbar_arrive_expect_tx(bar(C::B_Q_FULL), C::kQBytes);
+            mbar_arrive_expect_tx(bar(C::B_Q_FULL + qb), C::kQBytes);
             for (int dc = 0; dc < C::kBoxes; ++dc)
-                tma_load_3d(sbase + C::q_off + dc * C::kQBoxBytes, &maps.q, dc * 64, info.kh * L.G,
-                            info.b * L.Nmax + info.qt * L.NB, bar(C::B_Q_FULL));
+                tma_load_3d(sbase + C::q_off + qb * C::kQBytes + dc * C::kQBoxBytes, &maps.q, dc * 64,
+                            info.kh * L.G, info.b * L.Nmax + info.qt * L.NB, bar(C::B_Q_FULL + qb));
         }
         ++qc;
         for (int t = info.tb; t < info.te; ++t) {
@@ -192,7 +210,8 @@ __device__ __forceinline__ void producer_loop(const AttnMaps &maps, const Layout
     }
     if (*abort && lane == 0) {
         // Let every copy this warp started land before the CTA can exit.
-        if (qc > 0) mbar_wait_drain(bar(C::B_Q_FULL), (qc - 1) & 1);
+        for (int s = 0; s < C::NQ; ++s)
+            if (qc > s) mbar_wait_drain(bar(C::B_Q_FULL + s), (((qc - 1 - s) / C::NQ)) & 1);
         for (int s = 0; s < C::NK; ++s)
             if (kc > s) mbar_wait_drain(bar(C::B_K_FULL + s), (((kc - 1 - s) / C::NK)) & 1);
         for (int s = 0; s < C::NV; ++s)
@@ -232,8 +251,10 @@ __device__ __forceinline__ void qk_loop(const AttnArgs &a, uint32_t sbase, uint3
             if (lane == 0) mbar_arrive(bar(C::B_ITEM_EMPTY + slot));
             continue;
         }
-        if (!mbar_wait(bar(C::B_Q_FULL), qc & 1, abort, a.status)) return;
+        const int qb = qc % C::NQ;
+        if (!mbar_wait(bar(C::B_Q_FULL + qb), (qc / C::NQ) & 1, abort, a.status)) return;
         ++qc;
+        const uint64_t qd = q_desc + ((qb * C::kQBytes) >> 4);
         const int nt = info.te - info.tb;
         for (int j = 0; j < nt; ++j, ++kc, ++g) {
             const int ks = kc % C::NK, sb = g % C::NS;
@@ -244,11 +265,11 @@ __device__ __forceinline__ void qk_loop(const AttnArgs &a, uint32_t sbase, uint3
                 const uint64_t b0 = k_desc + ((ks * C::kTileBytes) >> 4);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
-                    mma_ss(tmem + sb * 128, q_desc + (((kk >> 2) * C::kQBoxBytes + (kk & 3) * 32) >> 4),
+                    mma_ss(tmem + sb * 128, qd + (((kk >> 2) * C::kQBoxBytes + (kk & 3) * 32) >> 4),
                            b0 + (((kk >> 2) * (kBN * 128) + (kk & 3) * 32) >> 4), idesc_qk, kk > 0 ? 1u : 0u);
                 mma_commit(bar(C::B_S_FULL + sb));
                 mma_commit(bar(C::B_K_EMPTY + ks));
-                if (j == nt - 1) mma_commit(bar(C::B_Q_EMPTY));
+                if (j == nt - 1) mma_commit(bar(C::B_Q_EMPTY + qb));
             }
             __syncwarp();
         }
@@ -316,20 +337,41 @@ __device__ __forceinline__ void pv_loop(const AttnArgs &a, uint8_t *smem, uint32
     }
 }
 
+// Softmax and epilogue. Row r of the unit (TMEM lane r) is shared by two
+// warps: warp q handles S columns 0-63 and warp q + 4 columns 64-127 (both
+// reach lanes 32q..32q+31). They exchange their partial row max (each tile)
+// and row sum (each epilogue) through shared memory, synchronising on a
+// bounded mbarrier. Each exchange uses its own parity slot, so a warp that
+// runs ahead cannot overwrite a value its partner has not read yet.
 template <int D>
 __device__ __forceinline__ void softmax_loop(const Layout &L, const AttnArgs &a, uint32_t bars,
-                                             const ItemInfo *items_s, uint32_t tmem, volatile int *abort) {
+                                             const ItemInfo *items_s, float *xchg, uint32_t tmem,
+                                             volatile int *abort) {
     using C = AttnCfg<D>;
-    const int r = threadIdx.x;                      // stacked row = TMEM lane
-    const int wq = r >> 5, lane = r & 31;
+    constexpr int kHalf = kBN / 2;                  // S columns per warp
+    constexpr int kOHalf = D / 2;                   // O columns per warp
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int q = warp & 3, hh = warp >> 2;         // row quadrant, column half
+    const int r = q * 32 + lane;                    // stacked row = TMEM lane
     auto bar = [&](int i) { return bars + 8u * i; };
-    const uint32_t t_row = tmem + ((uint32_t)(wq * 32) << 16);
-    const uint32_t t_o = t_row + C::kColO;
+    const uint32_t t_row = tmem + ((uint32_t)(q * 32) << 16);
+    const uint32_t t_o = t_row + C::kColO + hh * kOHalf;
     const uint32_t *masks = reinterpret_cast<const uint32_t *>(a.ws + L.mask_off);
     float *opart = reinterpret_cast<float *>(a.ws + L.opart_off);
     float2 *mlpart = reinterpret_cast<float2 *>(a.ws + L.ml_off);
     const float sl2 = a.scale_log2;
-    int ic = 0, g = 0;
+    int ic = 0, g = 0, xc = 0;
+    // Exchange one float with the partner warp: returns false on abort.
+    auto exchange = [&](float mine, float &theirs) -> bool {
+        const int par = xc & 1;
+        xchg[(par * 2 + hh) * kRows + r] = mine;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(C::B_PAIR + q));
+        const bool ok = mbar_wait(bar(C::B_PAIR + q), xc & 1, abort, a.status);
+        ++xc;
+        theirs = xchg[(par * 2 + (hh ^ 1)) * kRows + r];
+        return ok;
+    };
 
     while (true) {
         const int slot = ic & 1;
@@ -346,46 +388,49 @@ __device__ __forceinline__ void softmax_loop(const Layout &L, const AttnArgs &a,
         const int head = info.kh * L.G + r % L.G;
         const bool row_valid = node < info.n;
         const uint32_t *mrow = masks + ((size_t)info.b * L.Nmax + (row_valid ? node : 0)) * L.W4;
-        float m_run = kNegInf, l_run = 0.f;
+        float m_run = kNegInf, l_part = 0.f;
         const int nt = info.te - info.tb;
         bool fail = false;
         for (int j = 0; j < nt; ++j) {
             const int t = info.tb + j;
             const bool tree = t >= info.t_pre;
-            uint4 mw = make_uint4(0u, 0u, 0u, 0u);
-            if (tree && row_valid) mw = *reinterpret_cast<const uint4 *>(mrow + 4 * (t - info.t_pre));
+            uint2 mw = make_uint2(0u, 0u);             // mask words of this warp's 64 keys
+            if (tree && row_valid) mw = *reinterpret_cast<const uint2 *>(mrow + 4 * (t - info.t_pre) + 2 * hh);
             const int sb = g % C::NS;
             const uint32_t t_s = t_row + sb * 128;
             if (!mbar_wait(bar(C::B_S_FULL + sb), (g / C::NS) & 1, abort, a.status)) { fail = true; break; }
             tc_fence_after();
-            // One TMEM round trip for the whole 128-column row of S.
-            uint32_t sv[kBN];
-            tmem_ld128(t_s, sv);
-            float sr[kBN];
+            uint32_t sv[kHalf];
+            tmem_ld64(t_s + hh * kHalf, sv);
+            float sr[kHalf];
 #pragma unroll
-            for (int c = 0; c < kBN; ++c) sr[c] = __uint_as_float(sv[c]);
+            for (int c = 0; c < kHalf; ++c) sr[c] = __uint_as_float(sv[c]);
             if (tree) {                                    // ancestors only (1-2 tiles per item)
-                const uint32_t w4[4] = {mw.x, mw.y, mw.z, mw.w};
+                const uint32_t w2[2] = {mw.x, mw.y};
 #pragma unroll
-                for (int c = 0; c < kBN; ++c)
-                    if (!((w4[c >> 5] >> (c & 31)) & 1u)) sr[c] = kNegInf;
+                for (int c = 0; c < kHalf; ++c)
+                    if (!((w2[c >> 5] >> (c & 31)) & 1u)) sr[c] = kNegInf;
             } else if (t == info.t_pre - 1) {
-                const int lim = info.P - t * kBN;          // valid keys of the last prefix tile
-                if (lim < kBN) {
+                const int lim = info.P - t * kBN - hh * kHalf;   // valid keys of this half
+                if (lim < kHalf) {
 #pragma unroll
-                    for (int c = 0; c < kBN; ++c)
+                    for (int c = 0; c < kHalf; ++c)
                         if (c >= lim) sr[c] = kNegInf;
                 }
             }
-            // row max: 8 independent chains of 3-input max
-            float m8[8];
+            float m4[4];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) m8[k] = sr[k];
+            for (int k = 0; k < 4; ++k) m4[k] = sr[k];
 #pragma unroll
-            for (int c = 8; c < kBN; c += 16)
+            for (int c = 4; c < kHalf; c += 8)
 #pragma unroll
-                for (int k = 0; k < 8; ++k) m8[k] = max3f(m8[k], sr[c + k], sr[c + 8 + k]);
-            const float mt = max3f(max3f(m8[0], m8[1], m8[2]), max3f(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7])) * sl2;
+                for (int k = 0; k < 4; ++k) m4[k] = max3f(m4[k], sr[c + k], sr[c + 4 + k]);
+            const float mine = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+            float theirs;
+            if (!exchange(mine, theirs)) { fail = true; break; }
+            // Both warps of the row hold the same inputs from here, so they take
+            // the same lazy-rescale decisions and keep the same m_run.
+            const float mt = fmaxf(mine, theirs) * sl2;
             bool waited_o = false;
             if (j == 0) {
                 m_run = mt;
@@ -393,14 +438,14 @@ __device__ __forceinline__ void softmax_loop(const Layout &L, const AttnArgs &a,
                 const float m_new = fmaxf(m_run, mt);
                 const bool need = m_new > m_run + 8.0f;
                 if (__any_sync(0xffffffffu, need)) {
-                    // O holds PV of the previous tile: wait for it, then
-                    // rescale in place.
+                    // O holds PV of the previous tile: wait for it, then rescale
+                    // this warp's half of the row in place.
                     if (!mbar_wait(bar(C::B_O_DONE), (g - 1) & 1, abort, a.status)) { fail = true; break; }
                     waited_o = true;
                     tc_fence_after();
                     const float alpha = need ? ex2_approx(m_run - m_new) : 1.0f;
-#pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
+#pragma unroll 1
+                    for (int c = 0; c < kOHalf / 32; ++c) {
                         uint32_t v[32];
                         tmem_ld32(t_o + c * 32, v);
 #pragma unroll
@@ -408,26 +453,28 @@ __device__ __forceinline__ void softmax_loop(const Layout &L, const AttnArgs &a,
                         tmem_st32(t_o + c * 32, v);
                     }
                     if (need) {
-                        l_run *= alpha;
+                        l_part *= alpha;
                         m_run = m_new;
                     }
                 }
             }
             const float neg_m = (m_run == kNegInf) ? 0.f : -m_run;
-            float sum8[8];
+            float sum4[4];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) sum8[k] = 0.f;
-            uint32_t pv[kBN / 2];
+            for (int k = 0; k < 4; ++k) sum4[k] = 0.f;
+            uint32_t pv[kHalf / 2];
 #pragma unroll
-            for (int c = 0; c < kBN; c += 2) {
+            for (int c = 0; c < kHalf; c += 2) {
                 const float p0 = ex2_approx(fmaf(sr[c], sl2, neg_m));
                 const float p1 = ex2_approx(fmaf(sr[c + 1], sl2, neg_m));
-                sum8[c & 7] += p0;
-                sum8[(c + 1) & 7] += p1;
+                sum4[c & 3] += p0;
+                sum4[(c + 1) & 3] += p1;
                 pv[c >> 1] = pack_bf16x2(p0, p1);
             }
-            tmem_st64(t_s, pv);                            // P (bf16 pairs) over S columns 0-63
-            l_run += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
+            // P (bf16 pairs) of keys 64*hh.. goes to S columns 32*hh..32*hh+31.
+            // The partner's S columns there were read before the exchange.
+            tmem_st32(t_s + hh * (kHalf / 2), pv);
+            l_part += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
             tmem_wait_st();
             // PV(g-1) must be complete before P(g) is released: O is then
             // stable for any rescale, and each o_done wait stays within one
@@ -444,11 +491,14 @@ __device__ __forceinline__ void softmax_loop(const Layout &L, const AttnArgs &a,
         // Epilogue: the last PV of this item is the last o_done phase.
         if (!mbar_wait(bar(C::B_O_DONE), (g - 1) & 1, abort, a.status)) break;
         tc_fence_after();
+        float l_other;
+        if (!exchange(l_part, l_other)) break;
+        const float l_run = l_part + l_other;
         if (info.ns <= 1) {
-            __nv_bfloat16 *dst = a.out + (((size_t)info.b * L.Nmax + node) * L.Hq + head) * D;
+            __nv_bfloat16 *dst = a.out + (((size_t)info.b * L.Nmax + node) * L.Hq + head) * D + hh * kOHalf;
             const float inv_l = 1.0f / l_run;
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
+#pragma unroll 1
+            for (int c = 0; c < kOHalf / 32; ++c) {
                 uint32_t v[32];
                 tmem_ld32(t_o + c * 32, v);
                 if (row_valid) {
@@ -462,9 +512,9 @@ __device__ __forceinline__ void softmax_loop(const Layout &L, const AttnArgs &a,
                 }
             }
         } else {
-            float4 *d4 = reinterpret_cast<float4 *>(opart + ((size_t)info.slot * kRows + r) * D);
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
+            float4 *d4 = reinterpret_cast<float4 *>(opart + ((size_t)info.slot * kRows + r) * D + hh * kOHalf);
+#pragma unroll 1
+            for (int c = 0; c < kOHalf / 32; ++c) {
                 uint32_t v[32];
                 tmem_ld32(t_o + c * 32, v);
 #pragma unroll
@@ -472,7 +522,7 @@ __device__ __forceinline__ void softmax_loop(const Layout &L, const AttnArgs &a,
                     d4[8 * c + k] = make_float4(__uint_as_float(v[4 * k]), __uint_as_float(v[4 * k + 1]),
                                                 __uint_as_float(v[4 * k + 2]), __uint_as_float(v[4 * k + 3]));
             }
-            mlpart[(size_t)info.slot * kRows + r] = make_float2(m_run, l_run);
+            if (hh == 0) mlpart[(size_t)info.slot * kRows + r] = make_float2(m_run, l_run);
         }
         tc_fence_before();
         __syncwarp();
@@ -484,8 +534,8 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     tree_attention_kernel(const __grid_constant__ AttnMaps maps, const Layout L, const AttnArgs a) {
     using C = AttnCfg<D>;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = smem_raw;
     const int warp = threadIdx.x >> 5;
     const uint32_t sbase = smem_u32(smem);
     const uint32_t bars = sbase + C::bar_off;
@@ -493,10 +543,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + C::misc_off);
     volatile int *abort = reinterpret_cast<volatile int *>(smem + C::misc_off + 4);
 
+    if (smem_u32(smem) & 1023u) {   // swizzled TMA tiles need 1024-byte alignment
+        if (threadIdx.x == 0) set_status(a.status, JF_STATUS_TIMEOUT);
+        return;
+    }
     if (threadIdx.x == 0) {
         auto init = [&](int i, uint32_t count) { mbar_init(bars + 8u * i, count); };
-        init(C::B_Q_FULL, 1);
-        init(C::B_Q_EMPTY, 1);
+        for (int s = 0; s < C::NQ; ++s) { init(C::B_Q_FULL + s, 1); init(C::B_Q_EMPTY + s, 1); }
         for (int s = 0; s < C::NK; ++s) { init(C::B_K_FULL + s, 1); init(C::B_K_EMPTY + s, 1); }
         for (int s = 0; s < C::NV; ++s) { init(C::B_V_FULL + s, 1); init(C::B_V_EMPTY + s, 1); }
         for (int s = 0; s < C::NS; ++s) {
@@ -509,6 +562,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             init(C::B_ITEM_FULL + s, 1);
             init(C::B_ITEM_EMPTY + s, 2 + kSoftmaxWarps);  // both issuers + every softmax warp
         }
+        for (int q = 0; q < 4; ++q) init(C::B_PAIR + q, 2); // the two warps that share a row quadrant
         *abort = 0;
         fence_mbar_init();
     }
@@ -537,7 +591,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     else if (warp == kPvWarp)
         pv_loop<D>(a, smem, sbase, bars, items_s, tmem, abort);
     else
-        softmax_loop<D>(L, a, bars, items_s, tmem, abort);
+        softmax_loop<D>(L, a, bars, items_s, reinterpret_cast<float *>(smem + C::xchg_off), tmem, abort);
 
     tc_fence_before();
     __syncthreads();

@@ -23,7 +23,7 @@ constexpr int kRows = 128;        // stacked query rows per work unit (one MMA t
 constexpr int kBN = 128;          // keys per KV tile
 constexpr int kMaxNodes = 256;    // tree slots per sequence
 constexpr int kMaxCtas = 256;     // cap on the persistent attention grid
-constexpr int kMinTilesPerSplit = 2;
+constexpr int kMinTilesPerCta = 2;   // smallest key range a CTA is given
 constexpr int kMaxBatch = 1024;   // sequences per jf_tree_attention call (plan staging)
 constexpr int kArgmaxThreads = 256;
 constexpr int kArgmaxVecs = 4;    // 16-byte loads in flight per thread
@@ -32,16 +32,6 @@ constexpr unsigned long long kTimeoutNs = 2000000000ull;        // 2 s per wait
 
 __host__ __device__ constexpr int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
-// One tree-attention work item: tiles [tile_begin, tile_end) of the virtual
-// key sequence (prefix tiles first, then tree tiles) for one work unit of
-// kRows stacked query rows.
-struct Item {
-    int32_t qtile;       // unit id (b * Hkv + kh) * QT + qt
-    int32_t tile_begin;
-    int32_t tile_end;
-    int32_t split;       // index of this split within the query tile
-};
-
 struct SeqInfo {         // per sequence, written by the prep kernel
     int32_t prefix_len;
     int32_t n_nodes;
@@ -49,19 +39,23 @@ struct SeqInfo {         // per sequence, written by the prep kernel
     int32_t pad;
 };
 
-// Per work unit: number of splits and the first partial slot.
+// Per work unit (kRows stacked query rows of one sequence and KV head): its
+// key tiles (prefix tiles first, then tree tiles), where they start in the
+// concatenation of all units' tiles, and how many CTA ranges cover it.
 struct QTile {
-    int32_t n_splits;
-    int32_t slot_base;
-    int32_t pad0;
-    int32_t pad1;
+    int32_t n_splits;    // CTA ranges covering the unit (0 = no work)
+    int32_t slot_base;   // first partial slot when n_splits > 1
+    int32_t tile_start;  // prefix sum of `tiles` over earlier units
+    int32_t tiles;
 };
 
+// Stream-K plan: CTA c owns tiles [c * total / n_ctas, (c + 1) * total / n_ctas)
+// of the concatenated unit tiles; `cta_first[c]` is the unit holding the first.
 struct PlanHeader {
-    int32_t n_items;
-    int32_t counter;     // dynamic work queue cursor
-    int32_t tiles_per_split;
     int32_t total_tiles;
+    int32_t n_ctas;
+    int32_t pad0;
+    int32_t pad1;
 };
 
 // Byte offsets of the workspace regions. Attention regions come first, then
@@ -72,9 +66,9 @@ struct Layout {
     int32_t NB;          // nodes per work unit = kRows / G
     int32_t W4;          // mask words per node (multiple of 4)
     int32_t n_qtiles;    // work units: B * Hkv * QT
-    int32_t max_items;
+    int32_t max_items;   // bound on split pieces: n_qtiles + kMaxCtas
     int32_t chunks;      // argmax chunks per logits row
-    size_t mask_off, seq_off, plan_off, qtab_off, items_off, ml_off, opart_off;
+    size_t mask_off, seq_off, plan_off, qtab_off, first_off, ml_off, opart_off;
     size_t amp_off;
     size_t total;
 };
@@ -97,7 +91,7 @@ inline Layout make_layout(int B, int Nmax, int Hq, int Hkv, int D, int Pcap, int
     L.seq_off = take(sizeof(SeqInfo) * (size_t)B);
     L.plan_off = take(sizeof(PlanHeader));
     L.qtab_off = take(sizeof(QTile) * (size_t)L.n_qtiles);
-    L.items_off = take(sizeof(Item) * (size_t)L.max_items);
+    L.first_off = take(sizeof(int32_t) * (size_t)kMaxCtas);
     L.ml_off = take(sizeof(float2) * (size_t)L.max_items * kRows);
     L.opart_off = take(sizeof(float) * (size_t)L.max_items * kRows * D);
     L.amp_off = take(sizeof(int2) * (size_t)B * Nmax * L.chunks);

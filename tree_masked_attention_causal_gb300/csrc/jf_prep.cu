@@ -2,7 +2,7 @@
 //
 //  tree_prep_kernel  one block per sequence validates the tree and builds
 //                    per-node ancestor bitmasks; one more block plans the
-//                    split-KV work items of the attention kernel.
+//                    attention kernel's stream-K split of the key tiles.
 //
 // Ancestor mask ("JetFlow: Scaling Speculative Decoding with Parallel Tree
 // Drafting", blog, section "What JetFlow Does Differently": a node attends to
@@ -22,7 +22,6 @@ namespace {
 
 constexpr int kPrepThreads = 256;
 constexpr int kMaskWords = kMaxNodes / 32;   // 8
-constexpr int kHistBins = 256;
 
 // Block-wide exclusive scan of one int per thread; returns the block total.
 __device__ int block_exclusive_scan(int v, int *out_excl, int *sh) {
@@ -103,17 +102,16 @@ __device__ void build_sequence(const Layout &L, const AttnArgs &a, int b) {
     }
 }
 
-// Plan. A query tile (b, kh, qt) needs T = ceil(P_b/128) prefix tiles plus
-// the ceil(n_hi/128) tree tiles under its highest node. With
-// tps = max(kMinTilesPerSplit, ceil(total / num_ctas)), it is cut into
-// chunks of tps tiles plus one remainder chunk. Items are ordered longest
-// first (counting sort on length) for the attention kernel's atomic queue,
-// so the short remainders fill in behind the long chunks.
+// Stream-K plan. Unit u (sequence b, KV head kh, query tile qt) needs
+// T_u = ceil(P_b/128) prefix tiles plus the ceil(n_hi/128) tree tiles under
+// its highest node. Concatenate all units' tiles (total) and give CTA c the
+// equal range [c * total / C, (c + 1) * total / C), C = min(num_ctas,
+// total / kMinTilesPerCta). A unit that several ranges cover is split; its
+// split s is the s-th covering CTA (key order), writing partial slot
+// slot_base + s for the combine kernel.
 __device__ void plan(const Layout &L, const AttnArgs &a) {
     __shared__ int sh[32];
-    __shared__ int hist[kHistBins];
     __shared__ int sP[kMaxBatch], sN[kMaxBatch];
-    __shared__ int s_total;
     const int tid = threadIdx.x;
     for (int b = tid; b < L.B; b += blockDim.x) {
         const int P = a.prefix_lens[b], n = a.n_nodes[b];
@@ -121,64 +119,51 @@ __device__ void plan(const Layout &L, const AttnArgs &a) {
         sP[b] = ok ? P : 0;
         sN[b] = ok ? n : 0;
     }
-    for (int k = tid; k < kHistBins; k += blockDim.x) hist[k] = 0;
     __syncthreads();
-    auto tiles = [&](int b, int qt) {
+    auto tiles_of = [&](int u) {
+        const int b = u / (L.Hkv * L.QT), qt = u % L.QT;
         const int n = sN[b], node0 = qt * L.NB;
         if (node0 >= n) return 0;
         return ceil_div(sP[b], kBN) + ceil_div(min(node0 + L.NB, n), kBN);
     };
-    int local = 0;
-    for (int k = tid; k < L.B * L.QT; k += blockDim.x) local += tiles(k / L.QT, k % L.QT);
-    int excl;
-    const int total = L.Hkv * block_exclusive_scan(local, &excl, sh);
-    const int tps = max(kMinTilesPerSplit, ceil_div(total, max(1, a.num_ctas)));
-    auto bin_of = [&](int size) { return min(size, kHistBins - 1); };
-
     QTile *qtab = reinterpret_cast<QTile *>(a.ws + L.qtab_off);
-    Item *items = reinterpret_cast<Item *>(a.ws + L.items_off);
+    int32_t *cta_first = reinterpret_cast<int32_t *>(a.ws + L.first_off);
     PlanHeader *hdr = reinterpret_cast<PlanHeader *>(a.ws + L.plan_off);
-    // pass 1: split counts, length histogram, partial-slot bases
+    // pass 1: tile counts and their prefix sums
+    int run = 0;
+    for (int base = 0; base < L.n_qtiles; base += blockDim.x) {
+        const int u = base + tid;
+        const int T = u < L.n_qtiles ? tiles_of(u) : 0;
+        int ex;
+        const int tot = block_exclusive_scan(T, &ex, sh);
+        if (u < L.n_qtiles) qtab[u] = QTile{0, 0, run + ex, T};
+        run += tot;
+    }
+    const int total = run;
+    const int C = max(1, min(a.num_ctas, total / kMinTilesPerCta));
+    __syncthreads();   // qtab of every unit is visible to the whole block
+    // pass 2: covering CTA ranges, split slots, each CTA's first unit
     int slot_run = 0;
     for (int base = 0; base < L.n_qtiles; base += blockDim.x) {
-        const int q = base + tid;
-        int ns = 0;
-        if (q < L.n_qtiles) {
-            const int T = tiles(q / (L.Hkv * L.QT), q % L.QT);
-            ns = ceil_div(T, tps);
-            for (int s = 0; s < ns; ++s) atomicAdd(&hist[bin_of(min(tps, T - s * tps))], 1);
+        const int u = base + tid;
+        int ns = 0, S = 0, T = 0;
+        if (u < L.n_qtiles) {
+            S = qtab[u].tile_start;
+            T = qtab[u].tiles;
+            if (T > 0) {
+                const int c_first = (int)(((long long)(S + 1) * C - 1) / total);
+                const int c_last = (int)(((long long)(S + T) * C - 1) / total);
+                ns = c_last - c_first + 1;
+                for (int c = c_first; c <= c_last; ++c)   // ranges that start inside u
+                    if ((long long)c * total / C >= S) cta_first[c] = u;
+            }
         }
         int ex;
         const int tot = block_exclusive_scan(ns > 1 ? ns : 0, &ex, sh);
-        if (q < L.n_qtiles) qtab[q] = QTile{ns, slot_run + ex, 0, 0};
+        if (u < L.n_qtiles) qtab[u] = QTile{ns, slot_run + ex, S, T};
         slot_run += tot;
     }
-    __syncthreads();
-    if (tid == 0) {   // longest first: starting offsets in descending length
-        int run = 0;
-        for (int k = kHistBins - 1; k >= 0; --k) {
-            const int c = hist[k];
-            hist[k] = run;
-            run += c;
-        }
-        s_total = run;
-    }
-    __syncthreads();
-    // pass 2: scatter items
-    for (int q = tid; q < L.n_qtiles; q += blockDim.x) {
-        const int T = tiles(q / (L.Hkv * L.QT), q % L.QT);
-        const int ns = ceil_div(T, tps);
-        for (int s = 0; s < ns; ++s) {
-            const int b0 = s * tps, b1 = min(T, b0 + tps);
-            const int pos = atomicAdd(&hist[bin_of(b1 - b0)], 1);
-            if (pos < L.max_items) items[pos] = Item{q, b0, b1, s};
-        }
-    }
-    if (tid == 0) {
-        // n_items <= n_qtiles + num_ctas = max_items always: sum ceil(T/tps)
-        // <= total/tps + n_qtiles and tps >= total/num_ctas.
-        *hdr = PlanHeader{min(s_total, L.max_items), 0, tps, total};
-    }
+    if (tid == 0) *hdr = PlanHeader{total, total > 0 ? C : 0, 0, 0};
 }
 
 __global__ void __launch_bounds__(kPrepThreads) tree_prep_kernel(const Layout L, const AttnArgs a) {
