@@ -32,10 +32,10 @@
 //                 NK / NV stages)
 //      warp 9     QK^T issuer and TMEM owner: S(g) = Q K(g)^T into S buffer g % 3
 //      warp 10    PV issuer: O += P(g) V(g)
-//    A single thread can issue about one 128x128x16 tcgen05 MMA per 110-140
-//    cycles, about half the tensor core's rate at N = 128. Two issuing warps
-//    with independent accumulators run concurrently, and the tensor core
-//    overlaps them.
+//    One warp issuing 128x128x16 tcgen05 MMAs (elected lane, warp-uniform
+//    operands) manages one per ~87 cycles, about 3/4 of the tensor core's
+//    rate at N = 128. Two issuing warps with independent accumulators run
+//    concurrently, and the tensor core overlaps them.
 //    TMEM: S buffers at columns 0, 128, 256; O at [384, 384+d). P is written
 //    back as bf16 over its own S. The three S buffers are a ring between the
 //    two issuers: QK^T may run two tiles ahead of the softmax, and a buffer
@@ -261,17 +261,15 @@ __device__ __forceinline__ void qk_loop(const AttnArgs &a, uint32_t sbase, uint3
             if (!mbar_wait(bar(C::B_K_FULL + ks), (kc / C::NK) & 1, abort, a.status)) return;
             if (!mbar_wait(bar(C::B_S_FREE + sb), ((g / C::NS) & 1) ^ 1, abort, a.status)) return;
             tc_fence_after();
-            if (lane == 0) {
-                const uint64_t b0 = k_desc + ((ks * C::kTileBytes) >> 4);
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                    mma_ss(tmem + sb * 128, qd + (((kk >> 2) * C::kQBoxBytes + (kk & 3) * 32) >> 4),
-                           b0 + (((kk >> 2) * (kBN * 128) + (kk & 3) * 32) >> 4), idesc_qk, kk > 0 ? 1u : 0u);
-                mma_commit(bar(C::B_S_FULL + sb));
-                mma_commit(bar(C::B_K_EMPTY + ks));
-                if (j == nt - 1) mma_commit(bar(C::B_Q_EMPTY + qb));
-            }
             __syncwarp();
+            const uint64_t b0 = k_desc + ((ks * C::kTileBytes) >> 4);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk)
+                mma_ss(tmem + sb * 128, qd + (((kk >> 2) * C::kQBoxBytes + (kk & 3) * 32) >> 4),
+                       b0 + (((kk >> 2) * (kBN * 128) + (kk & 3) * 32) >> 4), idesc_qk, kk > 0 ? 1u : 0u);
+            mma_commit(bar(C::B_S_FULL + sb));
+            mma_commit(bar(C::B_K_EMPTY + ks));
+            if (j == nt - 1) mma_commit(bar(C::B_Q_EMPTY + qb));
         }
         if (lane == 0) mbar_arrive(bar(C::B_ITEM_EMPTY + slot));
     }
@@ -321,17 +319,15 @@ __device__ __forceinline__ void pv_loop(const AttnArgs &a, uint8_t *smem, uint32
                 __syncwarp();
             }
             tc_fence_after();
-            if (lane == 0) {
-                const uint64_t b0 = v_desc + ((vs * C::kTileBytes) >> 4);
-#pragma unroll
-                for (int kk = 0; kk < kBN / 16; ++kk)
-                    mma_ts(tmem + C::kColO, tmem + sb * 128 + kk * 8, b0 + ((kk * 2048) >> 4), idesc_pv,
-                           (j > 0 || kk > 0) ? 1u : 0u);
-                mma_commit(bar(C::B_S_FREE + sb));
-                mma_commit(bar(C::B_V_EMPTY + vs));
-                mma_commit(bar(C::B_O_DONE));
-            }
             __syncwarp();
+            const uint64_t b0 = v_desc + ((vs * C::kTileBytes) >> 4);
+#pragma unroll
+            for (int kk = 0; kk < kBN / 16; ++kk)
+                mma_ts(tmem + C::kColO, tmem + sb * 128 + kk * 8, b0 + ((kk * 2048) >> 4), idesc_pv,
+                       (j > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(bar(C::B_S_FREE + sb));
+            mma_commit(bar(C::B_V_EMPTY + vs));
+            mma_commit(bar(C::B_O_DONE));
         }
         if (lane == 0) mbar_arrive(bar(C::B_ITEM_EMPTY + slot));
     }
