@@ -24,12 +24,14 @@
 //    by a single range is normalised and written as bf16 here. Every piece of
 //    a unit covered by several ranges writes fp32 (O, m, l) partials, which
 //    the combine kernel merges.
-//  * One CTA per SM, 11 warps:
-//      warps 0-7  softmax: warp w owns TMEM lanes 32 (w % 4).. (rows) and S
-//                 columns 64 (w / 4)..; two warps per row quadrant hide
-//                 each other's latencies
-//      warp 8     TMA producer (Q per item, double-buffered; K/V rings of
-//                 NK / NV stages)
+//  * One CTA per SM, 12 warps:
+//      warps 0-7  softmax: warp w owns TMEM lanes 32 (w % 4).. (rows) for
+//                 the key tiles g with g % 2 == w / 4; the two warps of a
+//                 row quadrant alternate tiles and hide each other's
+//                 latencies
+//      warp 8     TMA producer of Q (per item, double-buffered) and of the
+//                 NK-stage K ring
+//      warp 11    TMA producer of the NV-stage V ring
 //      warp 9     QK^T issuer and TMEM owner: S(g) = Q K(g)^T into S buffer g % 3
 //      warp 10    PV issuer: O += P(g) V(g)
 //    One warp issuing 128x128x16 tcgen05 MMAs (elected lane, warp-uniform
@@ -37,16 +39,17 @@
 //    rate at N = 128. Two issuing warps with independent accumulators run
 //    concurrently, and the tensor core overlaps them.
 //    TMEM: S buffers at columns 0, 128, 256; O at [384, 384+d). P is written
-//    back as bf16 over its own S. The three S buffers are a ring between the
-//    two issuers: QK^T may run two tiles ahead of the softmax, and a buffer
-//    returns to the QK issuer when the PV that read its P completes.
-//  * Softmax per tile and warp: one 64-column TMEM load, 3-input max chains,
-//    a row-max exchange with the partner warp, ex2 on the MUFU pipe, bf16
-//    packing, one 32-column TMEM store of P.
-//  * Online softmax in the exp2 domain, lazy rescale: O and l are rescaled
-//    only when a row max grows by more than 2^8. Before releasing P(g), the
-//    softmax makes sure PV(g-1) has completed. O is then stable whenever it
-//    is rescaled, and each o_done wait stays within one barrier phase.
+//    back as bf16 over the first 64 columns of its own S. The three S buffers
+//    are a ring between the two issuers: QK^T may run two tiles ahead of the
+//    softmax, and a buffer returns to the QK issuer when the PV that read its
+//    P completes.
+//  * Softmax per tile (one warp per row quadrant): one 128-column TMEM load
+//    into registers, the row max, the running max handed over from the
+//    previous tile's owner, ex2 on the MUFU pipe, bf16 packing, P stored.
+//  * Online softmax in the exp2 domain, lazy rescale: O is rescaled only
+//    when a row max grows by more than 2^8, by the owner of that tile, once
+//    the previous tile's PV has completed. The first PV of an item waits
+//    until every softmax warp has read the previous item's O.
 //  * Launched as a programmatic dependent of the prep kernel: barrier init,
 //    TMEM allocation and tensor-map prefetch overlap it, and every thread
 //    waits (griddepcontrol.wait) before reading the plan or the masks.
@@ -78,12 +81,13 @@ struct AttnCfg {
     static constexpr uint32_t bar_off = v_off + NV * kTileBytes;
     static constexpr int B_Q_FULL = 0, B_Q_EMPTY = B_Q_FULL + NQ, B_K_FULL = B_Q_EMPTY + NQ, B_K_EMPTY = B_K_FULL + NK,
                          B_V_FULL = B_K_EMPTY + NK, B_V_EMPTY = B_V_FULL + NV, B_S_FULL = B_V_EMPTY + NV,
-                         B_S_FREE = B_S_FULL + NS, B_P_FULL = B_S_FREE + NS, B_O_DONE = B_P_FULL + NS,
-                         B_ITEM_FULL = B_O_DONE + 1, B_ITEM_EMPTY = B_ITEM_FULL + 2, B_PAIR = B_ITEM_EMPTY + 2,
-                         N_BARS = B_PAIR + 4;
+                         B_S_FREE = B_S_FULL + NS, B_P_FULL = B_S_FREE + NS, B_O_FREE = B_P_FULL + NS,
+                         B_ITEM_FULL = B_O_FREE + 1, B_ITEM_EMPTY = B_ITEM_FULL + 2, B_PAIR = B_ITEM_EMPTY + 2,
+                         B_HAND = B_PAIR + 4, N_BARS = B_HAND + 8;
     static constexpr uint32_t item_off = bar_off + ((N_BARS * 8 + 15) / 16) * 16;
-    static constexpr uint32_t xchg_off = item_off + 2 * sizeof(ItemInfo);   // float [2 parity][2 half][128 rows]
-    static constexpr uint32_t misc_off = xchg_off + 2 * 2 * kRows * sizeof(float);
+    static constexpr uint32_t hand_off = item_off + 2 * sizeof(ItemInfo);   // float [4 quadrants][2 slots][32]
+    static constexpr uint32_t xchg_off = hand_off + 4 * 2 * 32 * sizeof(float);   // float [2 warps][128 rows]
+    static constexpr uint32_t misc_off = xchg_off + 2 * kRows * sizeof(float);
     static constexpr uint32_t bytes = misc_off + 16;         // tmem holder, abort flag
     // The dynamic shared-memory window starts 1024-byte aligned (no static
     // shared memory precedes it); the kernel checks this and aborts if not.
@@ -92,11 +96,16 @@ struct AttnCfg {
     static constexpr uint32_t kColO = 384;                   // S buffer s at column 128 * s
 };
 
-constexpr int kThreads = 352;
+constexpr int kThreads = 384;
 constexpr int kSoftmaxWarps = 8;    // warp w: TMEM lanes 32 * (w % 4), S columns 64 * (w / 4)
 constexpr int kProducerWarp = 8;
 constexpr int kQkWarp = 9;
 constexpr int kPvWarp = 10;
+constexpr int kVProducerWarp = 11;
+constexpr int kLaunchRegs = 168;            // per thread at launch: 384 x 168 = 64512
+constexpr uint32_t kSoftmaxRegs = 224;      // warpgroups 0-1 after setmaxnreg
+constexpr uint32_t kOtherRegs = 56;         // warpgroup 2 (producers, issuers)
+static_assert(256 * kSoftmaxRegs + 128 * kOtherRegs <= kThreads * kLaunchRegs, "register split");
 constexpr float kNegInf = -__builtin_huge_valf();
 
 // Wait that ignores the abort flag: used only to drain in-flight copies.
@@ -122,7 +131,7 @@ __device__ __forceinline__ void producer_loop(const AttnMaps &maps, const Layout
     long long lo = c < n_ctas ? (long long)c * total / n_ctas : 0;
     const long long hi = c < n_ctas ? (long long)(c + 1) * total / n_ctas : 0;
     int u = lo < hi ? reinterpret_cast<const int32_t *>(a.ws + L.first_off)[c] : 0;
-    int ic = 0, qc = 0, kc = 0, vc = 0;
+    int ic = 0, qc = 0, kc = 0;
     bool ok = true;
     while (ok) {
         const int slot = ic & 1;
@@ -191,21 +200,6 @@ __device__ __forceinline__ void producer_loop(const AttnMaps &maps, const Layout
                 }
             }
             ++kc;
-            const int vs = vc % C::NV;
-            if (!mbar_wait(bar(C::B_V_EMPTY + vs), ((vc / C::NV) & 1) ^ 1, abort, a.status)) { ok = false; break; }
-            if (lane == 0) {
-                mbar_arrive_expect_tx(bar(C::B_V_FULL + vs), C::kTileBytes);
-                for (int dc = 0; dc < C::kBoxes; ++dc) {
-                    const uint32_t dst = sbase + C::v_off + vs * C::kTileBytes + dc * (kBN * 128);
-                    if (tree)
-                        tma_load_3d(dst, &maps.tree_v, dc * 64, info.kh, info.b * L.Nmax + (t - info.t_pre) * kBN,
-                                    bar(C::B_V_FULL + vs));
-                    else
-                        tma_load_3d(dst, &maps.v_cache, dc * 64, t * kBN, info.b * L.Hkv + info.kh,
-                                    bar(C::B_V_FULL + vs));
-                }
-            }
-            ++vc;
         }
     }
     if (*abort && lane == 0) {
@@ -214,8 +208,6 @@ __device__ __forceinline__ void producer_loop(const AttnMaps &maps, const Layout
             if (qc > s) mbar_wait_drain(bar(C::B_Q_FULL + s), (((qc - 1 - s) / C::NQ)) & 1);
         for (int s = 0; s < C::NK; ++s)
             if (kc > s) mbar_wait_drain(bar(C::B_K_FULL + s), (((kc - 1 - s) / C::NK)) & 1);
-        for (int s = 0; s < C::NV; ++s)
-            if (vc > s) mbar_wait_drain(bar(C::B_V_FULL + s), (((vc - 1 - s) / C::NV)) & 1);
     }
 }
 
@@ -229,6 +221,51 @@ __device__ __forceinline__ bool next_item(uint32_t bars, const ItemInfo *items_s
     info = items_s[slot];
     ++ic;
     return info.valid != 0;
+}
+
+// V producer: the V tiles of each item into the NV-stage ring. It runs apart
+// from the Q/K producer so that a K load never waits behind a V stage that a
+// slower PV still holds.
+template <int D>
+__device__ __forceinline__ void v_producer_loop(const AttnMaps &maps, const Layout &L, const AttnArgs &a,
+                                                uint32_t sbase, uint32_t bars, const ItemInfo *items_s,
+                                                volatile int *abort) {
+    using C = AttnCfg<D>;
+    const int lane = threadIdx.x & 31;
+    auto bar = [&](int i) { return bars + 8u * i; };
+    int ic = 0, vc = 0;
+    ItemInfo info;
+    bool ok = true;
+    while (ok && next_item<D>(bars, items_s, ic, info, abort, a.status)) {
+        const int slot = (ic - 1) & 1;
+        if (!info.skip) {
+            for (int t = info.tb; t < info.te; ++t) {
+                const bool tree = t >= info.t_pre;
+                const int vs = vc % C::NV;
+                if (!mbar_wait(bar(C::B_V_EMPTY + vs), ((vc / C::NV) & 1) ^ 1, abort, a.status)) { ok = false; break; }
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(bar(C::B_V_FULL + vs), C::kTileBytes);
+                    for (int dc = 0; dc < C::kBoxes; ++dc) {
+                        const uint32_t dst = sbase + C::v_off + vs * C::kTileBytes + dc * (kBN * 128);
+                        if (tree)
+                            tma_load_3d(dst, &maps.tree_v, dc * 64, info.kh,
+                                        info.b * L.Nmax + (t - info.t_pre) * kBN, bar(C::B_V_FULL + vs));
+                        else
+                            tma_load_3d(dst, &maps.v_cache, dc * 64, t * kBN, info.b * L.Hkv + info.kh,
+                                        bar(C::B_V_FULL + vs));
+                    }
+                }
+                __syncwarp();
+                ++vc;
+            }
+        }
+        if (ok && lane == 0) mbar_arrive(bar(C::B_ITEM_EMPTY + slot));
+    }
+    if (*abort && lane == 0) {
+        // Let every copy this warp started land before the CTA can exit.
+        for (int s = 0; s < C::NV; ++s)
+            if (vc > s) mbar_wait_drain(bar(C::B_V_FULL + s), (((vc - 1 - s) / C::NV)) & 1);
+    }
 }
 
 // QK^T issuer: S(g) = Q K(g)^T into S buffer g % 3, up to 2 tiles ahead.
@@ -285,7 +322,7 @@ __device__ __forceinline__ void pv_loop(const AttnArgs &a, uint8_t *smem, uint32
     auto bar = [&](int i) { return bars + 8u * i; };
     constexpr uint32_t idesc_pv = idesc_bf16_f32(kBM, D, false, true);
     const uint64_t v_desc = sdesc_sw128(sbase + C::v_off, kBN * 128, 1024);
-    int ic = 0, vc = 0, g = 0;
+    int ic = 0, vc = 0, g = 0, items = 0;
     ItemInfo info;
     while (next_item<D>(bars, items_s, ic, info, abort, a.status)) {
         const int slot = (ic - 1) & 1;
@@ -293,6 +330,10 @@ __device__ __forceinline__ void pv_loop(const AttnArgs &a, uint8_t *smem, uint32
             if (lane == 0) mbar_arrive(bar(C::B_ITEM_EMPTY + slot));
             continue;
         }
+        // The first PV of an item overwrites O: every softmax warp must have
+        // read the previous item's O first.
+        if (items > 0 && !mbar_wait(bar(C::B_O_FREE), (items - 1) & 1, abort, a.status)) return;
+        ++items;
         const int nt = info.te - info.tb;
         for (int j = 0; j < nt; ++j, ++vc, ++g) {
             const int vs = vc % C::NV, sb = g % C::NS;
@@ -321,52 +362,109 @@ __device__ __forceinline__ void pv_loop(const AttnArgs &a, uint8_t *smem, uint32
             tc_fence_after();
             __syncwarp();
             const uint64_t b0 = v_desc + ((vs * C::kTileBytes) >> 4);
+            // P of keys 16kk..16kk+15: bf16 pairs at S columns 8kk..8kk+7
 #pragma unroll
             for (int kk = 0; kk < kBN / 16; ++kk)
                 mma_ts(tmem + C::kColO, tmem + sb * 128 + kk * 8, b0 + ((kk * 2048) >> 4), idesc_pv,
                        (j > 0 || kk > 0) ? 1u : 0u);
             mma_commit(bar(C::B_S_FREE + sb));
             mma_commit(bar(C::B_V_EMPTY + vs));
-            mma_commit(bar(C::B_O_DONE));
         }
         if (lane == 0) mbar_arrive(bar(C::B_ITEM_EMPTY + slot));
     }
 }
 
-// Softmax and epilogue. Row r of the unit (TMEM lane r) is shared by two
-// warps: warp q handles S columns 0-63 and warp q + 4 columns 64-127 (both
-// reach lanes 32q..32q+31). They exchange their partial row max (each tile)
-// and row sum (each epilogue) through shared memory, synchronising on a
-// bounded mbarrier. Each exchange uses its own parity slot, so a warp that
-// runs ahead cannot overwrite a value its partner has not read yet.
+// Softmax and epilogue. The two warps of a row quadrant (q and q + 4, both
+// on TMEM lanes 32q..32q+31) take alternate key tiles: warp q + 4p owns the
+// tiles of global index g with g % 2 == p and does the whole 128-column row
+// of its tiles. One warp's TMEM-load and reduction latency then overlaps the
+// other's ex2 work, instead of both warps running the same phase together.
+//
+// The running max is the one piece of state that crosses tiles. The owner of
+// tile g publishes m(g) to its partner right after its row max (hand-off slot
+// g % 2 of the quadrant, a bounded mbarrier); the owner of tile g + 1 reads it
+// before its exps. Each warp keeps its own part of the row sum, l_own, with
+// the reference max it is expressed in; the two parts are merged in the
+// epilogue. O is rescaled, when needed, by the owner of the tile that raised
+// the max, after the PV of the previous tile has completed.
+//
+// The warp holds the tile's whole 128-key row in registers (one TMEM load);
+// the softmax warpgroups get 224 registers per thread for it (setmaxnreg),
+// the producer and issuer warpgroup 56. P (bf16 pairs) goes back over the S
+// columns 0-63 of its buffer.
 template <int D>
 __device__ __forceinline__ void softmax_loop(const Layout &L, const AttnArgs &a, uint32_t bars,
-                                             const ItemInfo *items_s, float *xchg, uint32_t tmem,
+                                             const ItemInfo *items_s, float *hand, float *xchg, uint32_t tmem,
                                              volatile int *abort) {
     using C = AttnCfg<D>;
-    constexpr int kHalf = kBN / 2;                  // S columns per warp
-    constexpr int kOHalf = D / 2;                   // O columns per warp
+    constexpr int kHalf = kBN / 2;                  // keys per TMEM load
+    constexpr int kOHalf = D / 2;                   // O columns per warp in the epilogue
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int q = warp & 3, hh = warp >> 2;         // row quadrant, column half
+    const int q = warp & 3, par = warp >> 2;        // row quadrant, tile parity (= epilogue column half)
     const int r = q * 32 + lane;                    // stacked row = TMEM lane
     auto bar = [&](int i) { return bars + 8u * i; };
     const uint32_t t_row = tmem + ((uint32_t)(q * 32) << 16);
-    const uint32_t t_o = t_row + C::kColO + hh * kOHalf;
+    const uint32_t t_o = t_row + C::kColO;
     const uint32_t *masks = reinterpret_cast<const uint32_t *>(a.ws + L.mask_off);
     float *opart = reinterpret_cast<float *>(a.ws + L.opart_off);
     float2 *mlpart = reinterpret_cast<float2 *>(a.ws + L.ml_off);
+    float *hand_q = hand + q * 64;
     const float sl2 = a.scale_log2;
     int ic = 0, g = 0, xc = 0;
-    // Exchange one float with the partner warp: returns false on abort.
-    auto exchange = [&](float mine, float &theirs) -> bool {
-        const int par = xc & 1;
-        xchg[(par * 2 + hh) * kRows + r] = mine;
+
+    auto publish = [&](int gg, float m) {
+        hand_q[(gg & 1) * 32 + lane] = m;
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(C::B_PAIR + q));
-        const bool ok = mbar_wait(bar(C::B_PAIR + q), xc & 1, abort, a.status);
-        ++xc;
-        theirs = xchg[(par * 2 + (hh ^ 1)) * kRows + r];
-        return ok;
+        if (lane == 0) mbar_arrive(bar(C::B_HAND + q * 2 + (gg & 1)));
+    };
+    auto receive = [&](int gg, float &m) -> bool {
+        if (!mbar_wait(bar(C::B_HAND + q * 2 + (gg & 1)), (gg >> 1) & 1, abort, a.status)) return false;
+        m = hand_q[(gg & 1) * 32 + lane];
+        return true;
+    };
+    // PV of tile gg has completed (its S buffer was handed back).
+    auto wait_pv = [&](int gg) {
+        return mbar_wait(bar(C::B_S_FREE + gg % C::NS), (gg / C::NS) & 1, abort, a.status);
+    };
+    // -inf on keys this row may not see: not an ancestor (tree tile, one mask
+    // bit per key) or past the prefix length (lim keys valid).
+    auto mask128 = [&](uint32_t (&sv)[kBN], bool tree, const uint4 &mw, int lim) {
+        if (tree) {
+            const uint32_t w[4] = {mw.x, mw.y, mw.z, mw.w};
+#pragma unroll
+            for (int c = 0; c < kBN; ++c)
+                if (!((w[c >> 5] >> (c & 31)) & 1u)) sv[c] = __float_as_uint(kNegInf);
+        } else if (lim < kBN) {
+#pragma unroll
+            for (int c = 0; c < kBN; ++c)
+                if (c >= lim) sv[c] = __float_as_uint(kNegInf);
+        }
+    };
+    auto max128 = [&](const uint32_t (&sv)[kBN]) {
+        float m4[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) m4[k] = __uint_as_float(sv[k]);
+#pragma unroll
+        for (int c = 4; c < kBN - 4; c += 8)
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                m4[k] = max3f(m4[k], __uint_as_float(sv[c + k]), __uint_as_float(sv[c + 4 + k]));
+#pragma unroll
+        for (int k = 0; k < 4; ++k) m4[k] = fmaxf(m4[k], __uint_as_float(sv[kBN - 4 + k]));
+        return fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+    };
+    // P = 2^(s * sl2 - m) of keys h*64..h*64+63 as bf16 pairs; returns their fp32 sum.
+    auto exp64 = [&](const uint32_t (&sv)[kBN], int h, float neg_m, uint32_t (&pv)[kHalf / 2]) {
+        float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int c = 0; c < kHalf; c += 2) {
+            const float p0 = ex2_approx(fmaf(__uint_as_float(sv[h * kHalf + c]), sl2, neg_m));
+            const float p1 = ex2_approx(fmaf(__uint_as_float(sv[h * kHalf + c + 1]), sl2, neg_m));
+            sum4[c & 3] += p0;
+            sum4[(c + 1) & 3] += p1;
+            pv[c >> 1] = pack_bf16x2(p0, p1);
+        }
+        return (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
     };
 
     while (true) {
@@ -384,119 +482,94 @@ __device__ __forceinline__ void softmax_loop(const Layout &L, const AttnArgs &a,
         const int head = info.kh * L.G + r % L.G;
         const bool row_valid = node < info.n;
         const uint32_t *mrow = masks + ((size_t)info.b * L.Nmax + (row_valid ? node : 0)) * L.W4;
-        float m_run = kNegInf, l_part = 0.f;
+        float m_run = kNegInf;                      // reference of O after this warp's last tile
+        float m_own = kNegInf, l_own = 0.f;         // this warp's part of the row sum, and its reference
         const int nt = info.te - info.tb;
         bool fail = false;
-        for (int j = 0; j < nt; ++j) {
+        for (int j = 0; j < nt; ++j, ++g) {
+            if ((g & 1) != par) continue;                  // the partner's tile
             const int t = info.tb + j;
             const bool tree = t >= info.t_pre;
-            uint2 mw = make_uint2(0u, 0u);             // mask words of this warp's 64 keys
-            if (tree && row_valid) mw = *reinterpret_cast<const uint2 *>(mrow + 4 * (t - info.t_pre) + 2 * hh);
+            uint4 mw = make_uint4(0u, 0u, 0u, 0u);         // ancestor bits of the tile's 128 keys
+            if (tree && row_valid) mw = *reinterpret_cast<const uint4 *>(mrow + 4 * (t - info.t_pre));
+            const int lim = (!tree && t == info.t_pre - 1) ? info.P - t * kBN : kBN;
             const int sb = g % C::NS;
             const uint32_t t_s = t_row + sb * 128;
             if (!mbar_wait(bar(C::B_S_FULL + sb), (g / C::NS) & 1, abort, a.status)) { fail = true; break; }
             tc_fence_after();
-            uint32_t sv[kHalf];
-            tmem_ld64(t_s + hh * kHalf, sv);
-            float sr[kHalf];
-#pragma unroll
-            for (int c = 0; c < kHalf; ++c) sr[c] = __uint_as_float(sv[c]);
-            if (tree) {                                    // ancestors only (1-2 tiles per item)
-                const uint32_t w2[2] = {mw.x, mw.y};
-#pragma unroll
-                for (int c = 0; c < kHalf; ++c)
-                    if (!((w2[c >> 5] >> (c & 31)) & 1u)) sr[c] = kNegInf;
-            } else if (t == info.t_pre - 1) {
-                const int lim = info.P - t * kBN - hh * kHalf;   // valid keys of this half
-                if (lim < kHalf) {
-#pragma unroll
-                    for (int c = 0; c < kHalf; ++c)
-                        if (c >= lim) sr[c] = kNegInf;
-                }
+            uint32_t sv[kBN];                              // the whole row of the tile
+            tmem_ld128(t_s, sv);
+            mask128(sv, tree, mw, lim);
+            const float mt = max128(sv) * sl2;
+            float m_new = mt, m_prev = kNegInf;
+            bool need = false;
+            if (j > 0) {
+                if (!receive(g - 1, m_prev)) { fail = true; break; }
+                m_new = fmaxf(m_prev, mt);
+                need = m_new > m_prev + 8.0f;              // lazy: O keeps m_prev unless it grows > 2^8
+                if (!need) m_new = m_prev;
             }
-            float m4[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) m4[k] = sr[k];
-#pragma unroll
-            for (int c = 4; c < kHalf; c += 8)
-#pragma unroll
-                for (int k = 0; k < 4; ++k) m4[k] = max3f(m4[k], sr[c + k], sr[c + 4 + k]);
-            const float mine = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-            float theirs;
-            if (!exchange(mine, theirs)) { fail = true; break; }
-            // Both warps of the row hold the same inputs from here, so they take
-            // the same lazy-rescale decisions and keep the same m_run.
-            const float mt = fmaxf(mine, theirs) * sl2;
-            bool waited_o = false;
-            if (j == 0) {
-                m_run = mt;
-            } else {
-                const float m_new = fmaxf(m_run, mt);
-                const bool need = m_new > m_run + 8.0f;
+            publish(g, m_new);                             // the partner's next tile can go on
+            if (j > 0) {
                 if (__any_sync(0xffffffffu, need)) {
-                    // O holds PV of the previous tile: wait for it, then rescale
-                    // this warp's half of the row in place.
-                    if (!mbar_wait(bar(C::B_O_DONE), (g - 1) & 1, abort, a.status)) { fail = true; break; }
-                    waited_o = true;
+                    // O holds PV up to the previous tile: wait for it, then
+                    // rescale the quadrant's rows in place.
+                    if (!wait_pv(g - 1)) { fail = true; break; }
                     tc_fence_after();
-                    const float alpha = need ? ex2_approx(m_run - m_new) : 1.0f;
+                    const float alpha = need ? ex2_approx(m_prev - m_new) : 1.0f;
 #pragma unroll 1
-                    for (int c = 0; c < kOHalf / 32; ++c) {
+                    for (int c = 0; c < D / 32; ++c) {
                         uint32_t v[32];
                         tmem_ld32(t_o + c * 32, v);
 #pragma unroll
                         for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * alpha);
                         tmem_st32(t_o + c * 32, v);
                     }
-                    if (need) {
-                        l_part *= alpha;
-                        m_run = m_new;
-                    }
                 }
             }
+            m_run = m_new;
+            if (m_own != m_run) {                          // bring l_own to the new reference
+                l_own *= ex2_approx(m_own - m_run);        // l_own = 0 while m_own = -inf
+                m_own = m_run;
+            }
             const float neg_m = (m_run == kNegInf) ? 0.f : -m_run;
-            float sum4[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) sum4[k] = 0.f;
             uint32_t pv[kHalf / 2];
-#pragma unroll
-            for (int c = 0; c < kHalf; c += 2) {
-                const float p0 = ex2_approx(fmaf(sr[c], sl2, neg_m));
-                const float p1 = ex2_approx(fmaf(sr[c + 1], sl2, neg_m));
-                sum4[c & 3] += p0;
-                sum4[(c + 1) & 3] += p1;
-                pv[c >> 1] = pack_bf16x2(p0, p1);
-            }
-            // P (bf16 pairs) of keys 64*hh.. goes to S columns 32*hh..32*hh+31.
-            // The partner's S columns there were read before the exchange.
-            tmem_st32(t_s + hh * (kHalf / 2), pv);
-            l_part += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
+            float lsum = exp64(sv, 0, neg_m, pv);
+            tmem_st32(t_s, pv);                            // P of keys 0-63 -> S columns 0-31
+            lsum += exp64(sv, 1, neg_m, pv);
+            tmem_st32(t_s + 32, pv);                       // P of keys 64-127 -> S columns 32-63
+            l_own += lsum;
             tmem_wait_st();
-            // PV(g-1) must be complete before P(g) is released: O is then
-            // stable for any rescale, and each o_done wait stays within one
-            // phase of its barrier.
-            if (j > 0 && !waited_o) {
-                if (!mbar_wait(bar(C::B_O_DONE), (g - 1) & 1, abort, a.status)) { fail = true; break; }
-            }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(C::B_P_FULL + sb));
-            ++g;
         }
         if (fail) break;
-        // Epilogue: the last PV of this item is the last o_done phase.
-        if (!mbar_wait(bar(C::B_O_DONE), (g - 1) & 1, abort, a.status)) break;
+        // Epilogue. The final max is m(g_last), published by the last tile's
+        // owner; the partner is the reader its hand-off slot expects.
+        const int g_last = g - 1;
+        float m_fin = m_run;
+        if ((g_last & 1) != par && !receive(g_last, m_fin)) break;
+        const float l_mine = (m_own == m_fin) ? l_own : l_own * ex2_approx(m_own - m_fin);
+        // The last PV of the item has completed: O is final, and the partner
+        // cannot reach its next epilogue (which would reuse xchg) before this
+        // warp has read xchg and released O.
+        if (!wait_pv(g_last)) break;
         tc_fence_after();
-        float l_other;
-        if (!exchange(l_part, l_other)) break;
-        const float l_run = l_part + l_other;
+        xchg[par * kRows + r] = l_mine;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(C::B_PAIR + q));
+        if (!mbar_wait(bar(C::B_PAIR + q), xc & 1, abort, a.status)) break;
+        ++xc;
+        const float l_run = l_mine + xchg[(par ^ 1) * kRows + r];
+        const uint32_t t_oh = t_o + par * kOHalf;
         if (info.ns <= 1) {
-            __nv_bfloat16 *dst = a.out + (((size_t)info.b * L.Nmax + node) * L.Hq + head) * D + hh * kOHalf;
+            __nv_bfloat16 *dst = a.out + (((size_t)info.b * L.Nmax + node) * L.Hq + head) * D + par * kOHalf;
             const float inv_l = 1.0f / l_run;
 #pragma unroll 1
             for (int c = 0; c < kOHalf / 32; ++c) {
                 uint32_t v[32];
-                tmem_ld32(t_o + c * 32, v);
+                tmem_ld32(t_oh + c * 32, v);
                 if (row_valid) {
                     uint4 *d4 = reinterpret_cast<uint4 *>(dst + c * 32);
                     auto f = [&](int e) { return __uint_as_float(v[e]) * inv_l; };
@@ -508,21 +581,24 @@ __device__ __forceinline__ void softmax_loop(const Layout &L, const AttnArgs &a,
                 }
             }
         } else {
-            float4 *d4 = reinterpret_cast<float4 *>(opart + ((size_t)info.slot * kRows + r) * D + hh * kOHalf);
+            float4 *d4 = reinterpret_cast<float4 *>(opart + ((size_t)info.slot * kRows + r) * D + par * kOHalf);
 #pragma unroll 1
             for (int c = 0; c < kOHalf / 32; ++c) {
                 uint32_t v[32];
-                tmem_ld32(t_o + c * 32, v);
+                tmem_ld32(t_oh + c * 32, v);
 #pragma unroll
                 for (int k = 0; k < 8; ++k)
                     d4[8 * c + k] = make_float4(__uint_as_float(v[4 * k]), __uint_as_float(v[4 * k + 1]),
                                                 __uint_as_float(v[4 * k + 2]), __uint_as_float(v[4 * k + 3]));
             }
-            if (hh == 0) mlpart[(size_t)info.slot * kRows + r] = make_float2(m_run, l_run);
+            if (par == 0) mlpart[(size_t)info.slot * kRows + r] = make_float2(m_fin, l_run);
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(C::B_ITEM_EMPTY + slot));
+        if (lane == 0) {
+            mbar_arrive(bar(C::B_O_FREE));
+            mbar_arrive(bar(C::B_ITEM_EMPTY + slot));
+        }
     }
 }
 
@@ -551,14 +627,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < C::NS; ++s) {
             init(C::B_S_FULL + s, 1);
             init(C::B_S_FREE + s, 1);
-            init(C::B_P_FULL + s, kSoftmaxWarps);          // one arrival per softmax warp
+            init(C::B_P_FULL + s, kSoftmaxWarps / 2);      // the tile's owner in each row quadrant
         }
-        init(C::B_O_DONE, 1);
+        init(C::B_O_FREE, kSoftmaxWarps);
         for (int s = 0; s < 2; ++s) {
             init(C::B_ITEM_FULL + s, 1);
-            init(C::B_ITEM_EMPTY + s, 2 + kSoftmaxWarps);  // both issuers + every softmax warp
+            init(C::B_ITEM_EMPTY + s, 3 + kSoftmaxWarps);  // both issuers, the V producer, every softmax warp
         }
         for (int q = 0; q < 4; ++q) init(C::B_PAIR + q, 2); // the two warps that share a row quadrant
+        for (int h = 0; h < 8; ++h) init(C::B_HAND + h, 1); // row-max hand-off, [quadrant][tile parity]
         *abort = 0;
         fence_mbar_init();
     }
@@ -579,15 +656,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     // now: it waits for this grid before it reads any partial.
     pdl_wait_prior_grid();
     pdl_launch_dependents();
-
-    if (warp == kProducerWarp)
-        producer_loop<D>(maps, L, a, sbase, bars, items_s, abort);
-    else if (warp == kQkWarp)
-        qk_loop<D>(a, sbase, bars, items_s, tmem, abort);
-    else if (warp == kPvWarp)
-        pv_loop<D>(a, smem, sbase, bars, items_s, tmem, abort);
-    else
-        softmax_loop<D>(L, a, bars, items_s, reinterpret_cast<float *>(smem + C::xchg_off), tmem, abort);
+    // 256 x 224 + 128 x 56 = 384 x 168, the registers the block launched with
+    // (the host refuses to launch a build that uses any other count).
+    if (warp >= kSoftmaxWarps) {
+        setmaxnreg_dec<kOtherRegs>();
+        if (warp == kProducerWarp)
+            producer_loop<D>(maps, L, a, sbase, bars, items_s, abort);
+        else if (warp == kQkWarp)
+            qk_loop<D>(a, sbase, bars, items_s, tmem, abort);
+        else if (warp == kPvWarp)
+            pv_loop<D>(a, smem, sbase, bars, items_s, tmem, abort);
+        else if (warp == kVProducerWarp)
+            v_producer_loop<D>(maps, L, a, sbase, bars, items_s, abort);
+    } else {
+        setmaxnreg_inc<kSoftmaxRegs>();
+        softmax_loop<D>(L, a, bars, items_s, reinterpret_cast<float *>(smem + C::hand_off),
+                        reinterpret_cast<float *>(smem + C::xchg_off), tmem, abort);
+    }
 
     tc_fence_before();
     __syncthreads();
@@ -604,6 +689,12 @@ cudaError_t launch_d(const Layout &L, const AttnMaps &m, const AttnArgs &a, cuda
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (configured_device != dev) {
+        // setmaxnreg hands out exactly the registers the block launched with;
+        // a build with another per-thread count would make it wait forever.
+        cudaFuncAttributes fa{};
+        e = cudaFuncGetAttributes(&fa, tree_attention_kernel<D>);
+        if (e != cudaSuccess) return e;
+        if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
         e = cudaFuncSetAttribute(tree_attention_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)C::smem_request);
         if (e != cudaSuccess) return e;

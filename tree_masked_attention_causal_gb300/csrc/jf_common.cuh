@@ -319,6 +319,17 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&v)[64]) {
         : "memory");
 }
 
+// Per-warpgroup register budget (all 128 threads of the warpgroup execute
+// it). The launch's total (threads x registers per thread) is the pool.
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // Store 64 consecutive 32-bit columns of this thread's TMEM lane.
 __device__ __forceinline__ void tmem_st64(uint32_t taddr, const uint32_t (&v)[64]) {
     asm volatile(
