@@ -300,7 +300,7 @@ def run_gpu(args, rank, world, local):
     for k, name in enumerate(trace_names):
         per.setdefault(name, []).append(events[2 * k].elapsed_time(events[2 * k + 1]))
     avg = {n: statistics.mean(v) for n, v in per.items()}
-    attn_ms = sum(avg.get(n, 0.0) for n in ("tree_prep", "tree_attention"))
+    attn_ms = sum(avg.get(n, 0.0) for n in ("tree_prep", "tree_attention", "split_combine"))
     verify_ms = sum(avg.get(n, 0.0) for n in ("argmax_chunk", "accept_walk"))
 
     # e2e through the public calls: pinned host inputs, H2D every step, D2H results

@@ -75,6 +75,10 @@ int32_t check_shape(const jf_shape *s, bool need_vocab, bool need_attn) {
         // 32-bit index arithmetic in the kernels
         if ((long long)s->batch * s->max_nodes * s->n_q_heads * s->head_dim > 0x7FFFFFFFll) return JF_ERR_SHAPE;
         if ((long long)s->batch * s->n_kv_heads * s->prefix_cap > 0x7FFFFFFFll) return JF_ERR_SHAPE;
+        // the stream-K plan counts key tiles of all work units in 32 bits
+        const long long units = (long long)s->batch * s->n_kv_heads * ((s->max_nodes * G + kRows - 1) / kRows);
+        if (units * ((s->prefix_cap + kBN - 1) / kBN + (s->max_nodes + kBN - 1) / kBN) > 0x7FFFFFFFll)
+            return JF_ERR_SHAPE;
     }
     if (need_vocab) {
         if (s->vocab < 8 || s->vocab % 8) return JF_ERR_SHAPE;
@@ -128,17 +132,18 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// 3-D bf16 map, 128-byte swizzle, zero fill out of bounds. dims/box are
+// 3-D 16-bit map, 128-byte swizzle, zero fill out of bounds. dims/box are
 // innermost first; strides are the byte strides of dims 1 and 2.
 bool encode3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1, uint64_t s2,
-              uint32_t b0, uint32_t b1, uint32_t b2) {
+              uint32_t b0, uint32_t b1, uint32_t b2,
+              CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[3] = {d0, d1, d2};
     const cuuint64_t strides[2] = {s1, s2};
     const cuuint32_t box[3] = {b0, b1, b2};
     const cuuint32_t estr[3] = {1, 1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+    return fn(m, dtype, 3, const_cast<void *>(base), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -197,6 +202,9 @@ JF_API int32_t jf_tree_attention(const void *q, const void *k_cache, const void 
     ok = ok && encode3d(&maps.v_cache, v_cache, D, Pcap, (uint64_t)B * Hkv, e2 * D, e2 * D * Pcap, 64, kBN, 1);
     ok = ok && encode3d(&maps.tree_k, tree_k, D, Hkv, (uint64_t)B * N, e2 * D, e2 * D * Hkv, 64, 1, kBN);
     ok = ok && encode3d(&maps.tree_v, tree_v, D, Hkv, (uint64_t)B * N, e2 * D, e2 * D * Hkv, 64, 1, kBN);
+    ok = ok && encode3d(&maps.out, out, D, Hq, (uint64_t)B * N, e2 * D, e2 * D * Hq, 64, L.G, L.NB);
+    ok = ok && encode3d(&maps.part, static_cast<uint8_t *>(workspace) + L.opart_off, D, kRows, L.max_pieces, e2 * D,
+                        e2 * D * kRows, 64, kRows, 1, CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
     if (!ok) return JF_ERR_CUDA;
 
     AttnArgs args;
@@ -211,7 +219,6 @@ JF_API int32_t jf_tree_attention(const void *q, const void *k_cache, const void 
     args.num_ctas = sms < kMaxCtas ? sms : kMaxCtas;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (launch_tree_prep(L, args, s) != cudaSuccess) return JF_ERR_CUDA;
     if (launch_tree_attention(L, maps, args, s) != cudaSuccess) return JF_ERR_CUDA;
     if (launch_split_combine(L, args, s) != cudaSuccess) return JF_ERR_CUDA;
     return JF_OK;

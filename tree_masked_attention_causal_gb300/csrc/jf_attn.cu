@@ -16,14 +16,16 @@
 //    (from k_cache/v_cache) followed by ceil(n_hi/128) dense tree tiles (from
 //    tree_k/tree_v). Here n_hi is one past the unit's highest node, and
 //    parents[i] < i means no key above a node is ever its ancestor. The
-//    ancestor bitmask (built by the prep kernel) masks the tree tiles in
-//    registers; a key-count bound masks the ragged last prefix tile.
-//  * Stream-K split of the keys. The prep kernel concatenates every unit's
-//    key tiles and gives each CTA an equal contiguous range. A CTA walks its
-//    range as one or a few items (one per unit it touches). A unit covered
-//    by a single range is normalised and written as bf16 here. Every piece of
-//    a unit covered by several ranges writes fp32 (O, m, l) partials, which
-//    the combine kernel merges.
+//    ancestor bits of a tree tile come from a walk up the parents array and
+//    mask the tile in registers; a key-count bound masks the ragged last
+//    prefix tile.
+//  * Stream-K split of the keys. Each CTA derives the plan itself from
+//    prefix_lens and n_nodes: every unit's key tiles concatenated, and an
+//    equal contiguous range per CTA. A CTA walks its range as one or a few
+//    items (one per unit it touches). A unit covered by a single range is
+//    normalised and written as bf16 here. Every piece of a unit covered by
+//    several ranges writes fp32 (O, m, l) partials, which the combine kernel
+//    merges; the CTA where a unit starts records the unit's split plan.
 //  * One CTA per SM, 12 warps:
 //      warps 0-7  softmax: warp w owns TMEM lanes 32 (w % 4).. (rows) for
 //                 the key tiles g with g % 2 == w / 4; the two warps of a
@@ -50,9 +52,9 @@
 //    when a row max grows by more than 2^8, by the owner of that tile, once
 //    the previous tile's PV has completed. The first PV of an item waits
 //    until every softmax warp has read the previous item's O.
-//  * Launched as a programmatic dependent of the prep kernel: barrier init,
-//    TMEM allocation and tensor-map prefetch overlap it, and every thread
-//    waits (griddepcontrol.wait) before reading the plan or the masks.
+//  * Nothing runs before it: its first TMA loads start at launch.
+//    Tree validation and the NaN rows of malformed sequences are left to the
+//    combine kernel, which overwrites whatever this kernel wrote for them.
 //  * Rows of padding nodes are computed but never stored. V rows past the
 //    prefix length or past n_nodes are zeroed in shared memory before the
 //    PV MMA, so NaN in unused cache rows cannot reach an output.
@@ -62,7 +64,7 @@ namespace jf {
 namespace {
 
 struct ItemInfo {
-    int32_t valid, skip, b, kh, qt, tb, te, t_pre, P, n, ns, slot, qtile, split, pad0, pad1;
+    int32_t valid, b, kh, qt, tb, te, t_pre, P, n, ns, slot, qtile, pad0, pad1, pad2, pad3;
 };
 
 template <int D>
@@ -83,7 +85,7 @@ struct AttnCfg {
                          B_V_FULL = B_K_EMPTY + NK, B_V_EMPTY = B_V_FULL + NV, B_S_FULL = B_V_EMPTY + NV,
                          B_S_FREE = B_S_FULL + NS, B_P_FULL = B_S_FREE + NS, B_O_FREE = B_P_FULL + NS,
                          B_ITEM_FULL = B_O_FREE + 1, B_ITEM_EMPTY = B_ITEM_FULL + 2, B_PAIR = B_ITEM_EMPTY + 2,
-                         B_HAND = B_PAIR + 4, N_BARS = B_HAND + 8;
+                         B_HAND = B_PAIR + 4, B_EPI = B_HAND + 8, N_BARS = B_EPI + 1;
     static constexpr uint32_t item_off = bar_off + ((N_BARS * 8 + 15) / 16) * 16;
     static constexpr uint32_t hand_off = item_off + 2 * sizeof(ItemInfo);   // float [4 quadrants][2 slots][32]
     static constexpr uint32_t xchg_off = hand_off + 4 * 2 * 32 * sizeof(float);   // float [2 warps][128 rows]
@@ -122,47 +124,77 @@ __device__ __forceinline__ void producer_loop(const AttnMaps &maps, const Layout
                                               volatile int *abort) {
     using C = AttnCfg<D>;
     const int lane = threadIdx.x & 31;
-    const PlanHeader hdr = *reinterpret_cast<const PlanHeader *>(a.ws + L.plan_off);
-    const SeqInfo *seqs = reinterpret_cast<const SeqInfo *>(a.ws + L.seq_off);
-    const QTile *qtab = reinterpret_cast<const QTile *>(a.ws + L.qtab_off);
+    QTile *qtab = reinterpret_cast<QTile *>(a.ws + L.qtab_off);
     auto bar = [&](int i) { return bars + 8u * i; };
-    // This CTA's stream-K range of the concatenated unit tiles.
-    const int c = blockIdx.x, n_ctas = hdr.n_ctas, total = hdr.total_tiles;
-    long long lo = c < n_ctas ? (long long)c * total / n_ctas : 0;
-    const long long hi = c < n_ctas ? (long long)(c + 1) * total / n_ctas : 0;
-    int u = lo < hi ? reinterpret_cast<const int32_t *>(a.ws + L.first_off)[c] : 0;
+    // This CTA's stream-K range of the concatenated unit tiles, derived here
+    // from prefix_lens and n_nodes (no earlier kernel needed).
+    const int c = blockIdx.x;
+    const PlanSeq ps = plan_locate(L, a.prefix_lens, a.n_nodes, c, a.num_ctas);
+    const int total = ps.total, n_ctas = ps.n_ctas;
+    const long long lo0 = ps.lo, hi = ps.hi;
+    long long lo = lo0;
+    // The unit (b, kh, qt) holding tile lo, and its first tile S.
+    int b = ps.b, kh = 0, qt = 0, P = ps.P, n = ps.n;
+    long long S = 0;
+    if (lo < hi) {
+        if (b < 0) {
+            lo = hi;                        // unreachable for a consistent plan
+        } else {
+            const int th = head_tiles(P, n, L);
+            kh = (int)((lo - ps.seq_start) / th);
+            S = ps.seq_start + (long long)kh * th;
+            for (int ut = unit_tiles(P, n, 0, L); S + ut <= lo && qt + 1 < L.QT; ut = unit_tiles(P, n, qt, L)) {
+                S += ut;
+                ++qt;
+            }
+        }
+    }
     int ic = 0, qc = 0, kc = 0;
     bool ok = true;
     while (ok) {
         const int slot = ic & 1;
         if (!mbar_wait(bar(C::B_ITEM_EMPTY + slot), ((ic >> 1) & 1) ^ 1, abort, a.status)) break;
         ItemInfo info{};
-        QTile q{};
         if (lo < hi) {
-            q = qtab[u];
-            while (q.tiles == 0) q = qtab[++u];          // units without work
-        }
-        if (lo < hi) {
-            const int per_b = L.Hkv * L.QT;
+            const int T = unit_tiles(P, n, qt, L);
+            const int u = (b * L.Hkv + kh) * L.QT + qt;
             info.valid = 1;
             info.qtile = u;
-            info.b = u / per_b;
-            const int rem = u - info.b * per_b;
-            info.kh = rem / L.QT;
-            info.qt = rem - info.kh * L.QT;
-            info.tb = (int)(lo - q.tile_start);
-            info.te = (int)(min(hi, (long long)q.tile_start + q.tiles) - q.tile_start);
-            const SeqInfo si = seqs[info.b];
-            info.skip = si.bad;
-            info.P = si.prefix_len;
-            info.n = si.n_nodes;
-            info.t_pre = ceil_div(si.prefix_len, kBN);
-            info.ns = q.n_splits;
-            const int c_first = (int)(((long long)(q.tile_start + 1) * n_ctas - 1) / total);
-            info.split = c - c_first;
-            info.slot = q.n_splits > 1 ? q.slot_base + info.split : -1;
-            lo = (long long)q.tile_start + info.te;
-            ++u;
+            info.b = b;
+            info.kh = kh;
+            info.qt = qt;
+            info.tb = (int)(lo - S);
+            info.te = (int)(min(hi, S + T) - S);
+            info.P = P;
+            info.n = n;
+            info.t_pre = ceil_div(P, kBN);
+            const int c_first = cta_of_tile(S, total, n_ctas);
+            info.ns = cta_of_tile(S + T - 1, total, n_ctas) - c_first + 1;
+            // A split unit is at most this CTA's first item (slot 2c) or its
+            // last (slot 2c + 1): units in between lie wholly in the range.
+            info.slot = info.ns > 1 ? 2 * c + (ic > 0 ? 1 : 0) : -1;
+            if (S >= lo0 && lane == 0)      // the unit starts in this range: record its split plan
+                qtab[u] = QTile{info.ns, c, S == lo0 ? 1 : 0, (int)S};
+            lo = S + info.te;
+            S += T;
+            if (lo < hi) {                  // the next unit with tiles
+                if ((qt + 1) * L.NB < n) {
+                    ++qt;
+                } else {
+                    qt = 0;
+                    if (kh + 1 < L.Hkv) {
+                        ++kh;
+                    } else {
+                        kh = 0;
+                        for (++b; b < L.B; ++b) {
+                            P = a.prefix_lens[b];
+                            n = a.n_nodes[b];
+                            if (seq_valid(P, n, L)) break;
+                        }
+                        if (b >= L.B) lo = hi;  // unreachable for a consistent plan
+                    }
+                }
+            }
         }
         if (lane == 0) {
             items_s[slot] = info;
@@ -171,7 +203,6 @@ __device__ __forceinline__ void producer_loop(const AttnMaps &maps, const Layout
         __syncwarp();
         ++ic;
         if (!info.valid) break;
-        if (info.skip) continue;
         // Q: 128 stacked rows (G heads x 128/G nodes), one box per 64 d, into
         // buffer qc % NQ so that it can land while the previous unit runs.
         const int qb = qc % C::NQ;
@@ -238,7 +269,7 @@ __device__ __forceinline__ void v_producer_loop(const AttnMaps &maps, const Layo
     bool ok = true;
     while (ok && next_item<D>(bars, items_s, ic, info, abort, a.status)) {
         const int slot = (ic - 1) & 1;
-        if (!info.skip) {
+        {
             for (int t = info.tb; t < info.te; ++t) {
                 const bool tree = t >= info.t_pre;
                 const int vs = vc % C::NV;
@@ -284,10 +315,6 @@ __device__ __forceinline__ void qk_loop(const AttnArgs &a, uint32_t sbase, uint3
     ItemInfo info;
     while (next_item<D>(bars, items_s, ic, info, abort, a.status)) {
         const int slot = (ic - 1) & 1;
-        if (info.skip) {
-            if (lane == 0) mbar_arrive(bar(C::B_ITEM_EMPTY + slot));
-            continue;
-        }
         const int qb = qc % C::NQ;
         if (!mbar_wait(bar(C::B_Q_FULL + qb), (qc / C::NQ) & 1, abort, a.status)) return;
         ++qc;
@@ -306,7 +333,6 @@ __device__ __forceinline__ void qk_loop(const AttnArgs &a, uint32_t sbase, uint3
                        b0 + (((kk >> 2) * (kBN * 128) + (kk & 3) * 32) >> 4), idesc_qk, kk > 0 ? 1u : 0u);
             mma_commit(bar(C::B_S_FULL + sb));
             mma_commit(bar(C::B_K_EMPTY + ks));
-            if (j == nt - 1) mma_commit(bar(C::B_Q_EMPTY + qb));
         }
         if (lane == 0) mbar_arrive(bar(C::B_ITEM_EMPTY + slot));
     }
@@ -326,10 +352,6 @@ __device__ __forceinline__ void pv_loop(const AttnArgs &a, uint8_t *smem, uint32
     ItemInfo info;
     while (next_item<D>(bars, items_s, ic, info, abort, a.status)) {
         const int slot = (ic - 1) & 1;
-        if (info.skip) {
-            if (lane == 0) mbar_arrive(bar(C::B_ITEM_EMPTY + slot));
-            continue;
-        }
         // The first PV of an item overwrites O: every softmax warp must have
         // read the previous item's O first.
         if (items > 0 && !mbar_wait(bar(C::B_O_FREE), (items - 1) & 1, abort, a.status)) return;
@@ -374,6 +396,32 @@ __device__ __forceinline__ void pv_loop(const AttnArgs &a, uint8_t *smem, uint32
     }
 }
 
+// Ancestor mask ("JetFlow: Scaling Speculative Decoding with Parallel Tree
+// Drafting", blog, section "What JetFlow Does Differently": a node attends to
+// its ancestors, never to siblings or descendants). Bit k of the result is
+// set iff tree key k0 + k (k < 128) is the node itself or one of its
+// ancestors. The walk follows parents from the node toward the root and
+// stops below k0; indices strictly decrease along it, so it ends after at
+// most kMaxNodes steps even on a malformed tree (whose output the combine
+// kernel then replaces with NaN).
+__device__ __forceinline__ uint4 ancestor_bits(const int32_t *parents, int node, int k0) {
+    uint32_t w0 = 0u, w1 = 0u, w2 = 0u, w3 = 0u;
+    int j = node;
+    for (int hop = 0; hop < kMaxNodes && j >= k0; ++hop) {
+        const int k = j - k0;
+        if (k < kBN) {
+            const uint32_t bit = 1u << (k & 31);
+            w0 |= (k >> 5) == 0 ? bit : 0u;
+            w1 |= (k >> 5) == 1 ? bit : 0u;
+            w2 |= (k >> 5) == 2 ? bit : 0u;
+            w3 |= (k >> 5) == 3 ? bit : 0u;
+        }
+        const int p = __ldg(parents + j);
+        j = p < j ? p : -1;
+    }
+    return make_uint4(w0, w1, w2, w3);
+}
+
 // Softmax and epilogue. The two warps of a row quadrant (q and q + 4, both
 // on TMEM lanes 32q..32q+31) take alternate key tiles: warp q + 4p owns the
 // tiles of global index g with g % 2 == p and does the whole 128-column row
@@ -393,9 +441,9 @@ __device__ __forceinline__ void pv_loop(const AttnArgs &a, uint8_t *smem, uint32
 // the producer and issuer warpgroup 56. P (bf16 pairs) goes back over the S
 // columns 0-63 of its buffer.
 template <int D>
-__device__ __forceinline__ void softmax_loop(const Layout &L, const AttnArgs &a, uint32_t bars,
-                                             const ItemInfo *items_s, float *hand, float *xchg, uint32_t tmem,
-                                             volatile int *abort) {
+__device__ __forceinline__ void softmax_loop(const AttnMaps &maps, const Layout &L, const AttnArgs &a,
+                                             uint8_t *smem, uint32_t bars, const ItemInfo *items_s, float *hand,
+                                             float *xchg, uint32_t tmem, volatile int *abort) {
     using C = AttnCfg<D>;
     constexpr int kHalf = kBN / 2;                  // keys per TMEM load
     constexpr int kOHalf = D / 2;                   // O columns per warp in the epilogue
@@ -405,13 +453,22 @@ __device__ __forceinline__ void softmax_loop(const Layout &L, const AttnArgs &a,
     auto bar = [&](int i) { return bars + 8u * i; };
     const uint32_t t_row = tmem + ((uint32_t)(q * 32) << 16);
     const uint32_t t_o = t_row + C::kColO;
-    const uint32_t *masks = reinterpret_cast<const uint32_t *>(a.ws + L.mask_off);
-    float *opart = reinterpret_cast<float *>(a.ws + L.opart_off);
+    __half *opart = reinterpret_cast<__half *>(a.ws + L.opart_off);
     float2 *mlpart = reinterpret_cast<float2 *>(a.ws + L.ml_off);
     float *hand_q = hand + q * 64;
     const float sl2 = a.scale_log2;
-    int ic = 0, g = 0, xc = 0;
+    int ic = 0, g = 0, xc = 0, items = 0;
+    int pending_q = -1;         // thread 0: Q buffer whose TMA store has not yet read it back
 
+    // Thread 0 hands a staging buffer back to the producer once the bulk
+    // store that reads it has done so.
+    auto release_q = [&]() {
+        if (threadIdx.x == 0 && pending_q >= 0) {
+            bulk_wait_read();
+            mbar_arrive(bar(C::B_Q_EMPTY + pending_q));
+            pending_q = -1;
+        }
+    };
     auto publish = [&](int gg, float m) {
         hand_q[(gg & 1) * 32 + lane] = m;
         __syncwarp();
@@ -473,25 +530,21 @@ __device__ __forceinline__ void softmax_loop(const Layout &L, const AttnArgs &a,
         const ItemInfo info = items_s[slot];
         ++ic;
         if (!info.valid) break;
-        if (info.skip) {
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(C::B_ITEM_EMPTY + slot));
-            continue;
-        }
         const int node = info.qt * L.NB + r / L.G;
         const int head = info.kh * L.G + r % L.G;
         const bool row_valid = node < info.n;
-        const uint32_t *mrow = masks + ((size_t)info.b * L.Nmax + (row_valid ? node : 0)) * L.W4;
+        const int32_t *par_b = a.parents + (size_t)info.b * L.Nmax;
         float m_run = kNegInf;                      // reference of O after this warp's last tile
         float m_own = kNegInf, l_own = 0.f;         // this warp's part of the row sum, and its reference
         const int nt = info.te - info.tb;
         bool fail = false;
         for (int j = 0; j < nt; ++j, ++g) {
             if ((g & 1) != par) continue;                  // the partner's tile
+            release_q();
             const int t = info.tb + j;
             const bool tree = t >= info.t_pre;
             uint4 mw = make_uint4(0u, 0u, 0u, 0u);         // ancestor bits of the tile's 128 keys
-            if (tree && row_valid) mw = *reinterpret_cast<const uint4 *>(mrow + 4 * (t - info.t_pre));
+            if (tree && row_valid) mw = ancestor_bits(par_b, node, (t - info.t_pre) * kBN);
             const int lim = (!tree && t == info.t_pre - 1) ? info.P - t * kBN : kBN;
             const int sb = g % C::NS;
             const uint32_t t_s = t_row + sb * 128;
@@ -547,6 +600,7 @@ __device__ __forceinline__ void softmax_loop(const Layout &L, const AttnArgs &a,
         if (fail) break;
         // Epilogue. The final max is m(g_last), published by the last tile's
         // owner; the partner is the reader its hand-off slot expects.
+        release_q();
         const int g_last = g - 1;
         float m_fin = m_run;
         if ((g_last & 1) != par && !receive(g_last, m_fin)) break;
@@ -562,43 +616,88 @@ __device__ __forceinline__ void softmax_loop(const Layout &L, const AttnArgs &a,
         if (!mbar_wait(bar(C::B_PAIR + q), xc & 1, abort, a.status)) break;
         ++xc;
         const float l_run = l_mine + xchg[(par ^ 1) * kRows + r];
-        const uint32_t t_oh = t_o + par * kOHalf;
-        if (info.ns <= 1) {
-            __nv_bfloat16 *dst = a.out + (((size_t)info.b * L.Nmax + node) * L.Hq + head) * D + par * kOHalf;
-            const float inv_l = 1.0f / l_run;
-#pragma unroll 1
-            for (int c = 0; c < kOHalf / 32; ++c) {
-                uint32_t v[32];
-                tmem_ld32(t_oh + c * 32, v);
-                if (row_valid) {
-                    uint4 *d4 = reinterpret_cast<uint4 *>(dst + c * 32);
-                    auto f = [&](int e) { return __uint_as_float(v[e]) * inv_l; };
-#pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        d4[k] = make_uint4(pack_bf16x2(f(8 * k), f(8 * k + 1)), pack_bf16x2(f(8 * k + 2), f(8 * k + 3)),
-                                           pack_bf16x2(f(8 * k + 4), f(8 * k + 5)),
-                                           pack_bf16x2(f(8 * k + 6), f(8 * k + 7)));
-                }
-            }
-        } else {
-            float4 *d4 = reinterpret_cast<float4 *>(opart + ((size_t)info.slot * kRows + r) * D + par * kOHalf);
-#pragma unroll 1
-            for (int c = 0; c < kOHalf / 32; ++c) {
-                uint32_t v[32];
-                tmem_ld32(t_oh + c * 32, v);
-#pragma unroll
-                for (int k = 0; k < 8; ++k)
-                    d4[8 * c + k] = make_float4(__uint_as_float(v[4 * k]), __uint_as_float(v[4 * k + 1]),
-                                                __uint_as_float(v[4 * k + 2]), __uint_as_float(v[4 * k + 3]));
-            }
-            if (par == 0) mlpart[(size_t)info.slot * kRows + r] = make_float2(m_fin, l_run);
-        }
+        // This warp's half of the row; then O's TMEM belongs to the next item.
+        uint32_t ov[kOHalf];
+        if constexpr (kOHalf == 64)
+            tmem_ld64(t_o + par * kOHalf, ov);
+        else
+            tmem_ld32(t_o + par * kOHalf, ov);
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) {
-            mbar_arrive(bar(C::B_O_FREE));
-            mbar_arrive(bar(C::B_ITEM_EMPTY + slot));
+        if (lane == 0) mbar_arrive(bar(C::B_O_FREE));
+        // Final rows are bf16; the pieces of a split unit are fp16 rows already
+        // divided by their own l, with (m, l) beside them for the merge.
+        const bool split = info.ns > 1;
+        const float inv_l = 1.0f / l_run;
+        auto pack8 = [&](int k) {
+            auto f = [&](int e) { return __uint_as_float(ov[8 * k + e]) * inv_l; };
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                if (split) {
+                    const __half2 h = __floats2half2_rn(f(2 * e), f(2 * e + 1));
+                    w[e] = *reinterpret_cast<const uint32_t *>(&h);
+                } else {
+                    w[e] = pack_bf16x2(f(2 * e), f(2 * e + 1));
+                }
+            }
+            return make_uint4(w[0], w[1], w[2], w[3]);
+        };
+        // A unit whose rows are all real nodes is staged in its own Q buffer
+        // (free since its last QK^T) in the 128-byte-swizzled box layout and
+        // written by TMA bulk stores: one wide store instead of 32 scattered
+        // rows per warp instruction. Other units write their valid rows
+        // directly.
+        const bool whole = (info.qt + 1) * L.NB <= info.n;
+        const int qb = items % C::NQ;
+        if (whole) {
+            uint8_t *row = smem + C::q_off + qb * C::kQBytes + ((par * kOHalf) / 64) * C::kQBoxBytes + r * 128;
+            const int c0 = ((par * kOHalf) % 64) / 8;      // first 16-byte chunk of this warp's columns
+#pragma unroll
+            for (int k = 0; k < kOHalf / 8; ++k)
+                *reinterpret_cast<uint4 *>(row + (((c0 + k) ^ (r & 7)) << 4)) = pack8(k);
+            fence_proxy_async_smem();
+        } else if (row_valid) {
+            uint4 *dst = split ? reinterpret_cast<uint4 *>(opart + ((size_t)info.slot * kRows + r) * D + par * kOHalf)
+                               : reinterpret_cast<uint4 *>(a.out + (((size_t)info.b * L.Nmax + node) * L.Hq + head) * D +
+                                                           par * kOHalf);
+#pragma unroll
+            for (int k = 0; k < kOHalf / 8; ++k) dst[k] = pack8(k);
         }
+        if (split && par == 0) mlpart[(size_t)info.slot * kRows + r] = make_float2(m_fin, l_run);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(C::B_EPI));
+        bool ok_epi = true;
+        if (threadIdx.x == 0) {
+            ok_epi = mbar_wait(bar(C::B_EPI), items & 1, abort, a.status);
+            if (ok_epi && whole) {
+                const uint32_t src = smem_u32(smem + C::q_off + qb * C::kQBytes);
+                for (int dc = 0; dc < C::kBoxes; ++dc) {
+                    if (split)
+                        tma_store_3d(&maps.part, src + dc * C::kQBoxBytes, dc * 64, 0, info.slot);
+                    else
+                        tma_store_3d(&maps.out, src + dc * C::kQBoxBytes, dc * 64, info.kh * L.G,
+                                     info.b * L.Nmax + info.qt * L.NB);
+                }
+                bulk_commit();
+                pending_q = qb;
+            } else if (ok_epi) {
+                mbar_arrive(bar(C::B_Q_EMPTY + qb));
+            }
+        }
+        if (warp == 0) ok_epi = __shfl_sync(0xffffffffu, ok_epi ? 1 : 0, 0) != 0;
+        if (!ok_epi) break;
+        ++items;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(C::B_ITEM_EMPTY + slot));
+    }
+    // Every bulk store of this CTA has landed before it can exit.
+    if (threadIdx.x == 0) {
+        if (pending_q >= 0) {
+            bulk_wait_read();
+            mbar_arrive(bar(C::B_Q_EMPTY + pending_q));
+        }
+        bulk_wait_all();
     }
 }
 
@@ -636,6 +735,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int q = 0; q < 4; ++q) init(C::B_PAIR + q, 2); // the two warps that share a row quadrant
         for (int h = 0; h < 8; ++h) init(C::B_HAND + h, 1); // row-max hand-off, [quadrant][tile parity]
+        init(C::B_EPI, kSoftmaxWarps);                     // an item's output is staged
         *abort = 0;
         fence_mbar_init();
     }
@@ -651,10 +751,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
-    // Everything above overlapped the prep kernel; the plan and the masks it
-    // writes are read only after this point. The combine kernel may launch
-    // now: it waits for this grid before it reads any partial.
-    pdl_wait_prior_grid();
+    // The combine kernel may launch now: it waits for this grid before it
+    // reads any partial or writes any output.
     pdl_launch_dependents();
     // 256 x 224 + 128 x 56 = 384 x 168, the registers the block launched with
     // (the host refuses to launch a build that uses any other count).
@@ -670,7 +768,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             v_producer_loop<D>(maps, L, a, sbase, bars, items_s, abort);
     } else {
         setmaxnreg_inc<kSoftmaxRegs>();
-        softmax_loop<D>(L, a, bars, items_s, reinterpret_cast<float *>(smem + C::hand_off),
+        softmax_loop<D>(maps, L, a, smem, bars, items_s, reinterpret_cast<float *>(smem + C::hand_off),
                         reinterpret_cast<float *>(smem + C::xchg_off), tmem, abort);
     }
 
@@ -705,11 +803,6 @@ cudaError_t launch_d(const Layout &L, const AttnMaps &m, const AttnArgs &a, cuda
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = C::smem_request;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
     trace_begin("tree_attention", s);
     e = cudaLaunchKernelEx(&cfg, tree_attention_kernel<D>, m, L, a);
     if (e == cudaSuccess) e = cudaGetLastError();

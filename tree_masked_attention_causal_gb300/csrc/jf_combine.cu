@@ -1,17 +1,24 @@
-// jf_combine.cu - merge of the split-KV partials of tree attention.
+// jf_combine.cu - the kernel that follows tree attention: tree validation,
+// the NaN rows of malformed sequences, and the merge of split-KV partials.
 //
-// A work unit whose keys were split over several CTAs has, per split s, an
-// unnormalised fp32 row O_s plus (m_s, l_s), with m in the exp2 domain. The
-// merged row is the log-sum-exp rescale:
-//   O = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s,   M = max_s m_s.
+// Validation follows the tree's definition (node 0 is the root, parent[0] =
+// -1, every other node's parent comes earlier, 0 <= parent[i] < i), plus the
+// ranges of n_nodes and prefix_lens. Every output row of a sequence that
+// fails it becomes NaN and JF_STATUS_BAD_TREE is raised; the attention kernel
+// has computed those rows without checking, and they are overwritten here.
+//
+// A work unit whose keys were split over several CTAs has, per split s, a
+// row o_s = O_s / l_s in fp16 plus (m_s, l_s) in fp32, with m in the exp2
+// domain. The merged row is the log-sum-exp rescale:
+//   O = sum_s w_s o_s / sum_s w_s,   w_s = 2^(m_s - M) l_s,   M = max_s m_s.
 // The sums run in split order, so the result is deterministic.
 //
-// The merge is spread over the whole GPU: grid (units, 256 / 8 rows), one
-// warp per row, lane k holding d/32 consecutive columns. The (m, l) of all
-// splits and the O rows of up to 8 splits are loaded in one round trip.
-// The kernel is a programmatic dependent of the attention kernel: it
-// launches while that kernel runs and waits for it before reading any
-// partial.
+// Grid (units, 128 / 8 rows), one warp per row, lane k holding d/32
+// consecutive columns. The (m, l) of all splits and the O rows of up to 8
+// splits are loaded in one round trip. The kernel is a programmatic
+// dependent of the attention kernel: it validates the tree (inputs only)
+// while that kernel runs, then waits for it before reading any partial or
+// writing any output.
 #include "jf_common.cuh"
 
 namespace jf {
@@ -23,30 +30,51 @@ constexpr int kCombineBatch = 8;             // splits whose loads are issued to
 
 template <int D>
 __global__ void __launch_bounds__(kCombineThreads) split_combine_kernel(const Layout L, const AttnArgs a) {
-    pdl_wait_prior_grid();
     const int q = blockIdx.x;
-    const QTile qi = reinterpret_cast<const QTile *>(a.ws + L.qtab_off)[q];
-    const int ns = qi.n_splits, base = qi.slot_base;
-    if (ns <= 1) return;
     const int b = q / (L.Hkv * L.QT);
     const int rem = q - b * (L.Hkv * L.QT);
     const int kh = rem / L.QT, qt = rem - kh * L.QT;
-    const SeqInfo si = reinterpret_cast<const SeqInfo *>(a.ws + L.seq_off)[b];
-    if (si.bad) return;
+    // Validate sequence b: one node per thread (Nmax <= blockDim).
+    const int P = a.prefix_lens[b], n = a.n_nodes[b];
+    const int i = threadIdx.x;
+    bool bad = !seq_valid(P, n, L);
+    if (!bad && i < n) {
+        const int p = a.parents[(size_t)b * L.Nmax + i];
+        bad = (i == 0) ? (p != -1) : (p < 0 || p >= i);
+    }
+    bad = __syncthreads_or(bad);
+    pdl_wait_prior_grid();          // the attention grid is complete from here on
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int r = blockIdx.y * kCombineRowsPerBlock + warp;
     const int node = qt * L.NB + r / L.G;
-    if (node >= si.n_nodes) return;
+    if (node >= L.Nmax) return;
     const int head = kh * L.G + r % L.G;
-    const float2 *ml = reinterpret_cast<const float2 *>(a.ws + L.ml_off);
-    const float *op = reinterpret_cast<const float *>(a.ws + L.opart_off);
     constexpr int E = D / 32;   // columns per lane
+    __nv_bfloat16 *dst = a.out + (((size_t)b * L.Nmax + node) * L.Hq + head) * D + lane * E;
+    if (bad) {
+        if (kh == 0 && qt == 0 && blockIdx.y == 0 && threadIdx.x == 0) set_status(a.status, JF_STATUS_BAD_TREE);
+        const uint32_t nan2 = 0x7FC07FC0u;
+        if constexpr (E == 4)
+            *reinterpret_cast<uint2 *>(dst) = make_uint2(nan2, nan2);
+        else
+            *reinterpret_cast<uint32_t *>(dst) = nan2;
+        return;
+    }
+    if (node >= n || unit_tiles(P, n, qt, L) == 0) return;
+    const QTile qi = reinterpret_cast<const QTile *>(a.ws + L.qtab_off)[q];
+    const int ns = qi.n_splits;
+    if (ns <= 1) return;
+    // split s sits in slot 2c + 1 at c = c_first when the unit is not that
+    // CTA's first item, else in slot 2c, c = c_first + s
+    auto slot_of = [&](int sidx) { return 2 * (qi.c_first + sidx) + ((sidx == 0 && !qi.first_item) ? 1 : 0); };
+    const float2 *ml = reinterpret_cast<const float2 *>(a.ws + L.ml_off);
+    const __half *op = reinterpret_cast<const __half *>(a.ws + L.opart_off);
     constexpr float kNegInf = -__builtin_huge_valf();
     // (m_s, l_s): lane s holds split s (splits past 32 are folded in below)
     float2 mine = make_float2(kNegInf, 0.f);
-    if (lane < ns) mine = __ldcg(&ml[(size_t)(base + lane) * kRows + r]);
+    if (lane < ns) mine = __ldcg(&ml[(size_t)slot_of(lane) * kRows + r]);
     float M = mine.x;
-    for (int s = 32 + lane; s < ns; s += 32) M = fmaxf(M, __ldcg(&ml[(size_t)(base + s) * kRows + r]).x);
+    for (int s = 32 + lane; s < ns; s += 32) M = fmaxf(M, __ldcg(&ml[(size_t)slot_of(s) * kRows + r]).x);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     if (M == kNegInf) M = 0.f;
@@ -55,18 +83,18 @@ __global__ void __launch_bounds__(kCombineThreads) split_combine_kernel(const La
     for (int e = 0; e < E; ++e) acc[e] = 0.f;
     float Lsum = 0.f;
     for (int s0 = 0; s0 < ns; s0 += kCombineBatch) {
-        float v[kCombineBatch][E];
+        uint32_t v[kCombineBatch][E / 2];           // fp16 pairs
 #pragma unroll
         for (int k = 0; k < kCombineBatch; ++k) {    // all loads of the batch first
             const int s = s0 + k;
             if (s < ns) {
-                const float *src = op + ((size_t)(base + s) * kRows + r) * D + lane * E;
+                const __half *src = op + ((size_t)slot_of(s) * kRows + r) * D + lane * E;
                 if constexpr (E == 4) {
-                    const float4 x = __ldcg(reinterpret_cast<const float4 *>(src));
-                    v[k][0] = x.x; v[k][1] = x.y; v[k][2] = x.z; v[k][3] = x.w;
+                    const uint2 x = __ldcg(reinterpret_cast<const uint2 *>(src));
+                    v[k][0] = x.x;
+                    v[k][1] = x.y;
                 } else {
-                    const float2 x = __ldcg(reinterpret_cast<const float2 *>(src));
-                    v[k][0] = x.x; v[k][1] = x.y;
+                    v[k][0] = __ldcg(reinterpret_cast<const unsigned int *>(src));
                 }
             }
         }
@@ -76,16 +104,20 @@ __global__ void __launch_bounds__(kCombineThreads) split_combine_kernel(const La
             if (s < ns) {
                 const float2 mls = s < 32 ? make_float2(__shfl_sync(0xffffffffu, mine.x, s),
                                                         __shfl_sync(0xffffffffu, mine.y, s))
-                                          : __ldcg(&ml[(size_t)(base + s) * kRows + r]);
-                const float w = ex2_approx(mls.x - M);
-                Lsum += w * mls.y;
+                                          : __ldcg(&ml[(size_t)slot_of(s) * kRows + r]);
+                // the piece is O_s / l_s: its weight in the sum is 2^(m_s - M) l_s
+                const float w = ex2_approx(mls.x - M) * mls.y;
+                Lsum += w;
 #pragma unroll
-                for (int e = 0; e < E; ++e) acc[e] += w * v[k][e];
+                for (int e = 0; e < E / 2; ++e) {
+                    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&v[k][e]));
+                    acc[2 * e] += w * f.x;
+                    acc[2 * e + 1] += w * f.y;
+                }
             }
         }
     }
     const float inv = 1.0f / Lsum;
-    __nv_bfloat16 *dst = a.out + (((size_t)b * L.Nmax + node) * L.Hq + head) * D + lane * E;
     if constexpr (E == 4) {
         *reinterpret_cast<uint2 *>(dst) = make_uint2(pack_bf16x2(acc[0] * inv, acc[1] * inv),
                                                      pack_bf16x2(acc[2] * inv, acc[3] * inv));

@@ -10,6 +10,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -24,7 +25,7 @@ constexpr int kBN = 128;          // keys per KV tile
 constexpr int kMaxNodes = 256;    // tree slots per sequence
 constexpr int kMaxCtas = 256;     // cap on the persistent attention grid
 constexpr int kMinTilesPerCta = 2;   // smallest key range a CTA is given
-constexpr int kMaxBatch = 1024;   // sequences per jf_tree_attention call (plan staging)
+constexpr int kMaxBatch = 1024;   // sequences per jf_tree_attention call
 constexpr int kArgmaxThreads = 256;
 constexpr int kArgmaxVecs = 4;    // 16-byte loads in flight per thread
 constexpr int kArgmaxChunk = 51200;  // bf16 elements of one logits row per CTA (100 KB)
@@ -32,30 +33,15 @@ constexpr unsigned long long kTimeoutNs = 2000000000ull;        // 2 s per wait
 
 __host__ __device__ constexpr int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
-struct SeqInfo {         // per sequence, written by the prep kernel
-    int32_t prefix_len;
-    int32_t n_nodes;
-    int32_t bad;
-    int32_t pad;
-};
-
-// Per work unit (kRows stacked query rows of one sequence and KV head): its
-// key tiles (prefix tiles first, then tree tiles), where they start in the
-// concatenation of all units' tiles, and how many CTA ranges cover it.
+// Per work unit (kRows stacked query rows of one sequence and KV head),
+// written by the attention CTA whose key range holds the unit's first tile
+// and read by the combine kernel: how many CTA ranges split the unit, the
+// first of them, and whether the unit is that CTA's first item.
 struct QTile {
-    int32_t n_splits;    // CTA ranges covering the unit (0 = no work)
-    int32_t slot_base;   // first partial slot when n_splits > 1
-    int32_t tile_start;  // prefix sum of `tiles` over earlier units
-    int32_t tiles;
-};
-
-// Stream-K plan: CTA c owns tiles [c * total / n_ctas, (c + 1) * total / n_ctas)
-// of the concatenated unit tiles; `cta_first[c]` is the unit holding the first.
-struct PlanHeader {
-    int32_t total_tiles;
-    int32_t n_ctas;
-    int32_t pad0;
-    int32_t pad1;
+    int32_t n_splits;    // CTA ranges covering the unit (1 = not split)
+    int32_t c_first;     // CTA whose range holds the unit's first tile
+    int32_t first_item;  // 1 if the unit starts that CTA's range
+    int32_t tile_start;  // the unit's first tile in the concatenation of all units' tiles
 };
 
 // Byte offsets of the workspace regions. Attention regions come first, then
@@ -64,11 +50,10 @@ struct Layout {
     int32_t B, Nmax, Hq, Hkv, G, D, Pcap, V;
     int32_t QT;          // work units per (sequence, kv head)
     int32_t NB;          // nodes per work unit = kRows / G
-    int32_t W4;          // mask words per node (multiple of 4)
     int32_t n_qtiles;    // work units: B * Hkv * QT
-    int32_t max_items;   // bound on split pieces: n_qtiles + kMaxCtas
+    int32_t max_pieces;  // partial slots: two per CTA (its first and its last item)
     int32_t chunks;      // argmax chunks per logits row
-    size_t mask_off, seq_off, plan_off, qtab_off, first_off, ml_off, opart_off;
+    size_t qtab_off, ml_off, opart_off;
     size_t amp_off;
     size_t total;
 };
@@ -81,22 +66,128 @@ inline Layout make_layout(int B, int Nmax, int Hq, int Hkv, int D, int Pcap, int
     L.B = B; L.Nmax = Nmax; L.Hq = Hq; L.Hkv = Hkv; L.G = Hq / Hkv; L.D = D; L.Pcap = Pcap; L.V = V;
     L.NB = kRows / L.G;
     L.QT = ceil_div(Nmax, L.NB);
-    L.W4 = 4 * ceil_div(Nmax, kBN);
     L.n_qtiles = B * Hkv * L.QT;
-    L.max_items = L.n_qtiles + kMaxCtas;
+    L.max_pieces = 2 * kMaxCtas;
     L.chunks = V > 0 ? ceil_div(V, kArgmaxChunk) : 1;
     size_t off = 0;
     auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 256); return o; };
-    L.mask_off = take(sizeof(uint32_t) * (size_t)B * Nmax * L.W4);
-    L.seq_off = take(sizeof(SeqInfo) * (size_t)B);
-    L.plan_off = take(sizeof(PlanHeader));
     L.qtab_off = take(sizeof(QTile) * (size_t)L.n_qtiles);
-    L.first_off = take(sizeof(int32_t) * (size_t)kMaxCtas);
-    L.ml_off = take(sizeof(float2) * (size_t)L.max_items * kRows);
-    L.opart_off = take(sizeof(float) * (size_t)L.max_items * kRows * D);
+    L.ml_off = take(sizeof(float2) * (size_t)L.max_pieces * kRows);
+    L.opart_off = take(2 * (size_t)L.max_pieces * kRows * D);   // fp16 rows, already divided by their l
     L.amp_off = take(sizeof(int2) * (size_t)B * Nmax * L.chunks);
     L.total = off;
     return L;
+}
+
+// ------------------------------------------------------------- the plan
+// Work unit u = (b, kh, qt), u = (b * Hkv + kh) * QT + qt, holds kRows
+// stacked query rows: the G query heads of KV head kh for nodes
+// qt * NB .. qt * NB + NB - 1 of sequence b. Its keys are ceil(P / 128)
+// prefix tiles followed by the tree tiles up to its highest node (with
+// parents[i] < i no key above a node can be its ancestor). The units' tiles
+// are concatenated in u order and CTA c of C takes the equal range
+// [c * total / C, (c + 1) * total / C) (stream-K). Every kernel derives this
+// plan from prefix_lens and n_nodes alone, with the functions below.
+
+// A sequence with an out-of-range length or prefix gets no work.
+__host__ __device__ inline bool seq_valid(int P, int n, const Layout &L) {
+    return n >= 1 && n <= L.Nmax && P >= 0 && P <= L.Pcap;
+}
+
+__device__ __forceinline__ int unit_tiles(int P, int n, int qt, const Layout &L) {
+    const int node0 = qt * L.NB;
+    if (node0 >= n) return 0;
+    return ceil_div(P, kBN) + ceil_div(min(node0 + L.NB, n), kBN);
+}
+
+// Tiles of all units of one KV head of a valid sequence, in closed form:
+// unit qt < nq - 1 reaches node (qt + 1) * NB, i.e. ceil((qt + 1) / G) tree
+// tiles since NB * G = 128, and the last unit reaches node n.
+__device__ __forceinline__ int head_tiles(int P, int n, const Layout &L) {
+    const int nq = ceil_div(n, L.NB);
+    const int m = nq - 1, q = m / L.G, r = m - q * L.G;
+    return nq * ceil_div(P, kBN) + L.G * q * (q + 1) / 2 + r * (q + 1) + ceil_div(n, kBN);
+}
+
+__device__ __forceinline__ int plan_ctas(int total, int num_ctas) {
+    return max(1, min(num_ctas, total / kMinTilesPerCta));
+}
+
+// The CTA whose range holds tile x.
+__device__ __forceinline__ int cta_of_tile(long long x, int total, int C) {
+    return (int)(((x + 1) * C - 1) / total);
+}
+
+// Warp-collective: the plan as seen from CTA c. Returns total tiles and C,
+// and, if the CTA's range [lo, hi) is not empty, the sequence b holding
+// tile lo with its first tile, prefix length and node count (every lane gets
+// the same). One pass over the sequences; a batch of up to 32 sequences is
+// read from memory once.
+struct PlanSeq {
+    int total, n_ctas;
+    long long lo, hi;
+    int b, P, n;
+    long long seq_start;
+};
+
+__device__ inline PlanSeq plan_locate(const Layout &L, const int32_t *prefix_lens, const int32_t *n_nodes, int c,
+                                      int num_ctas) {
+    const int lane = threadIdx.x & 31;
+    PlanSeq r{};
+    r.b = -1;
+    auto seq_tiles = [&](int P, int n) { return seq_valid(P, n, L) ? L.Hkv * head_tiles(P, n, L) : 0; };
+    int P0 = 0, n0 = 0, t0 = 0;                      // this lane's sequence of the first 32
+    int sum = 0;
+    for (int b0 = 0; b0 < L.B; b0 += 32) {
+        const int b = b0 + lane;
+        int P = 0, n = 0;
+        if (b < L.B) {
+            P = prefix_lens[b];
+            n = n_nodes[b];
+        }
+        const int t = b < L.B ? seq_tiles(P, n) : 0;
+        if (b0 == 0) {
+            P0 = P;
+            n0 = n;
+            t0 = t;
+        }
+        sum += t;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    r.total = sum;
+    r.n_ctas = sum > 0 ? plan_ctas(sum, num_ctas) : 0;
+    if (c >= r.n_ctas) return r;
+    r.lo = (long long)c * sum / r.n_ctas;
+    r.hi = (long long)(c + 1) * sum / r.n_ctas;
+    long long carry = 0;
+    for (int b0 = 0; b0 < L.B; b0 += 32) {
+        const int b = b0 + lane;
+        int P = P0, n = n0, t = t0;
+        if (b0 > 0) {
+            P = b < L.B ? prefix_lens[b] : 0;
+            n = b < L.B ? n_nodes[b] : 0;
+            t = b < L.B ? seq_tiles(P, n) : 0;
+        }
+        int incl = t;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        const long long start = carry + incl - t;
+        const unsigned hit = __ballot_sync(0xffffffffu, t > 0 && r.lo >= start && r.lo < start + t);
+        if (hit) {
+            const int src = __ffs(hit) - 1;
+            r.b = b0 + src;
+            r.seq_start = __shfl_sync(0xffffffffu, start, src);
+            r.P = __shfl_sync(0xffffffffu, P, src);
+            r.n = __shfl_sync(0xffffffffu, n, src);
+            return r;
+        }
+        carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    return r;
 }
 
 // ------------------------------------------------------------- PTX: misc
@@ -176,6 +267,19 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *map, int c
         "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
         : "memory");
 }
+
+// 3-D tiled bulk tensor store shared -> global (bulk async-group completion).
+// Coordinates are element indices, innermost first; none may be negative.
+__device__ __forceinline__ void tma_store_3d(const void *map, uint32_t src, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(map),
+                 "r"(c0), "r"(c1), "r"(c2), "r"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until every committed bulk store of this thread has read its shared memory.
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Wait until every committed bulk store of this thread has completed.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // Generic-proxy shared-memory writes -> visible to the async proxy (TMA/MMA).
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -374,6 +478,8 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // (defined in the .cu files, called by the C ABI in jf_api.cu)
 struct AttnMaps {
     CUtensorMap q, k_cache, v_cache, tree_k, tree_v;
+    CUtensorMap out;    // bf16 [B * Nmax, Hq, d], box {64, G, NB}: one work unit, like q
+    CUtensorMap part;   // fp16 [pieces, 128 rows, d], box {64, 128, 1}: split partials
 };
 
 struct AttnArgs {
@@ -387,7 +493,6 @@ struct AttnArgs {
     int32_t num_ctas;    // persistent grid size of the attention kernel
 };
 
-cudaError_t launch_tree_prep(const Layout &L, const AttnArgs &a, cudaStream_t s);
 cudaError_t launch_tree_attention(const Layout &L, const AttnMaps &m, const AttnArgs &a,
                                   cudaStream_t s);
 cudaError_t launch_split_combine(const Layout &L, const AttnArgs &a, cudaStream_t s);
