@@ -105,8 +105,8 @@ constexpr int kQkWarp = 9;
 constexpr int kPvWarp = 10;
 constexpr int kVProducerWarp = 11;
 constexpr int kLaunchRegs = 168;            // per thread at launch: 384 x 168 = 64512
-constexpr uint32_t kSoftmaxRegs = 224;      // warpgroups 0-1 after setmaxnreg
-constexpr uint32_t kOtherRegs = 56;         // warpgroup 2 (producers, issuers)
+constexpr uint32_t kSoftmaxRegs = 216;      // warpgroups 0-1 after setmaxnreg
+constexpr uint32_t kOtherRegs = 72;         // warpgroup 2 (producers, issuers)
 static_assert(256 * kSoftmaxRegs + 128 * kOtherRegs <= kThreads * kLaunchRegs, "register split");
 constexpr float kNegInf = -__builtin_huge_valf();
 
@@ -130,19 +130,18 @@ __device__ __forceinline__ void producer_loop(const AttnMaps &maps, const Layout
     // from prefix_lens and n_nodes (no earlier kernel needed).
     const int c = blockIdx.x;
     const PlanSeq ps = plan_locate(L, a.prefix_lens, a.n_nodes, c, a.num_ctas);
-    const int total = ps.total, n_ctas = ps.n_ctas;
-    const long long lo0 = ps.lo, hi = ps.hi;
-    long long lo = lo0;
+    const int lo0 = ps.lo, hi = ps.hi;
+    int lo = lo0;
     // The unit (b, kh, qt) holding tile lo, and its first tile S.
     int b = ps.b, kh = 0, qt = 0, P = ps.P, n = ps.n;
-    long long S = 0;
+    int S = 0;
     if (lo < hi) {
         if (b < 0) {
             lo = hi;                        // unreachable for a consistent plan
         } else {
             const int th = head_tiles(P, n, L);
-            kh = (int)((lo - ps.seq_start) / th);
-            S = ps.seq_start + (long long)kh * th;
+            kh = (lo - ps.seq_start) / th;
+            S = ps.seq_start + kh * th;
             for (int ut = unit_tiles(P, n, 0, L); S + ut <= lo && qt + 1 < L.QT; ut = unit_tiles(P, n, qt, L)) {
                 S += ut;
                 ++qt;
@@ -151,10 +150,31 @@ __device__ __forceinline__ void producer_loop(const AttnMaps &maps, const Layout
     }
     int ic = 0, qc = 0, kc = 0;
     bool ok = true;
+    // K tile t of the current item into the next ring stage.
+    auto issue_k = [&](const ItemInfo &info, int t) -> bool {
+        const bool tree = t >= info.t_pre;
+        const int ks = kc % C::NK;
+        if (!mbar_wait(bar(C::B_K_EMPTY + ks), ((kc / C::NK) & 1) ^ 1, abort, a.status)) return false;
+        if (lane == 0) {
+            mbar_arrive_expect_tx(bar(C::B_K_FULL + ks), C::kTileBytes);
+            for (int dc = 0; dc < C::kBoxes; ++dc) {
+                const uint32_t dst = sbase + C::k_off + ks * C::kTileBytes + dc * (kBN * 128);
+                if (tree)
+                    tma_load_3d(dst, &maps.tree_k, dc * 64, info.kh, info.b * L.Nmax + (t - info.t_pre) * kBN,
+                                bar(C::B_K_FULL + ks));
+                else
+                    tma_load_3d(dst, &maps.k_cache, dc * 64, t * kBN, info.b * L.Hkv + info.kh, bar(C::B_K_FULL + ks));
+            }
+        }
+        __syncwarp();
+        ++kc;
+        return true;
+    };
     while (ok) {
         const int slot = ic & 1;
         if (!mbar_wait(bar(C::B_ITEM_EMPTY + slot), ((ic >> 1) & 1) ^ 1, abort, a.status)) break;
         ItemInfo info{};
+        int t_next = 0;
         if (lo < hi) {
             const int T = unit_tiles(P, n, qt, L);
             const int u = (b * L.Hkv + kh) * L.QT + qt;
@@ -163,18 +183,32 @@ __device__ __forceinline__ void producer_loop(const AttnMaps &maps, const Layout
             info.b = b;
             info.kh = kh;
             info.qt = qt;
-            info.tb = (int)(lo - S);
-            info.te = (int)(min(hi, S + T) - S);
+            info.tb = lo - S;
+            info.te = min(hi, S + T) - S;
             info.P = P;
             info.n = n;
             info.t_pre = ceil_div(P, kBN);
-            const int c_first = cta_of_tile(S, total, n_ctas);
-            info.ns = cta_of_tile(S + T - 1, total, n_ctas) - c_first + 1;
+            // Q and the first K tiles go out before the rest of the item's
+            // bookkeeping, so that their latency overlaps it.
+            const int qb = qc % C::NQ;
+            if (!mbar_wait(bar(C::B_Q_EMPTY + qb), ((qc / C::NQ) & 1) ^ 1, abort, a.status)) break;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(bar(C::B_Q_FULL + qb), C::kQBytes);
+                for (int dc = 0; dc < C::kBoxes; ++dc)
+                    tma_load_3d(sbase + C::q_off + qb * C::kQBytes + dc * C::kQBoxBytes, &maps.q, dc * 64,
+                                info.kh * L.G, info.b * L.Nmax + info.qt * L.NB, bar(C::B_Q_FULL + qb));
+            }
+            ++qc;
+            t_next = info.tb;
+            for (; t_next < info.te && t_next < info.tb + C::NK && ok; ++t_next) ok = issue_k(info, t_next);
+            if (!ok) break;
+            const int c_first = cta_of_tile(S, ps.qt, ps.rt, ps.n_ctas);
+            info.ns = cta_of_tile(S + T - 1, ps.qt, ps.rt, ps.n_ctas) - c_first + 1;
             // A split unit is at most this CTA's first item (slot 2c) or its
             // last (slot 2c + 1): units in between lie wholly in the range.
             info.slot = info.ns > 1 ? 2 * c + (ic > 0 ? 1 : 0) : -1;
             if (S >= lo0 && lane == 0)      // the unit starts in this range: record its split plan
-                qtab[u] = QTile{info.ns, c, S == lo0 ? 1 : 0, (int)S};
+                qtab[u] = QTile{info.ns, c, S == lo0 ? 1 : 0, S};
             lo = S + info.te;
             S += T;
             if (lo < hi) {                  // the next unit with tiles
@@ -203,35 +237,8 @@ __device__ __forceinline__ void producer_loop(const AttnMaps &maps, const Layout
         __syncwarp();
         ++ic;
         if (!info.valid) break;
-        // Q: 128 stacked rows (G heads x 128/G nodes), one box per 64 d, into
-        // buffer qc % NQ so that it can land while the previous unit runs.
-        const int qb = qc % C::NQ;
-        if (!mbar_wait(bar(C::B_Q_EMPTY + qb), ((qc / C::NQ) & 1) ^ 1, abort, a.status)) break;
-        if (lane == 0) {
-            mbar_arrive_expect_tx(bar(C::B_Q_FULL + qb), C::kQBytes);
-            for (int dc = 0; dc < C::kBoxes; ++dc)
-                tma_load_3d(sbase + C::q_off + qb * C::kQBytes + dc * C::kQBoxBytes, &maps.q, dc * 64,
-                            info.kh * L.G, info.b * L.Nmax + info.qt * L.NB, bar(C::B_Q_FULL + qb));
-        }
-        ++qc;
-        for (int t = info.tb; t < info.te; ++t) {
-            const bool tree = t >= info.t_pre;
-            const int ks = kc % C::NK;
-            if (!mbar_wait(bar(C::B_K_EMPTY + ks), ((kc / C::NK) & 1) ^ 1, abort, a.status)) { ok = false; break; }
-            if (lane == 0) {
-                mbar_arrive_expect_tx(bar(C::B_K_FULL + ks), C::kTileBytes);
-                for (int dc = 0; dc < C::kBoxes; ++dc) {
-                    const uint32_t dst = sbase + C::k_off + ks * C::kTileBytes + dc * (kBN * 128);
-                    if (tree)
-                        tma_load_3d(dst, &maps.tree_k, dc * 64, info.kh, info.b * L.Nmax + (t - info.t_pre) * kBN,
-                                    bar(C::B_K_FULL + ks));
-                    else
-                        tma_load_3d(dst, &maps.k_cache, dc * 64, t * kBN, info.b * L.Hkv + info.kh,
-                                    bar(C::B_K_FULL + ks));
-                }
-            }
-            ++kc;
-        }
+        for (; t_next < info.te; ++t_next)
+            if (!issue_k(info, t_next)) { ok = false; break; }
     }
     if (*abort && lane == 0) {
         // Let every copy this warp started land before the CTA can exit.
@@ -437,8 +444,8 @@ __device__ __forceinline__ uint4 ancestor_bits(const int32_t *parents, int node,
 // the max, after the PV of the previous tile has completed.
 //
 // The warp holds the tile's whole 128-key row in registers (one TMEM load);
-// the softmax warpgroups get 224 registers per thread for it (setmaxnreg),
-// the producer and issuer warpgroup 56. P (bf16 pairs) goes back over the S
+// the softmax warpgroups get 216 registers per thread for it (setmaxnreg),
+// the producer and issuer warpgroup 72. P (bf16 pairs) goes back over the S
 // columns 0-63 of its buffer.
 template <int D>
 __device__ __forceinline__ void softmax_loop(const AttnMaps &maps, const Layout &L, const AttnArgs &a,
@@ -534,13 +541,15 @@ __device__ __forceinline__ void softmax_loop(const AttnMaps &maps, const Layout 
         const int head = info.kh * L.G + r % L.G;
         const bool row_valid = node < info.n;
         const int32_t *par_b = a.parents + (size_t)info.b * L.Nmax;
+        // The ancestor walks of the item's tree tiles read this sequence's
+        // parents (at most 1 KB): start pulling them into L1 now.
+        if (info.te > info.t_pre && lane < ceil_div(L.Nmax, 32)) prefetch_l1(par_b + 32 * lane);
         float m_run = kNegInf;                      // reference of O after this warp's last tile
         float m_own = kNegInf, l_own = 0.f;         // this warp's part of the row sum, and its reference
         const int nt = info.te - info.tb;
         bool fail = false;
         for (int j = 0; j < nt; ++j, ++g) {
             if ((g & 1) != par) continue;                  // the partner's tile
-            release_q();
             const int t = info.tb + j;
             const bool tree = t >= info.t_pre;
             uint4 mw = make_uint4(0u, 0u, 0u, 0u);         // ancestor bits of the tile's 128 keys
@@ -596,6 +605,7 @@ __device__ __forceinline__ void softmax_loop(const AttnMaps &maps, const Layout 
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(C::B_P_FULL + sb));
+            release_q();                                   // a staged output store has long read its buffer
         }
         if (fail) break;
         // Epilogue. The final max is m(g_last), published by the last tile's
@@ -754,7 +764,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // The combine kernel may launch now: it waits for this grid before it
     // reads any partial or writes any output.
     pdl_launch_dependents();
-    // 256 x 224 + 128 x 56 = 384 x 168, the registers the block launched with
+    // 256 x 216 + 128 x 72 = 384 x 168, the registers the block launched with
     // (the host refuses to launch a build that uses any other count).
     if (warp >= kSoftmaxWarps) {
         setmaxnreg_dec<kOtherRegs>();

@@ -64,6 +64,10 @@ __global__ void __launch_bounds__(kCombineThreads) split_combine_kernel(const La
     const QTile qi = reinterpret_cast<const QTile *>(a.ws + L.qtab_off)[q];
     const int ns = qi.n_splits;
     if (ns <= 1) return;
+    // The attention kernel records the plan of every unit with work; one that
+    // aborted (JF_STATUS_TIMEOUT) may not have: never follow slots outside
+    // the partial buffers.
+    if (qi.c_first < 0 || 2 * (qi.c_first + ns) > L.max_pieces) return;
     // split s sits in slot 2c + 1 at c = c_first when the unit is not that
     // CTA's first item, else in slot 2c, c = c_first + s
     auto slot_of = [&](int sidx) { return 2 * (qi.c_first + sidx) + ((sidx == 0 && !qi.first_item) ? 1 : 0); };

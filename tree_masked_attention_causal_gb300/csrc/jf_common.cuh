@@ -113,9 +113,20 @@ __device__ __forceinline__ int plan_ctas(int total, int num_ctas) {
     return max(1, min(num_ctas, total / kMinTilesPerCta));
 }
 
-// The CTA whose range holds tile x.
-__device__ __forceinline__ int cta_of_tile(long long x, int total, int C) {
-    return (int)(((x + 1) * C - 1) / total);
+// First tile of CTA c's range, floor(c * total / C), in 32-bit arithmetic:
+// with total = C * qt + rt, it is c * qt + floor(c * rt / C) (c, rt < 256).
+__device__ __forceinline__ int range_start(int c, int qt, int rt, int C) { return c * qt + (c * rt) / C; }
+
+// Warp-collective: the CTA whose range holds tile x, i.e. the number of
+// CTAs c >= 1 whose range starts at or before x.
+__device__ __forceinline__ int cta_of_tile(int x, int qt, int rt, int C) {
+    const int lane = threadIdx.x & 31;
+    int n = 0;
+    for (int c0 = 1; c0 < C; c0 += 32) {
+        const int c = c0 + lane;
+        n += __popc(__ballot_sync(0xffffffffu, c < C && range_start(c, qt, rt, C) <= x));
+    }
+    return n;
 }
 
 // Warp-collective: the plan as seen from CTA c. Returns total tiles and C,
@@ -125,9 +136,10 @@ __device__ __forceinline__ int cta_of_tile(long long x, int total, int C) {
 // read from memory once.
 struct PlanSeq {
     int total, n_ctas;
-    long long lo, hi;
+    int qt, rt;         // total = n_ctas * qt + rt
+    int lo, hi;
     int b, P, n;
-    long long seq_start;
+    int seq_start;
 };
 
 __device__ inline PlanSeq plan_locate(const Layout &L, const int32_t *prefix_lens, const int32_t *n_nodes, int c,
@@ -158,9 +170,11 @@ __device__ inline PlanSeq plan_locate(const Layout &L, const int32_t *prefix_len
     r.total = sum;
     r.n_ctas = sum > 0 ? plan_ctas(sum, num_ctas) : 0;
     if (c >= r.n_ctas) return r;
-    r.lo = (long long)c * sum / r.n_ctas;
-    r.hi = (long long)(c + 1) * sum / r.n_ctas;
-    long long carry = 0;
+    r.qt = sum / r.n_ctas;
+    r.rt = sum - r.qt * r.n_ctas;
+    r.lo = range_start(c, r.qt, r.rt, r.n_ctas);
+    r.hi = range_start(c + 1, r.qt, r.rt, r.n_ctas);
+    int carry = 0;
     for (int b0 = 0; b0 < L.B; b0 += 32) {
         const int b = b0 + lane;
         int P = P0, n = n0, t = t0;
@@ -175,7 +189,7 @@ __device__ inline PlanSeq plan_locate(const Layout &L, const int32_t *prefix_len
             const int y = __shfl_up_sync(0xffffffffu, incl, o);
             if (lane >= o) incl += y;
         }
-        const long long start = carry + incl - t;
+        const int start = carry + incl - t;
         const unsigned hit = __ballot_sync(0xffffffffu, t > 0 && r.lo >= start && r.lo < start + t);
         if (hit) {
             const int src = __ffs(hit) - 1;
@@ -280,6 +294,11 @@ __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.comm
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 // Wait until every committed bulk store of this thread has completed.
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Bring the line holding p into L1 (no register result).
+__device__ __forceinline__ void prefetch_l1(const void *p) {
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+}
 
 // Generic-proxy shared-memory writes -> visible to the async proxy (TMA/MMA).
 __device__ __forceinline__ void fence_proxy_async_smem() {
