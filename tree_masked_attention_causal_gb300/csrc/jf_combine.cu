@@ -13,9 +13,10 @@
 //   O = sum_s w_s o_s / sum_s w_s,   w_s = 2^(m_s - M) l_s,   M = max_s m_s.
 // The sums run in split order, so the result is deterministic.
 //
-// Grid (units, 128 / 8 rows), one warp per row, lane k holding d/32
-// consecutive columns. The (m, l) of all splits and the O rows of up to 8
-// splits are loaded in one round trip. The kernel is a programmatic
+// Grid (units, 128 / 16 rows), two rows per warp (16 lanes each, lane k
+// holding d/16 consecutive columns), so that every block of a work unit of
+// the benchmark shape is resident in one wave. The (m, l) of all splits and
+// the O rows of the first 4 splits are requested in one round trip. The kernel is a programmatic
 // dependent of the attention kernel: it validates the tree (inputs only)
 // while that kernel runs, then waits for it before reading any partial or
 // writing any output.
@@ -24,12 +25,29 @@
 namespace jf {
 namespace {
 
-constexpr int kCombineRowsPerBlock = 8;      // one warp per row
-constexpr int kCombineThreads = 32 * kCombineRowsPerBlock;
-constexpr int kCombineBatch = 8;             // splits whose loads are issued together
+constexpr int kCombineRowsPerBlock = 16;     // two rows per warp, 16 lanes per row
+constexpr int kCombineThreads = 256;
+constexpr int kCombineBatch = 4;             // splits whose loads are issued together
+constexpr int kGroup = 16;                   // lanes per row
+
+// Loads of E consecutive fp16 (E = 8: 16 B, E = 4: 8 B).
+template <int E>
+struct HalfVec;
+template <>
+struct HalfVec<8> {
+    uint4 v;
+    __device__ void load(const __half *p) { v = __ldcg(reinterpret_cast<const uint4 *>(p)); }
+    __device__ uint32_t word(int k) const { return k == 0 ? v.x : k == 1 ? v.y : k == 2 ? v.z : v.w; }
+};
+template <>
+struct HalfVec<4> {
+    uint2 v;
+    __device__ void load(const __half *p) { v = __ldcg(reinterpret_cast<const uint2 *>(p)); }
+    __device__ uint32_t word(int k) const { return k == 0 ? v.x : v.y; }
+};
 
 template <int D>
-__global__ void __launch_bounds__(kCombineThreads) split_combine_kernel(const Layout L, const AttnArgs a) {
+__global__ void __launch_bounds__(kCombineThreads, 4) split_combine_kernel(const Layout L, const AttnArgs a) {
     const int q = blockIdx.x;
     const int b = q / (L.Hkv * L.QT);
     const int rem = q - b * (L.Hkv * L.QT);
@@ -45,19 +63,21 @@ __global__ void __launch_bounds__(kCombineThreads) split_combine_kernel(const La
     bad = __syncthreads_or(bad);
     pdl_wait_prior_grid();          // the attention grid is complete from here on
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int r = blockIdx.y * kCombineRowsPerBlock + warp;
+    const int g = lane & (kGroup - 1);                     // lane within the row's group
+    const unsigned gmask = (lane < kGroup) ? 0x0000FFFFu : 0xFFFF0000u;
+    const int r = blockIdx.y * kCombineRowsPerBlock + warp * 2 + (lane >> 4);
     const int node = qt * L.NB + r / L.G;
-    if (node >= L.Nmax) return;
+    if (node >= L.Nmax) return;                            // whole 16-lane groups leave together
     const int head = kh * L.G + r % L.G;
-    constexpr int E = D / 32;   // columns per lane
-    __nv_bfloat16 *dst = a.out + (((size_t)b * L.Nmax + node) * L.Hq + head) * D + lane * E;
+    constexpr int E = D / kGroup;                          // columns per lane
+    __nv_bfloat16 *dst = a.out + (((size_t)b * L.Nmax + node) * L.Hq + head) * D + g * E;
     if (bad) {
         if (kh == 0 && qt == 0 && blockIdx.y == 0 && threadIdx.x == 0) set_status(a.status, JF_STATUS_BAD_TREE);
         const uint32_t nan2 = 0x7FC07FC0u;
-        if constexpr (E == 4)
-            *reinterpret_cast<uint2 *>(dst) = make_uint2(nan2, nan2);
+        if constexpr (E == 8)
+            *reinterpret_cast<uint4 *>(dst) = make_uint4(nan2, nan2, nan2, nan2);
         else
-            *reinterpret_cast<uint32_t *>(dst) = nan2;
+            *reinterpret_cast<uint2 *>(dst) = make_uint2(nan2, nan2);
         return;
     }
     if (node >= n || unit_tiles(P, n, qt, L) == 0) return;
@@ -74,47 +94,44 @@ __global__ void __launch_bounds__(kCombineThreads) split_combine_kernel(const La
     const float2 *ml = reinterpret_cast<const float2 *>(a.ws + L.ml_off);
     const __half *op = reinterpret_cast<const __half *>(a.ws + L.opart_off);
     constexpr float kNegInf = -__builtin_huge_valf();
-    // (m_s, l_s): lane s holds split s (splits past 32 are folded in below)
-    float2 mine = make_float2(kNegInf, 0.f);
-    if (lane < ns) mine = __ldcg(&ml[(size_t)slot_of(lane) * kRows + r]);
-    float M = mine.x;
-    for (int s = 32 + lane; s < ns; s += 32) M = fmaxf(M, __ldcg(&ml[(size_t)slot_of(s) * kRows + r]).x);
+    // The first batch of O pieces is requested together with (m, l).
+    HalfVec<E> v[kCombineBatch];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    for (int k = 0; k < kCombineBatch; ++k)
+        if (k < ns) v[k].load(op + ((size_t)slot_of(k) * kRows + r) * D + g * E);
+    // (m_s, l_s): lane g of the group holds split g (more are folded in below)
+    float2 mine = make_float2(kNegInf, 0.f);
+    if (g < ns) mine = __ldcg(&ml[(size_t)slot_of(g) * kRows + r]);
+    float M = mine.x;
+    for (int s = kGroup + g; s < ns; s += kGroup) M = fmaxf(M, __ldcg(&ml[(size_t)slot_of(s) * kRows + r]).x);
+#pragma unroll
+    for (int o = kGroup / 2; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(gmask, M, o));
     if (M == kNegInf) M = 0.f;
     float acc[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) acc[e] = 0.f;
     float Lsum = 0.f;
+    const int gbase = lane & kGroup;                       // first lane of this row's group
     for (int s0 = 0; s0 < ns; s0 += kCombineBatch) {
-        uint32_t v[kCombineBatch][E / 2];           // fp16 pairs
+        if (s0 > 0) {
 #pragma unroll
-        for (int k = 0; k < kCombineBatch; ++k) {    // all loads of the batch first
-            const int s = s0 + k;
-            if (s < ns) {
-                const __half *src = op + ((size_t)slot_of(s) * kRows + r) * D + lane * E;
-                if constexpr (E == 4) {
-                    const uint2 x = __ldcg(reinterpret_cast<const uint2 *>(src));
-                    v[k][0] = x.x;
-                    v[k][1] = x.y;
-                } else {
-                    v[k][0] = __ldcg(reinterpret_cast<const unsigned int *>(src));
-                }
-            }
+            for (int k = 0; k < kCombineBatch; ++k)
+                if (s0 + k < ns) v[k].load(op + ((size_t)slot_of(s0 + k) * kRows + r) * D + g * E);
         }
 #pragma unroll
-        for (int k = 0; k < kCombineBatch; ++k) {    // then the weighted sums, in split order
+        for (int k = 0; k < kCombineBatch; ++k) {          // weighted sums, in split order
             const int s = s0 + k;
             if (s < ns) {
-                const float2 mls = s < 32 ? make_float2(__shfl_sync(0xffffffffu, mine.x, s),
-                                                        __shfl_sync(0xffffffffu, mine.y, s))
-                                          : __ldcg(&ml[(size_t)slot_of(s) * kRows + r]);
+                const float2 mls = s < kGroup ? make_float2(__shfl_sync(gmask, mine.x, gbase + s),
+                                                            __shfl_sync(gmask, mine.y, gbase + s))
+                                              : __ldcg(&ml[(size_t)slot_of(s) * kRows + r]);
                 // the piece is O_s / l_s: its weight in the sum is 2^(m_s - M) l_s
                 const float w = ex2_approx(mls.x - M) * mls.y;
                 Lsum += w;
 #pragma unroll
                 for (int e = 0; e < E / 2; ++e) {
-                    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&v[k][e]));
+                    const uint32_t h2 = v[k].word(e);
+                    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&h2));
                     acc[2 * e] += w * f.x;
                     acc[2 * e + 1] += w * f.y;
                 }
@@ -122,11 +139,13 @@ __global__ void __launch_bounds__(kCombineThreads) split_combine_kernel(const La
         }
     }
     const float inv = 1.0f / Lsum;
-    if constexpr (E == 4) {
+    if constexpr (E == 8) {
+        *reinterpret_cast<uint4 *>(dst) =
+            make_uint4(pack_bf16x2(acc[0] * inv, acc[1] * inv), pack_bf16x2(acc[2] * inv, acc[3] * inv),
+                       pack_bf16x2(acc[4] * inv, acc[5] * inv), pack_bf16x2(acc[6] * inv, acc[7] * inv));
+    } else {
         *reinterpret_cast<uint2 *>(dst) = make_uint2(pack_bf16x2(acc[0] * inv, acc[1] * inv),
                                                      pack_bf16x2(acc[2] * inv, acc[3] * inv));
-    } else {
-        *reinterpret_cast<uint32_t *>(dst) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
     }
 }
 
