@@ -77,7 +77,7 @@ int32_t check_shape(const jf_shape *s, bool need_vocab, bool need_attn) {
         if ((long long)s->batch * s->n_kv_heads * s->prefix_cap > 0x7FFFFFFFll) return JF_ERR_SHAPE;
         // the stream-K plan counts key tiles of all work units in 32 bits
         const long long units = (long long)s->batch * s->n_kv_heads * ((s->max_nodes * G + kRows - 1) / kRows);
-        if (units * ((s->prefix_cap + kBN - 1) / kBN + (s->max_nodes + kBN - 1) / kBN) > 0x7FFFFFFFll)
+        if (units * ((s->prefix_cap + kBN - 1) / kBN + (s->max_nodes + kBN - 1) / kBN + kSwitchTiles) > 0x7FFFFFFFll)
             return JF_ERR_SHAPE;
     }
     if (need_vocab) {

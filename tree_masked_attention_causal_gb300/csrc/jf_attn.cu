@@ -130,20 +130,23 @@ __device__ __forceinline__ void producer_loop(const AttnMaps &maps, const Layout
     // from prefix_lens and n_nodes (no earlier kernel needed).
     const int c = blockIdx.x;
     const PlanSeq ps = plan_locate(L, a.prefix_lens, a.n_nodes, c, a.num_ctas);
-    const int lo0 = ps.lo, hi = ps.hi;
-    int lo = lo0;
-    // The unit (b, kh, qt) holding tile lo, and its first tile S.
+    const int alpha = ps.alpha;
+    const int hi = ps.hi;
+    int lo = ps.lo;
+    // The unit (b, kh, qt) holding virtual tile lo, and its first virtual
+    // tile S (its real tiles start at S + alpha).
     int b = ps.b, kh = 0, qt = 0, P = ps.P, n = ps.n;
     int S = 0;
     if (lo < hi) {
         if (b < 0) {
             lo = hi;                        // unreachable for a consistent plan
         } else {
-            const int th = head_tiles(P, n, L);
+            const int th = head_tiles(P, n, L) + alpha * head_units(n, L);
             kh = (lo - ps.seq_start) / th;
             S = ps.seq_start + kh * th;
-            for (int ut = unit_tiles(P, n, 0, L); S + ut <= lo && qt + 1 < L.QT; ut = unit_tiles(P, n, qt, L)) {
-                S += ut;
+            for (int us = unit_tiles(P, n, 0, L) + alpha; S + us <= lo && qt + 1 < L.QT;
+                 us = unit_tiles(P, n, qt, L) + alpha) {
+                S += us;
                 ++qt;
             }
         }
@@ -175,8 +178,13 @@ __device__ __forceinline__ void producer_loop(const AttnMaps &maps, const Layout
         if (!mbar_wait(bar(C::B_ITEM_EMPTY + slot), ((ic >> 1) & 1) ^ 1, abort, a.status)) break;
         ItemInfo info{};
         int t_next = 0;
+        if (lo < hi) {                      // skip the unit's virtual tiles
+            if (S + alpha >= hi) lo = hi;
+            else if (lo < S + alpha) lo = S + alpha;
+        }
         if (lo < hi) {
             const int T = unit_tiles(P, n, qt, L);
+            S += alpha;                     // S: the unit's first real tile
             const int u = (b * L.Hkv + kh) * L.QT + qt;
             info.valid = 1;
             info.qtile = u;
@@ -207,8 +215,8 @@ __device__ __forceinline__ void producer_loop(const AttnMaps &maps, const Layout
             // A split unit is at most this CTA's first item (slot 2c) or its
             // last (slot 2c + 1): units in between lie wholly in the range.
             info.slot = info.ns > 1 ? 2 * c + (ic > 0 ? 1 : 0) : -1;
-            if (S >= lo0 && lane == 0)      // the unit starts in this range: record its split plan
-                qtab[u] = QTile{info.ns, c, S == lo0 ? 1 : 0, S};
+            if (info.tb == 0 && lane == 0)  // the unit starts in this range: record its split plan
+                qtab[u] = QTile{info.ns, c, ic == 0 ? 1 : 0, S};
             lo = S + info.te;
             S += T;
             if (lo < hi) {                  // the next unit with tiles

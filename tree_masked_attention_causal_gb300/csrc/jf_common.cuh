@@ -134,22 +134,34 @@ __device__ __forceinline__ int cta_of_tile(int x, int qt, int rt, int C) {
 // tile lo with its first tile, prefix length and node count (every lane gets
 // the same). One pass over the sequences; a batch of up to 32 sequences is
 // read from memory once.
+// The split is weighted: every unit with work is preceded by alpha virtual
+// tiles, and the virtual sequence is cut into C equal ranges. A CTA whose
+// range crosses into another unit (an extra epilogue and pipeline refill)
+// thus gets about alpha fewer real tiles. alpha = min(kSwitchTiles, half of
+// the real tiles per CTA), so that no range can hold virtual tiles only.
+constexpr int kSwitchTiles = 3;
+
 struct PlanSeq {
-    int total, n_ctas;
-    int qt, rt;         // total = n_ctas * qt + rt
-    int lo, hi;
-    int b, P, n;
-    int seq_start;
+    int n_ctas, alpha;
+    int qt, rt;         // virtual total = n_ctas * qt + rt
+    int lo, hi;         // this CTA's virtual range
+    int b, P, n;        // the sequence holding virtual tile lo
+    int seq_start;      // its first virtual tile
 };
 
+// Units with work in one KV head of a valid sequence.
+__device__ __forceinline__ int head_units(int n, const Layout &L) { return ceil_div(n, L.NB); }
+
+// Warp-collective: the plan as seen from CTA c (every lane gets the same).
+// One pass over the sequences; a batch of up to 32 sequences is read from
+// memory once.
 __device__ inline PlanSeq plan_locate(const Layout &L, const int32_t *prefix_lens, const int32_t *n_nodes, int c,
                                       int num_ctas) {
     const int lane = threadIdx.x & 31;
     PlanSeq r{};
     r.b = -1;
-    auto seq_tiles = [&](int P, int n) { return seq_valid(P, n, L) ? L.Hkv * head_tiles(P, n, L) : 0; };
-    int P0 = 0, n0 = 0, t0 = 0;                      // this lane's sequence of the first 32
-    int sum = 0;
+    int P0 = 0, n0 = 0;                              // this lane's sequence of the first 32
+    int tiles = 0, units = 0;
     for (int b0 = 0; b0 < L.B; b0 += 32) {
         const int b = b0 + lane;
         int P = 0, n = 0;
@@ -157,32 +169,38 @@ __device__ inline PlanSeq plan_locate(const Layout &L, const int32_t *prefix_len
             P = prefix_lens[b];
             n = n_nodes[b];
         }
-        const int t = b < L.B ? seq_tiles(P, n) : 0;
         if (b0 == 0) {
             P0 = P;
             n0 = n;
-            t0 = t;
         }
-        sum += t;
+        if (b < L.B && seq_valid(P, n, L)) {
+            tiles += L.Hkv * head_tiles(P, n, L);
+            units += L.Hkv * head_units(n, L);
+        }
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-    r.total = sum;
-    r.n_ctas = sum > 0 ? plan_ctas(sum, num_ctas) : 0;
+    for (int o = 16; o > 0; o >>= 1) {
+        tiles += __shfl_xor_sync(0xffffffffu, tiles, o);
+        units += __shfl_xor_sync(0xffffffffu, units, o);
+    }
+    r.n_ctas = tiles > 0 ? plan_ctas(tiles, num_ctas) : 0;
     if (c >= r.n_ctas) return r;
-    r.qt = sum / r.n_ctas;
-    r.rt = sum - r.qt * r.n_ctas;
+    r.alpha = min(kSwitchTiles, tiles / r.n_ctas / 2);
+    const int total_v = tiles + r.alpha * units;
+    r.qt = total_v / r.n_ctas;
+    r.rt = total_v - r.qt * r.n_ctas;
     r.lo = range_start(c, r.qt, r.rt, r.n_ctas);
     r.hi = range_start(c + 1, r.qt, r.rt, r.n_ctas);
     int carry = 0;
     for (int b0 = 0; b0 < L.B; b0 += 32) {
         const int b = b0 + lane;
-        int P = P0, n = n0, t = t0;
+        int P = P0, n = n0;
         if (b0 > 0) {
             P = b < L.B ? prefix_lens[b] : 0;
             n = b < L.B ? n_nodes[b] : 0;
-            t = b < L.B ? seq_tiles(P, n) : 0;
         }
+        const int t = (b < L.B && seq_valid(P, n, L))
+                          ? L.Hkv * (head_tiles(P, n, L) + r.alpha * head_units(n, L)) : 0;
         int incl = t;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
