@@ -525,6 +525,19 @@ __device__ __forceinline__ void softmax_loop(const AttnMaps &maps, const Layout 
         for (int k = 0; k < 4; ++k) m4[k] = fmaxf(m4[k], __uint_as_float(sv[kBN - 4 + k]));
         return fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
     };
+    // P = 2^(s * sl2 - m) of 64 keys as bf16 pairs; returns their fp32 sum.
+    auto exp64h = [&](const uint32_t (&sv)[kHalf], float neg_m, uint32_t (&pv)[kHalf / 2]) {
+        float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int c = 0; c < kHalf; c += 2) {
+            const float p0 = ex2_approx(fmaf(__uint_as_float(sv[c]), sl2, neg_m));
+            const float p1 = ex2_approx(fmaf(__uint_as_float(sv[c + 1]), sl2, neg_m));
+            sum4[c & 3] += p0;
+            sum4[(c + 1) & 3] += p1;
+            pv[c >> 1] = pack_bf16x2(p0, p1);
+        }
+        return (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
+    };
     // P = 2^(s * sl2 - m) of keys h*64..h*64+63 as bf16 pairs; returns their fp32 sum.
     auto exp64 = [&](const uint32_t (&sv)[kBN], int h, float neg_m, uint32_t (&pv)[kHalf / 2]) {
         float sum4[4] = {0.f, 0.f, 0.f, 0.f};
@@ -567,10 +580,18 @@ __device__ __forceinline__ void softmax_loop(const AttnMaps &maps, const Layout 
             const uint32_t t_s = t_row + sb * 128;
             if (!mbar_wait(bar(C::B_S_FULL + sb), (g / C::NS) & 1, abort, a.status)) { fail = true; break; }
             tc_fence_after();
-            uint32_t sv[kBN];                              // the whole row of the tile
-            tmem_ld128(t_s, sv);
-            mask128(sv, tree, mw, lim);
-            const float mt = max128(sv) * sl2;
+            float mt;
+            {
+                uint32_t sv[kBN];                          // the whole row of the tile
+                tmem_ld128(t_s, sv);
+                if (tree || lim < kBN) {                   // rare: write the masked row back for the exp pass
+                    mask128(sv, tree, mw, lim);
+#pragma unroll
+                    for (int c4 = 0; c4 < 4; ++c4) tmem_st32(t_s + 32 * c4, *reinterpret_cast<uint32_t(*)[32]>(&sv[32 * c4]));
+                    tmem_wait_st();
+                }
+                mt = max128(sv) * sl2;
+            }
             float m_new = mt, m_prev = kNegInf;
             bool need = false;
             if (j > 0) {
@@ -603,11 +624,17 @@ __device__ __forceinline__ void softmax_loop(const AttnMaps &maps, const Layout 
                 m_own = m_run;
             }
             const float neg_m = (m_run == kNegInf) ? 0.f : -m_run;
-            uint32_t pv[kHalf / 2];
-            float lsum = exp64(sv, 0, neg_m, pv);
-            tmem_st32(t_s, pv);                            // P of keys 0-63 -> S columns 0-31
-            lsum += exp64(sv, 1, neg_m, pv);
-            tmem_st32(t_s + 32, pv);                       // P of keys 64-127 -> S columns 32-63
+            // exp pass in two rolled halves, each read again from TMEM: one
+            // copy of the exp code instead of two keeps the hot loop small
+            float lsum = 0.f;
+#pragma unroll 1
+            for (int h = 0; h < 2; ++h) {
+                uint32_t sh[kHalf];
+                tmem_ld64(t_s + kHalf * h, sh);
+                uint32_t pv[kHalf / 2];
+                lsum += exp64h(sh, neg_m, pv);
+                tmem_st32(t_s + (kHalf / 2) * h, pv);      // P of keys 64h.. -> S columns 32h..
+            }
             l_own += lsum;
             tmem_wait_st();
             tc_fence_before();
