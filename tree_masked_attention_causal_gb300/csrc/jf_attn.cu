@@ -46,8 +46,10 @@
 //    softmax, and a buffer returns to the QK issuer when the PV that read its
 //    P completes.
 //  * Softmax per tile (one warp per row quadrant): one 128-column TMEM load
-//    into registers, the row max, the running max handed over from the
-//    previous tile's owner, ex2 on the MUFU pipe, bf16 packing, P stored.
+//    for the row max, the running max handed over from the previous tile's
+//    owner, then ex2 on the MUFU pipe, bf16 packing and the P store in a
+//    rolled loop over 32-column chunks read again from TMEM. The kernel is
+//    instruction-fetch bound, so the hot loop is kept small.
 //  * Online softmax in the exp2 domain, lazy rescale: O is rescaled only
 //    when a row max grows by more than 2^8, by the owner of that tile, once
 //    the previous tile's PV has completed. The first PV of an item waits
@@ -451,16 +453,16 @@ __device__ __forceinline__ uint4 ancestor_bits(const int32_t *parents, int node,
 // epilogue. O is rescaled, when needed, by the owner of the tile that raised
 // the max, after the PV of the previous tile has completed.
 //
-// The warp holds the tile's whole 128-key row in registers (one TMEM load);
-// the softmax warpgroups get 216 registers per thread for it (setmaxnreg),
-// the producer and issuer warpgroup 72. P (bf16 pairs) goes back over the S
-// columns 0-63 of its buffer.
+// The warp reads the tile's whole 128-key row once for the row max, then
+// runs the exp pass over 32-column chunks read again from TMEM. The softmax
+// warpgroups get 216 registers per thread (setmaxnreg), the producer and
+// issuer warpgroup 72. P (bf16 pairs) goes back over the S columns 0-63 of
+// its buffer.
 template <int D>
 __device__ __forceinline__ void softmax_loop(const AttnMaps &maps, const Layout &L, const AttnArgs &a,
                                              uint8_t *smem, uint32_t bars, const ItemInfo *items_s, float *hand,
                                              float *xchg, uint32_t tmem, volatile int *abort) {
     using C = AttnCfg<D>;
-    constexpr int kHalf = kBN / 2;                  // keys per TMEM load
     constexpr int kOHalf = D / 2;                   // O columns per warp in the epilogue
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int q = warp & 3, par = warp >> 2;        // row quadrant, tile parity (= epilogue column half)
@@ -525,41 +527,14 @@ __device__ __forceinline__ void softmax_loop(const AttnMaps &maps, const Layout 
         for (int k = 0; k < 4; ++k) m4[k] = fmaxf(m4[k], __uint_as_float(sv[kBN - 4 + k]));
         return fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
     };
-    // P = 2^(s * sl2 - m) of 64 keys as bf16 pairs; returns their fp32 sum.
-    auto exp64h = [&](const uint32_t (&sv)[kHalf], float neg_m, uint32_t (&pv)[kHalf / 2]) {
-        float sum4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int c = 0; c < kHalf; c += 2) {
-            const float p0 = ex2_approx(fmaf(__uint_as_float(sv[c]), sl2, neg_m));
-            const float p1 = ex2_approx(fmaf(__uint_as_float(sv[c + 1]), sl2, neg_m));
-            sum4[c & 3] += p0;
-            sum4[(c + 1) & 3] += p1;
-            pv[c >> 1] = pack_bf16x2(p0, p1);
-        }
-        return (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
-    };
-    // P = 2^(s * sl2 - m) of keys h*64..h*64+63 as bf16 pairs; returns their fp32 sum.
-    auto exp64 = [&](const uint32_t (&sv)[kBN], int h, float neg_m, uint32_t (&pv)[kHalf / 2]) {
-        float sum4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int c = 0; c < kHalf; c += 2) {
-            const float p0 = ex2_approx(fmaf(__uint_as_float(sv[h * kHalf + c]), sl2, neg_m));
-            const float p1 = ex2_approx(fmaf(__uint_as_float(sv[h * kHalf + c + 1]), sl2, neg_m));
-            sum4[c & 3] += p0;
-            sum4[(c + 1) & 3] += p1;
-            pv[c >> 1] = pack_bf16x2(p0, p1);
-        }
-        return (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
-    };
-
     while (true) {
         const int slot = ic & 1;
         if (!mbar_wait(bar(C::B_ITEM_FULL + slot), (ic >> 1) & 1, abort, a.status)) break;
         const ItemInfo info = items_s[slot];
         ++ic;
         if (!info.valid) break;
-        const int node = info.qt * L.NB + r / L.G;
-        const int head = info.kh * L.G + r % L.G;
+        const int node = (info.qt << L.lgNB) + (r >> L.lgG);
+        const int head = (info.kh << L.lgG) + (r & (L.G - 1));
         const bool row_valid = node < info.n;
         const int32_t *par_b = a.parents + (size_t)info.b * L.Nmax;
         // The ancestor walks of the item's tree tiles read this sequence's
@@ -628,12 +603,21 @@ __device__ __forceinline__ void softmax_loop(const AttnMaps &maps, const Layout 
             // copy of the exp code instead of two keeps the hot loop small
             float lsum = 0.f;
 #pragma unroll 1
-            for (int h = 0; h < 2; ++h) {
-                uint32_t sh[kHalf];
-                tmem_ld64(t_s + kHalf * h, sh);
-                uint32_t pv[kHalf / 2];
-                lsum += exp64h(sh, neg_m, pv);
-                tmem_st32(t_s + (kHalf / 2) * h, pv);      // P of keys 64h.. -> S columns 32h..
+            for (int h = 0; h < 4; ++h) {
+                uint32_t sh[32];
+                tmem_ld32(t_s + 32 * h, sh);
+                uint32_t pv[16];
+                float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int c = 0; c < 32; c += 2) {
+                    const float p0 = ex2_approx(fmaf(__uint_as_float(sh[c]), sl2, neg_m));
+                    const float p1 = ex2_approx(fmaf(__uint_as_float(sh[c + 1]), sl2, neg_m));
+                    sum4[c & 3] += p0;
+                    sum4[(c + 1) & 3] += p1;
+                    pv[c >> 1] = pack_bf16x2(p0, p1);
+                }
+                lsum += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
+                tmem_st16(t_s + 16 * h, pv);               // P of keys 32h.. -> S columns 16h..
             }
             l_own += lsum;
             tmem_wait_st();
@@ -674,20 +658,20 @@ __device__ __forceinline__ void softmax_loop(const AttnMaps &maps, const Layout 
         // divided by their own l, with (m, l) beside them for the merge.
         const bool split = info.ns > 1;
         const float inv_l = 1.0f / l_run;
-        auto pack8 = [&](int k) {
-            auto f = [&](int e) { return __uint_as_float(ov[8 * k + e]) * inv_l; };
-            uint32_t w[4];
+        // Scaled and packed in place: ov[2k] holds the pair for columns 2k, 2k+1.
+        if (split) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                if (split) {
-                    const __half2 h = __floats2half2_rn(f(2 * e), f(2 * e + 1));
-                    w[e] = *reinterpret_cast<const uint32_t *>(&h);
-                } else {
-                    w[e] = pack_bf16x2(f(2 * e), f(2 * e + 1));
-                }
+            for (int e = 0; e < kOHalf / 2; ++e) {
+                const __half2 h = __floats2half2_rn(__uint_as_float(ov[2 * e]) * inv_l,
+                                                    __uint_as_float(ov[2 * e + 1]) * inv_l);
+                ov[e] = *reinterpret_cast<const uint32_t *>(&h);
             }
-            return make_uint4(w[0], w[1], w[2], w[3]);
-        };
+        } else {
+#pragma unroll
+            for (int e = 0; e < kOHalf / 2; ++e)
+                ov[e] = pack_bf16x2(__uint_as_float(ov[2 * e]) * inv_l, __uint_as_float(ov[2 * e + 1]) * inv_l);
+        }
+        auto pack8 = [&](int k) { return make_uint4(ov[4 * k], ov[4 * k + 1], ov[4 * k + 2], ov[4 * k + 3]); };
         // A unit whose rows are all real nodes is staged in its own Q buffer
         // (free since its last QK^T) in the 128-byte-swizzled box layout and
         // written by TMA bulk stores: one wide store instead of 32 scattered

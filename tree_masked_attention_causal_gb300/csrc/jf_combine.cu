@@ -66,9 +66,9 @@ __global__ void __launch_bounds__(kCombineThreads, 4) split_combine_kernel(const
     const int g = lane & (kGroup - 1);                     // lane within the row's group
     const unsigned gmask = (lane < kGroup) ? 0x0000FFFFu : 0xFFFF0000u;
     const int r = blockIdx.y * kCombineRowsPerBlock + warp * 2 + (lane >> 4);
-    const int node = qt * L.NB + r / L.G;
+    const int node = (qt << L.lgNB) + (r >> L.lgG);
     if (node >= L.Nmax) return;                            // whole 16-lane groups leave together
-    const int head = kh * L.G + r % L.G;
+    const int head = (kh << L.lgG) + (r & (L.G - 1));
     constexpr int E = D / kGroup;                          // columns per lane
     __nv_bfloat16 *dst = a.out + (((size_t)b * L.Nmax + node) * L.Hq + head) * D + g * E;
     if (bad) {

@@ -21,7 +21,7 @@ namespace jf {
 // ---------------------------------------------------------------- tiling
 constexpr int kBM = 128;          // rows of one tcgen05 MMA tile (= TMEM lanes)
 constexpr int kRows = 128;        // stacked query rows per work unit (one MMA tile)
-constexpr int kBN = 128;          // keys per KV tile
+constexpr int kBN = 128;          // keys per KV tile (the plan divides by it with >> 7)
 constexpr int kMaxNodes = 256;    // tree slots per sequence
 constexpr int kMaxCtas = 256;     // cap on the persistent attention grid
 constexpr int kMinTilesPerCta = 2;   // smallest key range a CTA is given
@@ -50,6 +50,7 @@ struct Layout {
     int32_t B, Nmax, Hq, Hkv, G, D, Pcap, V;
     int32_t QT;          // work units per (sequence, kv head)
     int32_t NB;          // nodes per work unit = kRows / G
+    int32_t lgG, lgNB;   // log2 of G and NB (both powers of two)
     int32_t n_qtiles;    // work units: B * Hkv * QT
     int32_t max_pieces;  // partial slots: two per CTA (its first and its last item)
     int32_t chunks;      // argmax chunks per logits row
@@ -65,6 +66,9 @@ inline Layout make_layout(int B, int Nmax, int Hq, int Hkv, int D, int Pcap, int
     Layout L{};
     L.B = B; L.Nmax = Nmax; L.Hq = Hq; L.Hkv = Hkv; L.G = Hq / Hkv; L.D = D; L.Pcap = Pcap; L.V = V;
     L.NB = kRows / L.G;
+    L.lgG = 0;
+    while ((1 << L.lgG) < L.G) ++L.lgG;
+    L.lgNB = 7 - L.lgG;   // kRows = 128
     L.QT = ceil_div(Nmax, L.NB);
     L.n_qtiles = B * Hkv * L.QT;
     L.max_pieces = 2 * kMaxCtas;
@@ -95,18 +99,18 @@ __host__ __device__ inline bool seq_valid(int P, int n, const Layout &L) {
 }
 
 __device__ __forceinline__ int unit_tiles(int P, int n, int qt, const Layout &L) {
-    const int node0 = qt * L.NB;
+    const int node0 = qt << L.lgNB;
     if (node0 >= n) return 0;
-    return ceil_div(P, kBN) + ceil_div(min(node0 + L.NB, n), kBN);
+    return ((P + kBN - 1) >> 7) + ((min(node0 + L.NB, n) + kBN - 1) >> 7);
 }
 
 // Tiles of all units of one KV head of a valid sequence, in closed form:
 // unit qt < nq - 1 reaches node (qt + 1) * NB, i.e. ceil((qt + 1) / G) tree
 // tiles since NB * G = 128, and the last unit reaches node n.
 __device__ __forceinline__ int head_tiles(int P, int n, const Layout &L) {
-    const int nq = ceil_div(n, L.NB);
-    const int m = nq - 1, q = m / L.G, r = m - q * L.G;
-    return nq * ceil_div(P, kBN) + L.G * q * (q + 1) / 2 + r * (q + 1) + ceil_div(n, kBN);
+    const int nq = (n + L.NB - 1) >> L.lgNB;
+    const int m = nq - 1, q = m >> L.lgG, r = m - (q << L.lgG);
+    return nq * ((P + kBN - 1) >> 7) + ((q * (q + 1) / 2) << L.lgG) + r * (q + 1) + ((n + kBN - 1) >> 7);
 }
 
 __device__ __forceinline__ int plan_ctas(int total, int num_ctas) {
@@ -122,6 +126,7 @@ __device__ __forceinline__ int range_start(int c, int qt, int rt, int C) { retur
 __device__ __forceinline__ int cta_of_tile(int x, int qt, int rt, int C) {
     const int lane = threadIdx.x & 31;
     int n = 0;
+#pragma unroll 1
     for (int c0 = 1; c0 < C; c0 += 32) {
         const int c = c0 + lane;
         n += __popc(__ballot_sync(0xffffffffu, c < C && range_start(c, qt, rt, C) <= x));
@@ -150,7 +155,7 @@ struct PlanSeq {
 };
 
 // Units with work in one KV head of a valid sequence.
-__device__ __forceinline__ int head_units(int n, const Layout &L) { return ceil_div(n, L.NB); }
+__device__ __forceinline__ int head_units(int n, const Layout &L) { return (n + L.NB - 1) >> L.lgNB; }
 
 // Warp-collective: the plan as seen from CTA c (every lane gets the same).
 // One pass over the sequences; a batch of up to 32 sequences is read from
@@ -162,6 +167,7 @@ __device__ inline PlanSeq plan_locate(const Layout &L, const int32_t *prefix_len
     r.b = -1;
     int P0 = 0, n0 = 0;                              // this lane's sequence of the first 32
     int tiles = 0, units = 0;
+#pragma unroll 1
     for (int b0 = 0; b0 < L.B; b0 += 32) {
         const int b = b0 + lane;
         int P = 0, n = 0;
@@ -192,6 +198,7 @@ __device__ inline PlanSeq plan_locate(const Layout &L, const int32_t *prefix_len
     r.lo = range_start(c, r.qt, r.rt, r.n_ctas);
     r.hi = range_start(c + 1, r.qt, r.rt, r.n_ctas);
     int carry = 0;
+#pragma unroll 1
     for (int b0 = 0; b0 < L.B; b0 += 32) {
         const int b = b0 + lane;
         int P = P0, n = n0;
@@ -429,6 +436,15 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32
         "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
         "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
         JF_W8(0), JF_W8(8), JF_W8(16), JF_W8(24)
+        : "memory");
+}
+
+// Store 16 consecutive 32-bit columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+        "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
         : "memory");
 }
 
