@@ -780,6 +780,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
+    // The inputs may come from the previous kernel of the stream.
+    pdl_wait_prior_grid();
     // The combine kernel may launch now: it waits for this grid before it
     // reads any partial or writes any output.
     pdl_launch_dependents();
@@ -832,6 +834,11 @@ cudaError_t launch_d(const Layout &L, const AttnMaps &m, const AttnArgs &a, cuda
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = C::smem_request;
     cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     trace_begin("tree_attention", s);
     e = cudaLaunchKernelEx(&cfg, tree_attention_kernel<D>, m, L, a);
     if (e == cudaSuccess) e = cudaGetLastError();

@@ -154,6 +154,7 @@ __global__ void __launch_bounds__(kMaxNodes)
     __shared__ int am[kMaxNodes];
     __shared__ unsigned char edge_ok[kMaxNodes];
     __shared__ int red[kMaxNodes / 32];
+    pdl_launch_dependents();        // whatever follows may start its prologue
     const int b = blockIdx.x, i = threadIdx.x;
     // inputs that the scan does not write: read them before waiting on it
     const int n = n_nodes[b];
