@@ -73,10 +73,21 @@ def check_attention(inp, scale=0.0, rows=None):
     return out, status
 
 
-@pytest.mark.parametrize("G,d", [(1, 64), (2, 128), (4, 64), (8, 128), (16, 64), (32, 128)])
+@pytest.mark.parametrize("G,d", [(1, 64), (2, 128), (4, 64), (8, 128), (16, 64), (32, 128), (64, 64), (128, 128)])
 def test_gqa_groups_and_head_dims(G, d):
     Hkv = 2
     inp = small_inputs(10 + G, B=2, N=40, Hq=G * Hkv, Hkv=Hkv, d=d, Pcap=300)
+    check_attention(inp)
+
+
+def test_many_sequences_mixed_lengths():
+    """Many small and large work units: the stream-K split cuts some units
+    into several pieces, leaves others whole, and CTAs cross unit
+    boundaries; prefixes of 0, 1, 127, 128, 129 tokens and ragged trees."""
+    B = 12
+    prefixes = torch.tensor([0, 1, 127, 128, 129, 700, 5, 640, 0, 300, 64, 1000], dtype=torch.int32)
+    n_nodes = torch.tensor([40, 1, 17, 33, 40, 2, 39, 40, 8, 31, 40, 25], dtype=torch.int32)
+    inp = small_inputs(50, B=B, N=40, Hq=8, Hkv=2, d=128, Pcap=1024, prefixes=prefixes, n_nodes=n_nodes)
     check_attention(inp)
 
 
