@@ -599,27 +599,30 @@ __device__ __forceinline__ void softmax_loop(const AttnMaps &maps, const Layout 
                 m_own = m_run;
             }
             const float neg_m = (m_run == kNegInf) ? 0.f : -m_run;
-            // exp pass in two rolled halves, each read again from TMEM: one
-            // copy of the exp code instead of two keeps the hot loop small
-            float lsum = 0.f;
+            // exp pass in four rolled 32-key chunks, each read again from
+            // TMEM: one copy of the exp code keeps the hot loop small. The
+            // scaling and the sums use packed f32x2 arithmetic (one
+            // instruction per key pair).
+            const uint64_t sl2x2 = f32x2(sl2, sl2), negm2 = f32x2(neg_m, neg_m);
+            uint64_t lsum2 = f32x2(0.f, 0.f);
 #pragma unroll 1
             for (int h = 0; h < 4; ++h) {
                 uint32_t sh[32];
                 tmem_ld32(t_s + 32 * h, sh);
                 uint32_t pv[16];
-                float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+                uint64_t sum2[2] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f)};
 #pragma unroll
                 for (int c = 0; c < 32; c += 2) {
-                    const float p0 = ex2_approx(fmaf(__uint_as_float(sh[c]), sl2, neg_m));
-                    const float p1 = ex2_approx(fmaf(__uint_as_float(sh[c + 1]), sl2, neg_m));
-                    sum4[c & 3] += p0;
-                    sum4[(c + 1) & 3] += p1;
+                    const float2 x = unpack_f32x2(fma_f32x2(f32x2(sh[c], sh[c + 1]), sl2x2, negm2));
+                    const float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
+                    sum2[(c >> 1) & 1] = add_f32x2(sum2[(c >> 1) & 1], f32x2(p0, p1));
                     pv[c >> 1] = pack_bf16x2(p0, p1);
                 }
-                lsum += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
+                lsum2 = add_f32x2(lsum2, add_f32x2(sum2[0], sum2[1]));
                 tmem_st16(t_s + 16 * h, pv);               // P of keys 32h.. -> S columns 16h..
             }
-            l_own += lsum;
+            const float2 ls = unpack_f32x2(lsum2);
+            l_own += ls.x + ls.y;
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
