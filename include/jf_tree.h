@@ -192,9 +192,11 @@ JF_API int32_t jf_tree_verify(const void *logits, const int32_t *tree_tokens,
  * fixed array of JF_NOALLOC_SCRATCH_BYTES in the library's device memory.
  * Every GPU that loads the library holds that array until the process
  * exits. The call itself allocates nothing.
- *  - Limit: batch * max_nodes * ceil(vocab / 51200) * 8 bytes must be <=
- *    JF_NOALLOC_SCRATCH_BYTES (e.g. 43690 logits rows of vocab 151936).
- *    Larger problems return JF_ERR_SHAPE and launch nothing.
+ *  - Limit: rows * chunks * 8 bytes must be <= JF_NOALLOC_SCRATCH_BYTES,
+ *    with rows = batch * max_nodes and chunks the argmax pieces per logits
+ *    row, at most max(ceil(vocab / 76800), ceil(608 / rows)). For vocab
+ *    151936 that is 2 from 304 rows up, so up to 65536 rows fit. Larger
+ *    problems return JF_ERR_SHAPE and launch nothing.
  *  - The first call on a device looks up the array's device address (with
  *    that device current) and caches it. Make that first call before any
  *    stream capture.

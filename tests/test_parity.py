@@ -180,7 +180,7 @@ def check_verify(inp, max_depth=16):
 
 
 def test_verify_ties_nan_and_signed_zero():
-    inp = small_inputs(20, B=2, N=8, vocab=110000)     # three scan chunks of 51200 per row
+    inp = small_inputs(20, B=2, N=8, vocab=110000)     # 16 rows: 4096-element argmax chunks
     lg = inp["logits"]
     lg[0, 0] = 0.0
     lg[0, 1, 20000] = 9.0
@@ -191,8 +191,8 @@ def test_verify_ties_nan_and_signed_zero():
     lg[0, 3, 57000] = 0.0                              # +0 == -0: index 0 wins
     lg[0, 4] = float("-inf")
     lg[0, 5, 109999] = float("inf")
-    lg[0, 6, 51199] = 10.0                             # chunk boundary
-    lg[0, 6, 51200] = 10.0
+    lg[0, 6, 49151] = 10.0                             # chunk boundary
+    lg[0, 6, 49152] = 10.0
     lg[0, 7, 51201] = float("nan")                     # NaN only in a later chunk
     lg[1, 0, 3] = 10.0
     lg[1, 0, 7] = 10.0                                 # tie inside one 8-element vector
@@ -229,6 +229,29 @@ def test_verify_random_trees_many_matches():
     for seed in range(3):
         inp = small_inputs(30 + seed, B=8, N=64, vocab=8)
         check_verify(inp, max_depth=63)
+
+
+@pytest.mark.parametrize("B,N", [(2, 8), (2, 256)])
+def test_verify_ties_at_chunk_boundaries(B, N):
+    """Equal maxima on both sides of 2048-element boundaries (every argmax
+    chunk ends on one), ties just past them and NaN on both sides: with few
+    rows (short chunks) and with many (two chunks per row of 151936)."""
+    V = 151936
+    inp = small_inputs(23, B=B, N=N, vocab=V)
+    lg = inp["logits"]
+    for r in range(B * N):
+        b, i = divmod(r, N)
+        e = ((r % 74) + 1) * 2048
+        if r % 3 == 0:
+            lg[b, i, e - 1] = 9.0
+            lg[b, i, e] = 9.0
+        elif r % 3 == 1:
+            lg[b, i, e] = 9.0
+            lg[b, i, e + 5] = 9.0
+        else:
+            lg[b, i, e - 2048] = float("nan")
+            lg[b, i, e] = float("nan")
+    check_verify(inp)
 
 
 def test_verify_all_chunks_vocab_151936():

@@ -24,9 +24,10 @@ A16 = 1 << 20            # fake aligned address, never dereferenced
 
 def test_noalloc_refuses_problems_beyond_the_array():
     _build.build()
-    # 4 x 256 rows x 3 chunks x 8 B = 24 KB fits; 200 x 256 x 3 x 8 B = 1.2 MB does not
+    # 4 x 256 rows x 2 chunks x 8 B = 16 KB fits; 200 x 256 rows of vocab
+    # 262144 (4 chunks of 65536) x 8 B = 1.6 MB does not
     ok = jb.make_shape(4, 0, 0, 0, 256, 0, 151936)
-    too_big = jb.make_shape(200, 0, 0, 0, 256, 0, 151936)
+    too_big = jb.make_shape(200, 0, 0, 0, 256, 0, 262144)
     assert jb.jf_tree_verify_noalloc(A16, A16, A16, A16, A16, A16, None, too_big, 16, stream=0,
                                      check=False) == jb.JF_ERR_SHAPE
     assert jb.jf_tree_verify_noalloc(None, A16, A16, A16, A16, A16, None, ok, 16, stream=0,

@@ -27,8 +27,11 @@ constexpr int kMaxCtas = 256;     // cap on the persistent attention grid
 constexpr int kMinTilesPerCta = 2;   // smallest key range a CTA is given
 constexpr int kMaxBatch = 1024;   // sequences per jf_tree_attention call
 constexpr int kArgmaxThreads = 256;
-constexpr int kArgmaxVecs = 4;    // 16-byte loads in flight per thread
-constexpr int kArgmaxChunk = 51200;  // bf16 elements of one logits row per CTA (100 KB)
+constexpr int kArgmaxVecs = 8;    // 16-byte loads in flight per thread
+constexpr int kArgmaxCtasPerSm = 5;  // resident argmax CTAs per SM (at most 51 registers)
+constexpr int kArgmaxMaxChunk = 76800;  // target bf16 of one logits row per CTA (150 KB)
+constexpr int kArgmaxGranule = kArgmaxThreads * 8;  // chunks are whole vectors per thread
+constexpr int kSmCount = 152;     // SMs of the part the chunking is tuned for
 constexpr unsigned long long kTimeoutNs = 2000000000ull;        // 2 s per wait
 
 __host__ __device__ constexpr int ceil_div(int a, int b) { return (a + b - 1) / b; }
@@ -53,6 +56,7 @@ struct Layout {
     int32_t lgG, lgNB;   // log2 of G and NB (both powers of two)
     int32_t n_qtiles;    // work units: B * Hkv * QT
     int32_t max_pieces;  // partial slots: two per CTA (its first and its last item)
+    int32_t chunk;       // bf16 elements of a logits row per argmax CTA
     int32_t chunks;      // argmax chunks per logits row
     size_t qtab_off, ml_off, opart_off;
     size_t amp_off;
@@ -72,7 +76,20 @@ inline Layout make_layout(int B, int Nmax, int Hq, int Hkv, int D, int Pcap, int
     L.QT = ceil_div(Nmax, L.NB);
     L.n_qtiles = B * Hkv * L.QT;
     L.max_pieces = 2 * kMaxCtas;
-    L.chunks = V > 0 ? ceil_div(V, kArgmaxChunk) : 1;
+    // Argmax chunks: rows are cut into pieces of about kArgmaxMaxChunk; with
+    // few rows into more, so that the grid reaches ~4 CTAs per SM while it
+    // still fits one wave of kArgmaxCtasPerSm per SM.
+    int per_row = V > 0 ? ceil_div(V, kArgmaxMaxChunk) : 1;
+    const long long rows = (long long)B * Nmax;
+    if (V > 0 && rows > 0) {
+        const long long fill = (4LL * kSmCount + rows - 1) / rows;
+        const long long wave = (long long)kArgmaxCtasPerSm * kSmCount / rows;
+        const long long want = fill < wave ? fill : wave;
+        const long long most = ceil_div(V, kArgmaxGranule);
+        if (want > per_row) per_row = (int)(want < most ? want : most);
+    }
+    L.chunk = V > 0 ? (int)align_up((size_t)ceil_div(V, per_row), kArgmaxGranule) : kArgmaxGranule;
+    L.chunks = V > 0 ? ceil_div(V, L.chunk) : 1;
     size_t off = 0;
     auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 256); return o; };
     L.qtab_off = take(sizeof(QTile) * (size_t)L.n_qtiles);
@@ -144,7 +161,7 @@ __device__ __forceinline__ int cta_of_tile(int x, int qt, int rt, int C) {
 // range crosses into another unit (an extra epilogue and pipeline refill)
 // thus gets about alpha fewer real tiles. alpha = min(kSwitchTiles, half of
 // the real tiles per CTA), so that no range can hold virtual tiles only.
-constexpr int kSwitchTiles = 3;
+constexpr int kSwitchTiles = 4;
 
 struct PlanSeq {
     int n_ctas, alpha;

@@ -6,15 +6,17 @@
 // tokens[c] == argmax(logits[p]); the result is the deepest accepted node.
 //
 //  argmax_chunk_kernel  HBM-bound scan of the logits. Each CTA owns a chunk
-//                       of up to 51200 bf16 of one row (one wave of CTAs for
-//                       a 256 x 151936 batch at 6 CTAs per SM). Every thread
-//                       streams 128-bit loads, 4 in flight, and keeps a
+//                       of one row: about 76800 bf16 (two chunks per row of
+//                       151936, one wave of CTAs for 256 rows at 5 CTAs per
+//                       SM), or shorter chunks when there are few rows, so
+//                       that the grid still fills the SMs. Every thread
+//                       streams 128-bit loads, 8 in flight, and keeps a
 //                       running maximum over its vectors: a packed bf16x2
-//                       NaN-propagating max per
-//                       vector, plus the index of the first vector that
-//                       reached it. At the end it re-reads that one vector
-//                       for the exact first position. A block reduction on
-//                       (value, index) writes the chunk's result.
+//                       NaN-propagating max per vector, plus the index of
+//                       the first vector that reached it. At the end it
+//                       re-reads that one vector for the exact first
+//                       position. A block reduction on (value, index) writes
+//                       the chunk's result.
 //  accept_walk_kernel   one block per sequence, one thread per node: merges
 //                       the chunk results (ties -> lowest index, the first
 //                       NaN wins), checks each edge against the parent's
@@ -66,9 +68,9 @@ __device__ __forceinline__ bool ranks_before(float a, int ia, float b, int ib) {
     return ia < ib;
 }
 
-__global__ void __launch_bounds__(kArgmaxThreads, 6)
+__global__ void __launch_bounds__(kArgmaxThreads, kArgmaxCtasPerSm)
     argmax_chunk_kernel(const __nv_bfloat16 *__restrict__ logits, const int32_t *__restrict__ n_nodes,
-                        int2 *__restrict__ part, int Nmax, int V, int chunks) {
+                        int2 *__restrict__ part, int Nmax, int V, int chunk, int chunks) {
     const int row = blockIdx.y;
     const int b = row / Nmax, i = row - b * Nmax;
     const int n = n_nodes[b];
@@ -77,8 +79,8 @@ __global__ void __launch_bounds__(kArgmaxThreads, 6)
         return;
     }
     const int tid = threadIdx.x;
-    const int e0 = blockIdx.x * kArgmaxChunk;
-    const int nvec = (min(V, e0 + kArgmaxChunk) - e0) >> 3;  // V % 8 == 0
+    const int e0 = blockIdx.x * chunk;
+    const int nvec = (min(V, e0 + chunk) - e0) >> 3;         // V % 8 == 0
     const uint4 *src = reinterpret_cast<const uint4 *>(logits + (size_t)row * V + e0);
     float best = -__int_as_float(0x7f800000);
     int best_k = -1;
@@ -234,7 +236,7 @@ cudaError_t launch_argmax(const Layout &L, const __nv_bfloat16 *logits, const in
     trace_begin("argmax_chunk", s);
     dim3 grid(L.chunks, L.B * L.Nmax);
     argmax_chunk_kernel<<<grid, kArgmaxThreads, 0, s>>>(logits, n_nodes, reinterpret_cast<int2 *>(ws + L.amp_off),
-                                                        L.Nmax, L.V, L.chunks);
+                                                        L.Nmax, L.V, L.chunk, L.chunks);
     cudaError_t e = cudaGetLastError();
     trace_end(s);
     return e;
