@@ -224,6 +224,21 @@ def test_verify_ragged_and_malformed():
     assert status & 1
 
 
+def test_verify_chain_of_256_deep_paths():
+    """A 256-node chain: every edge agrees up to node 200, then one breaks;
+    paths deeper than max_depth are cut."""
+    N = 256
+    par = torch.tensor([[-1] + list(range(N - 1))], dtype=torch.int32)
+    inp = small_inputs(24, B=1, N=N, parents=par, vocab=16)
+    top = inp["logits"][0].float().argmax(-1)          # no ties: N(0,1) bf16 logits, 16 values a row
+    tok = torch.zeros(1, N, dtype=torch.int32)
+    for c in range(1, N):
+        tok[0, c] = top[c - 1] if c <= 200 else (top[c - 1] + 1) % 16
+    inp["tokens"] = tok
+    for md in (255, 200, 64, 0):
+        check_verify(inp, max_depth=md)
+
+
 def test_verify_random_trees_many_matches():
     """Small vocabulary so that many edges agree and long paths form."""
     for seed in range(3):

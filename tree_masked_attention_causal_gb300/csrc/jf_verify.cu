@@ -17,12 +17,15 @@
 //                       re-reads that one vector for the exact first
 //                       position. A block reduction on (value, index) writes
 //                       the chunk's result.
-//  accept_walk_kernel   one block per sequence, one thread per node: merges
-//                       the chunk results (ties -> lowest index, the first
-//                       NaN wins), checks each edge against the parent's
-//                       argmax, walks each node's root path, and reduces
-//                       (depth, -index) to the deepest accepted node.
-//                       Launched as a programmatic dependent of the scan.
+//  accept_walk_kernel   one block per sequence, one thread per node. While
+//                       the scan runs (programmatic launch) it validates the
+//                       tree and builds every node's ancestor set by pointer
+//                       jumping. After the scan: merges the chunk results
+//                       (ties -> lowest index, the first NaN wins), checks
+//                       each edge against the parent's argmax, accepts a
+//                       node iff all edges on its root path agree (bit
+//                       masks), and reduces (depth, -index) to the deepest
+//                       accepted node, whose ancestor set gives the path.
 #include "jf_common.cuh"
 
 namespace jf {
@@ -146,47 +149,121 @@ __global__ void __launch_bounds__(kArgmaxThreads, kArgmaxCtasPerSm)
     }
 }
 
+// (value, index) as one integer that orders like ranks_before: a NaN above
+// every number, then the larger value (+0 == -0), then the lower index.
+__device__ __forceinline__ unsigned long long rank_key(int2 x) {
+    uint32_t u = static_cast<uint32_t>(x.x);
+    uint32_t ord;
+    if (is_nan_f(__int_as_float(x.x))) {
+        ord = 0xFFFFFFFFu;
+    } else {
+        if (u == 0x80000000u) u = 0u;                      // -0 -> +0
+        ord = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    }
+    return (static_cast<unsigned long long>(ord) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(x.y));
+}
+
 __global__ void __launch_bounds__(kMaxNodes)
     accept_walk_kernel(const int2 *__restrict__ part, const int32_t *__restrict__ tokens,
                        const int32_t *__restrict__ parents, const int32_t *__restrict__ n_nodes,
                        int32_t *__restrict__ accept_len, int32_t *__restrict__ accept_path,
                        int32_t *__restrict__ argmax_out, int Nmax, int chunks, int max_depth,
                        int32_t *status) {
-    __shared__ int par[kMaxNodes];
+    constexpr int W = kMaxNodes / 32;                       // words of a node mask
+    __shared__ uint32_t anc[kMaxNodes][W];                  // node i and its ancestors
+    __shared__ int jump[kMaxNodes];
     __shared__ int am[kMaxNodes];
-    __shared__ unsigned char edge_ok[kMaxNodes];
-    __shared__ int red[kMaxNodes / 32];
+    __shared__ unsigned long long best_key[kMaxNodes];      // merged chunk results
+    __shared__ uint32_t ok_bits[W];                         // nodes whose edge to the parent agrees
+    __shared__ int red[W];
     pdl_launch_dependents();        // whatever follows may start its prologue
     const int b = blockIdx.x, i = threadIdx.x;
-    // inputs that the scan does not write: read them before waiting on it
+    // Everything that depends on the tree alone is done before waiting for
+    // the scan: validation, and every node's ancestor set and depth.
     const int n = n_nodes[b];
     const bool n_ok = n >= 1 && n <= Nmax;
+    const bool real = n_ok && i < n;
     int p = -1, tok = 0;
-    if (n_ok && i < n) {
+    if (real) {
         p = parents[(size_t)b * Nmax + i];
         tok = tokens[(size_t)b * Nmax + i];
     }
+    bool bad = !n_ok;
+    if (real) bad = (i == 0) ? (p != -1) : (p < 0 || p >= i);
+    best_key[i] = 0ull;
+    bad = __syncthreads_or(bad);
+    uint32_t m[W];
+    int depth = 0;
+    if (!bad) {
+        // Pointer jumping: after round k, m holds the nodes on the path from
+        // i up to (not including) its 2^k-th ancestor jump[i]; 8 rounds
+        // cover any depth below 256.
+#pragma unroll
+        for (int w = 0; w < W; ++w) m[w] = (real && (i >> 5) == w) ? (1u << (i & 31)) : 0u;
+        int up = real ? p : -1;
+#pragma unroll
+        for (int w = 0; w < W; ++w) anc[i][w] = m[w];
+        jump[i] = up;
+        __syncthreads();
+#pragma unroll 1
+        for (int round = 0; round < 8; ++round) {
+            int up2 = -1;
+            if (up >= 0) {
+#pragma unroll
+                for (int w = 0; w < W; ++w) m[w] |= anc[up][w];
+                up2 = jump[up];
+            }
+            const bool more = __syncthreads_or(up2 >= 0);
+#pragma unroll
+            for (int w = 0; w < W; ++w) anc[i][w] = m[w];
+            jump[i] = up2;
+            up = up2;
+            __syncthreads();
+            if (!more) break;
+        }
+#pragma unroll
+        for (int w = 0; w < W; ++w) depth += __popc(m[w]);
+        depth -= 1;                                        // the node itself
+    }
     pdl_wait_prior_grid();
-    // merge the chunk results (all loads independent)
-    int a = -1;
-    if (n_ok && i < n) {
-        const int2 *pr = part + ((size_t)b * Nmax + i) * chunks;
-        float best = __int_as_float(pr[0].x);
-        a = pr[0].y;
-        for (int c = 1; c < chunks; ++c) {
-            const int2 x = __ldcg(pr + c);
-            if (ranks_before(__int_as_float(x.x), x.y, best, a)) {
-                best = __int_as_float(x.x);
-                a = x.y;
+    // Merge the chunk results. Up to 4 chunks per row: each node's thread
+    // loads its entries together and keeps the best. More: the block's
+    // threads share the sequence's n * chunks entries (node-major), four
+    // loads in flight each, and keep the best per node with a shared-memory
+    // atomic max on rank_key.
+    unsigned long long mine = 0ull;
+    if (chunks <= 4) {
+        if (real) {
+            const int2 *pr = part + ((size_t)b * Nmax + i) * chunks;
+            int2 x[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                if (c < chunks) x[c] = __ldcg(pr + c);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const unsigned long long k = c < chunks ? rank_key(x[c]) : 0ull;
+                mine = k > mine ? k : mine;
             }
         }
+    } else {
+        const int total = n_ok ? n * chunks : 0;
+        const int2 *pb = part + (size_t)b * Nmax * chunks;
+        for (int e0 = i; e0 < total; e0 += 4 * kMaxNodes) {
+            int2 x[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (e0 + u * kMaxNodes < total) x[u] = __ldcg(pb + e0 + u * kMaxNodes);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int e = e0 + u * kMaxNodes;
+                if (e < total) atomicMax(&best_key[e / chunks], rank_key(x[u]));
+            }
+        }
+        __syncthreads();
+        mine = best_key[i];
     }
-    am[i] = a;
+    const int a = real ? static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(mine)) : -1;
     if (argmax_out && i < Nmax) argmax_out[(size_t)b * Nmax + i] = a;
-    bool bad = !n_ok;
-    if (n_ok && i < n) bad = (i == 0) ? (p != -1) : (p < 0 || p >= i);
-    par[i] = p;
-    bad = __syncthreads_or(bad);
     int32_t *path = accept_path + (size_t)b * (max_depth + 1);
     if (bad) {
         for (int k = i; k <= max_depth; k += blockDim.x) path[k] = -1;
@@ -196,37 +273,31 @@ __global__ void __launch_bounds__(kMaxNodes)
         }
         return;
     }
-    edge_ok[i] = (i < n) && (i == 0 || tok == am[p]);
+    am[i] = a;
     __syncthreads();
-    // accepted iff every edge on the root path agrees
-    int key = -1;
-    if (i < n) {
-        bool acc = true;
-        int depth = 0;
-        for (int j = i; j > 0; j = par[j]) {
-            acc = acc && edge_ok[j];
-            ++depth;
-        }
-        if (acc) key = (depth << 16) | (0xFFFF - i);          // deepest, then lowest index
-    }
+    // edge (p, i) agrees with the target; the root always does
+    const bool edge = real && (i == 0 || tok == am[p]);
+    const unsigned e = __ballot_sync(0xffffffffu, edge);
+    if ((i & 31) == 0) ok_bits[i >> 5] = e;
+    __syncthreads();
+    // accepted iff every node on the root path (itself included) agrees
+    bool acc = real;
+#pragma unroll
+    for (int w = 0; w < W; ++w) acc = acc && (m[w] & ~ok_bits[w]) == 0u;
+    int key = acc ? (depth << 16) | (0xFFFF - i) : -1;      // deepest, then lowest index
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) key = max(key, __shfl_xor_sync(0xffffffffu, key, o));
     if ((i & 31) == 0) red[i >> 5] = key;
     __syncthreads();
-    if (i == 0) {
-        int k = red[0];
-        for (int w = 1; w < (int)(blockDim.x >> 5); ++w) k = max(k, red[w]);
-        const int best = 0xFFFF - (k & 0xFFFF);
-        const int depth = k >> 16;
-        const int len = min(depth, max_depth) + 1;
-        for (int s = len; s <= max_depth; ++s) path[s] = -1;
-        int node = best;
-        for (int d = depth; d >= 0; --d) {
-            if (d < len) path[d] = node;
-            node = par[node];
-        }
-        accept_len[b] = len;
-    }
+    int k = red[0];
+#pragma unroll
+    for (int w = 1; w < W; ++w) k = max(k, red[w]);
+    const int best = 0xFFFF - (k & 0xFFFF);                 // the root is always accepted
+    const int len = min(k >> 16, max_depth) + 1;
+    // the path: the nodes of best's root path at depth < len, in depth order
+    if (real && ((anc[best][i >> 5] >> (i & 31)) & 1u) && depth < len) path[depth] = i;
+    for (int t = len + i; t <= max_depth; t += blockDim.x) path[t] = -1;
+    if (i == 0) accept_len[b] = len;
 }
 
 }  // namespace
