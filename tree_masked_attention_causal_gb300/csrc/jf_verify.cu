@@ -12,11 +12,12 @@
 //                       that the grid still fills the SMs. Every thread
 //                       streams 128-bit loads, 8 in flight, and keeps a
 //                       running maximum over its vectors: a packed bf16x2
-//                       NaN-propagating max per vector, plus the index of
-//                       the first vector that reached it. At the end it
-//                       re-reads that one vector for the exact first
-//                       position. A block reduction on (value, index) writes
-//                       the chunk's result.
+//                       NaN-propagating max per vector, plus the first
+//                       vector that reached it (its index and its 8
+//                       values, kept in registers). At the end it finds the
+//                       exact first position in that vector. A block
+//                       reduction on (value, index) writes the chunk's
+//                       result.
 //  accept_walk_kernel   one block per sequence, one thread per node. While
 //                       the scan runs (programmatic launch) it validates the
 //                       tree and builds every node's ancestor set by pointer
@@ -87,6 +88,7 @@ __global__ void __launch_bounds__(kArgmaxThreads, kArgmaxCtasPerSm)
     const uint4 *src = reinterpret_cast<const uint4 *>(logits + (size_t)row * V + e0);
     float best = -__int_as_float(0x7f800000);
     int best_k = -1;
+    uint4 best_v = make_uint4(0u, 0u, 0u, 0u);              // the vector that holds it
     for (int k0 = tid; k0 < nvec; k0 += kArgmaxThreads * kArgmaxVecs) {
         uint4 v[kArgmaxVecs];
 #pragma unroll
@@ -104,6 +106,7 @@ __global__ void __launch_bounds__(kArgmaxThreads, kArgmaxCtasPerSm)
                 if (best_k < 0 || m > best || (is_nan_f(m) && !is_nan_f(best))) {
                     best = m;
                     best_k = k;
+                    best_v = v[u];
                 }
             }
         }
@@ -112,8 +115,7 @@ __global__ void __launch_bounds__(kArgmaxThreads, kArgmaxCtasPerSm)
     // first element of the winning vector that equals the maximum
     int idx = 0x7FFFFFFF;
     if (best_k >= 0) {
-        const uint4 v = src[best_k];
-        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+        const uint32_t w4[4] = {best_v.x, best_v.y, best_v.z, best_v.w};
         const bool want_nan = is_nan_f(best);
 #pragma unroll
         for (int q = 7; q >= 0; --q) {
