@@ -44,6 +44,32 @@ def test_workspace_bytes(lib):
     assert lib.jf_workspace_bytes(None) == 0
 
 
+def _argmax_chunks(rows, V):
+    """Chunks per logits row, as include/jf_tree.h and the layout state it:
+    pieces of about 76800 elements, more of them for few rows (up to ~4
+    CTAs per SM of 152, within one wave of 5 per SM), multiples of 2048."""
+    cdiv = lambda a, b: -(-a // b)
+    per = cdiv(V, 76800)
+    want = min(cdiv(4 * 152, rows), 5 * 152 // rows)
+    if want > per:
+        per = min(want, cdiv(V, 2048))
+    chunk = cdiv(cdiv(V, per), 2048) * 2048
+    return cdiv(V, chunk)
+
+
+@pytest.mark.parametrize("B,N,V,expect", [(1, 256, 151936, 2), (1, 16, 151936, 38), (16, 64, 151936, 2),
+                                          (2, 5, 151936, 38), (1, 16, 1024, 1), (4, 200, 262144, 4),
+                                          (1, 152, 151936, 4)])
+def test_argmax_chunk_rule(lib, B, N, V, expect):
+    """The verify region of the workspace holds one int2 per (row, chunk):
+    its growth from a one-chunk vocabulary pins the chunk count."""
+    assert _argmax_chunks(B * N, V) == expect
+    align = lambda x: -(-x // 256) * 256
+    base = jb.jf_workspace_bytes(jb.make_shape(B, 0, 0, 0, N, 0, 8))
+    ws = jb.jf_workspace_bytes(jb.make_shape(B, 0, 0, 0, N, 0, V))
+    assert ws - base == align(B * N * expect * 8) - align(B * N * 8)
+
+
 A16 = 1 << 20            # fake 16-byte-aligned addresses: never dereferenced
 
 
