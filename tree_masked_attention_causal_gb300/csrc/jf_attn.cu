@@ -48,15 +48,19 @@
 //  * Softmax per tile (one warp per row quadrant): one 128-column TMEM load
 //    for the row max, the running max handed over from the previous tile's
 //    owner, then ex2 on the MUFU pipe, bf16 packing and the P store in a
-//    rolled loop over 32-column chunks read again from TMEM. The kernel is
-//    instruction-fetch bound, so the hot loop is kept small.
+//    rolled loop over 32-column chunks read again from TMEM; the scaling
+//    and the row sums use packed f32x2 arithmetic. Instruction fetch is a
+//    first-order cost for this kernel, so the hot loop is kept small.
 //  * Online softmax in the exp2 domain, lazy rescale: O is rescaled only
 //    when a row max grows by more than 2^8, by the owner of that tile, once
 //    the previous tile's PV has completed. The first PV of an item waits
 //    until every softmax warp has read the previous item's O.
-//  * Nothing runs before it: its first TMA loads start at launch.
-//    Tree validation and the NaN rows of malformed sequences are left to the
-//    combine kernel, which overwrites whatever this kernel wrote for them.
+//  * Launched as a programmatic dependent of the previous kernel: barrier
+//    set-up, the TMEM allocation and the tensor-map prefetches run before
+//    the wait, every input read after it. No kernel of its own runs before
+//    it. Tree validation and the NaN rows of malformed sequences are left
+//    to the combine kernel, which overwrites whatever this kernel wrote for
+//    them.
 //  * Rows of padding nodes are computed but never stored. V rows past the
 //    prefix length or past n_nodes are zeroed in shared memory before the
 //    PV MMA, so NaN in unused cache rows cannot reach an output.
