@@ -775,6 +775,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort = 0;
         fence_mbar_init();
     }
+    if (warp == kProducerWarp) {
+        // The plan's first loads after the wait: start them towards L2 now.
+        const int lane = threadIdx.x & 31;
+        if (32 * lane < L.B) {
+            prefetch_l2(a.prefix_lens + 32 * lane);
+            prefetch_l2(a.n_nodes + 32 * lane);
+        }
+    }
     if (warp == kProducerWarp && (threadIdx.x & 31) == 0) {
         tma_prefetch_map(&maps.q);
         tma_prefetch_map(&maps.k_cache);
