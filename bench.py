@@ -54,6 +54,18 @@ def peaks():
     return FALLBACK_PEAKS, "fallback"
 
 
+def max_over_ranks(values, world: int, device):
+    """Element-wise maximum of the floats `values` over all ranks (the values
+    themselves on one rank): every timing is the slowest rank's."""
+    if world <= 1:
+        return [float(v) for v in values]
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -327,14 +339,9 @@ def run_gpu(args, rank, world, local):
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
-    total_ms = start.elapsed_time(end)
-    attn_call_ms = a0.elapsed_time(a1) / K
-    verify_call_ms = v0.elapsed_time(v1) / K
     clocks = clk.summary()
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms, attn_call_ms, verify_call_ms = max_over_ranks(
+        [start.elapsed_time(end), a0.elapsed_time(a1) / K, v0.elapsed_time(v1) / K], world, dev)
 
     # per-kernel durations of the traced replay: each includes its launch
     # gap after the previous event, without programmatic overlap
@@ -370,11 +377,7 @@ def run_gpu(args, rank, world, local):
         e2e_step()
     e1.record()
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks([e0.elapsed_time(e1)], world, dev)[0]
     assert int(h_alen[0]) == int(inp["planted_len"][0])
 
     flops = synth.attention_flops(inp["parents"], inp["n_nodes"], inp["prefix_lens"], Hq, d)
