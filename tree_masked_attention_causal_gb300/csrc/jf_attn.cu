@@ -76,8 +76,8 @@ struct ItemInfo {
 template <int D>
 struct AttnCfg {
     static constexpr int NQ = 2;                            // Q buffers: the next unit's Q loads early
-    static constexpr int NK = D == 128 ? 2 : 4;             // K ring stages (released right after QK^T)
-    static constexpr int NV = D == 128 ? 3 : 6;             // V ring stages
+    static constexpr int NK = D == 128 ? 3 : 4;             // K ring stages (released right after QK^T)
+    static constexpr int NV = D == 128 ? 2 : 6;             // V ring stages
     static constexpr int NS = 3;                            // S/P buffers in TMEM
     static constexpr int kBoxes = D / 64;                   // 64-column (128-byte) swizzled boxes
     static constexpr uint32_t kQBoxBytes = kRows * 128;     // one box: 128 rows x 128 B
