@@ -19,8 +19,10 @@ time of K back-to-back jf_tree_attention calls (tree_attention and
 split_combine kernels) and of K jf_tree_verify calls (argmax_chunk and
 accept_walk), timed the same way in the same clock window. Events the
 library records around each kernel, in a traced copy of the step graph,
-give per-kernel figures that include each launch gap. e2e times the public calls eagerly on inputs in pinned host
-memory: each step copies them to the device and reads the results back.
+give per-kernel figures that include each launch gap. e2e times the
+public calls eagerly on inputs in pinned host memory: each step's inputs
+are copied to the device (on a second stream, into the other of two input
+sets, while the previous step computes) and its results read back.
 `--impl reference` times the fp64 CPU oracle on the host cores.
 """
 
@@ -350,31 +352,53 @@ def run_gpu(args, rank, world, local):
         per.setdefault(name, []).append(events[2 * k].elapsed_time(events[2 * k + 1]))
     avg = {n: statistics.mean(v) for n, v in per.items()}
 
-    # e2e through the public calls: pinned host inputs, H2D every step, D2H results
+    # e2e through the public calls: pinned host inputs, an H2D copy of every
+    # step's inputs and a D2H read of every step's results. The copy of step
+    # i + 1's inputs runs on a second stream, into the other of two device
+    # input sets, while step i computes.
     host = {k: inp[k].pin_memory() for k in names}
-    dev_in = {k: torch.empty_like(copies[0][k]) for k in names}
+    dev_in = [{k: torch.empty_like(copies[0][k]) for k in names} for _ in range(2)]
     h_alen = torch.empty(B, dtype=torch.int32).pin_memory()
     h_path = torch.empty(B, MAX_DEPTH + 1, dtype=torch.int32).pin_memory()
     h_am = torch.empty(B, N, dtype=torch.int32).pin_memory()
     K_e2e = max(3, min(K, 50))
+    compute = torch.cuda.current_stream()
+    copy_stream = torch.cuda.Stream()
+    copied = [torch.cuda.Event() for _ in range(2)]
+    consumed = [torch.cuda.Event() for _ in range(2)]
 
-    def e2e_step():
-        for k in names:
-            dev_in[k].copy_(host[k], non_blocking=True)
-        step(dev_in)
+    def copy_in(i):
+        j = i % 2
+        with torch.cuda.stream(copy_stream):
+            copy_stream.wait_event(consumed[j])          # step i - 2 is done with set j
+            for k in names:
+                dev_in[j][k].copy_(host[k], non_blocking=True)
+            copied[j].record(copy_stream)
+
+    def run(i):
+        j = i % 2
+        compute.wait_event(copied[j])
+        step(dev_in[j])
+        consumed[j].record(compute)
         h_alen.copy_(alen, non_blocking=True)
         h_path.copy_(path, non_blocking=True)
         h_am.copy_(am, non_blocking=True)
 
-    for _ in range(2):
-        e2e_step()
+    def e2e_steps(n):
+        copy_stream.wait_stream(compute)
+        copy_in(0)
+        for i in range(n):
+            if i + 1 < n:
+                copy_in(i + 1)
+            run(i)
+
+    e2e_steps(2)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
-    for _ in range(K_e2e):
-        e2e_step()
+    e2e_steps(K_e2e)
     e1.record()
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks([e0.elapsed_time(e1)], world, dev)[0]
