@@ -36,10 +36,10 @@
 //      warp 11    TMA producer of the NV-stage V ring
 //      warp 9     QK^T issuer and TMEM owner: S(g) = Q K(g)^T into S buffer g % 3
 //      warp 10    PV issuer: O += P(g) V(g)
-//    One warp issuing 128x128x16 tcgen05 MMAs (elected lane, warp-uniform
-//    operands) manages one per ~87 cycles, about 3/4 of the tensor core's
-//    rate at N = 128. Two issuing warps with independent accumulators run
-//    concurrently, and the tensor core overlaps them.
+//    MMAs are issued by a whole converged warp (elected lane, warp-uniform
+//    operands); unrolled back to back, one warp keeps the tensor core at its
+//    full rate. The two issuers run concurrently on independent
+//    accumulators.
 //    TMEM: S buffers at columns 0, 128, 256; O at [384, 384+d). P is written
 //    back as bf16 over the first 64 columns of its own S. The three S buffers
 //    are a ring between the two issuers: QK^T may run two tiles ahead of the
