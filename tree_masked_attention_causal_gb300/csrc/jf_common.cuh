@@ -528,11 +528,6 @@ __device__ __forceinline__ void pdl_wait_prior_grid() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
-// Named barrier over the first `count` threads of the CTA.
-__device__ __forceinline__ void named_barrier(uint32_t id, uint32_t count) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-
 __device__ __forceinline__ float max3f(float a, float b, float c) {
     float r;
     asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
