@@ -557,6 +557,11 @@ __device__ __forceinline__ void softmax_loop(const AttnMaps &maps, const Layout 
             const int lim = (!tree && t == info.t_pre - 1) ? info.P - t * kBN : kBN;
             const int sb = g % C::NS;
             const uint32_t t_s = t_row + sb * 128;
+            // The running max so far, published by the previous tile's owner
+            // long before this tile's S is ready: taken before waiting for S,
+            // so that it is off the tile's critical path.
+            float m_prev = kNegInf;
+            if (j > 0 && !receive(g - 1, m_prev)) { fail = true; break; }
             if (!mbar_wait(bar(C::B_S_FULL + sb), (g / C::NS) & 1, abort, a.status)) { fail = true; break; }
             tc_fence_after();
             float mt;
@@ -571,10 +576,9 @@ __device__ __forceinline__ void softmax_loop(const AttnMaps &maps, const Layout 
                 }
                 mt = max128(sv) * sl2;
             }
-            float m_new = mt, m_prev = kNegInf;
+            float m_new = mt;
             bool need = false;
             if (j > 0) {
-                if (!receive(g - 1, m_prev)) { fail = true; break; }
                 m_new = fmaxf(m_prev, mt);
                 need = m_new > m_prev + 8.0f;              // lazy: O keeps m_prev unless it grows > 2^8
                 if (!need) m_new = m_prev;
