@@ -380,8 +380,10 @@ __device__ __forceinline__ void pv_loop(const AttnArgs &a, uint8_t *smem, uint32
         const int nt = info.te - info.tb;
         for (int j = 0; j < nt; ++j, ++vc, ++g) {
             const int vs = vc % C::NV, sb = g % C::NS;
-            if (!mbar_wait(bar(C::B_P_FULL + sb), (g / C::NS) & 1, abort, a.status)) return;
+            // V has long landed when P is ready: wait for it first, so that
+            // the PV goes out the moment the softmax hands P over.
             if (!mbar_wait(bar(C::B_V_FULL + vs), (vc / C::NV) & 1, abort, a.status)) return;
+            if (!mbar_wait(bar(C::B_P_FULL + sb), (g / C::NS) & 1, abort, a.status)) return;
             // V rows past the prefix length / past n_nodes: zero them so that
             // whatever the caller's memory holds there cannot reach O via 0 * NaN.
             const int t = info.tb + j;
