@@ -49,9 +49,9 @@ def is_stale() -> bool:
     return any(os.path.getmtime(p) > t for p in _deps())
 
 
-def _compile(src: str, verbose: bool) -> str:
-    obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
-    cmd = [nvcc(), *ARCH, *NVCC_FLAGS, "-c", src, "-o", obj]
+def _compile(src: str, verbose: bool, build_dir: str = BUILD, defines=()) -> str:
+    obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
+    cmd = [nvcc(), *ARCH, *NVCC_FLAGS, *[f"-D{d}" for d in defines], "-c", src, "-o", obj]
     if verbose:
         cmd += ["-Xptxas", "-v"]
     r = subprocess.run(cmd, capture_output=True, text=True)
@@ -66,18 +66,32 @@ def build(force: bool = False, verbose: bool = False) -> str:
     """Compile every csrc/*.cu for sm_103a and link libjf_tree.so (in-tree)."""
     if not force and not is_stale():
         return LIB
-    os.makedirs(BUILD, exist_ok=True)
+    return _link(LIB, BUILD, (), verbose)
+
+
+def build_variant(tag: str, defines) -> str:
+    """A second build of the library with extra preprocessor definitions,
+    libjf_tree_<tag>.so beside the main one (tests use it, e.g. the build
+    whose first K load never arrives, to exercise the bounded waits)."""
+    lib = os.path.join(PKG, f"libjf_tree_{tag}.so")
+    if os.path.exists(lib) and all(os.path.getmtime(p) <= os.path.getmtime(lib) for p in _deps()):
+        return lib
+    return _link(lib, os.path.join(PKG, f"_build_{tag}"), tuple(defines), False)
+
+
+def _link(lib: str, build_dir: str, defines, verbose: bool) -> str:
+    os.makedirs(build_dir, exist_ok=True)
     srcs = _sources()
     with cf.ThreadPoolExecutor(max_workers=len(srcs)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, verbose), srcs))
-    tmp = LIB + f".tmp{os.getpid()}"
+        objs = list(ex.map(lambda s: _compile(s, verbose, build_dir, defines), srcs))
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [nvcc(), *ARCH, "-shared", "-Xcompiler", "-fPIC", "-o", tmp, *objs,
            "-cudart", "static", "-ldl", "-lpthread", "-lrt"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -37,14 +37,24 @@ class JfError(RuntimeError):
 _lib = None
 
 
+def open_library(path: str) -> ctypes.CDLL:
+    """Open a build of the library at `path` with the argument types of
+    include/jf_tree.h set (load() uses this for the package's own build)."""
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with tree_masked_attention_causal_gb300._build.build()")
+    return _configure(ctypes.CDLL(path))
+
+
 def load() -> ctypes.CDLL:
     """Load libjf_tree.so from the package directory (built by _build.build())."""
     global _lib
     if _lib is None:
-        if not os.path.exists(LIB_PATH):
-            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
-                               "tree_masked_attention_causal_gb300._build.build()")
-        lib = ctypes.CDLL(LIB_PATH)
+        _lib = open_library(LIB_PATH)
+    return _lib
+
+
+def _configure(lib: ctypes.CDLL) -> ctypes.CDLL:
+    if True:
         P, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
         sp = ctypes.POINTER(JfShape)
         lib.jf_workspace_bytes.argtypes = [sp]
@@ -63,8 +73,9 @@ def load() -> ctypes.CDLL:
         lib.jf_trace_count.restype = i32
         lib.jf_trace_name.argtypes = [i32]
         lib.jf_trace_name.restype = ctypes.c_char_p
-        _lib = lib
-    return _lib
+        lib.jf_tree_verify_noalloc.argtypes = [P, P, P, P, P, P, P, sp, i32, P, P]
+        lib.jf_tree_verify_noalloc.restype = i32
+    return lib
 
 
 def header_symbols() -> List[str]:
@@ -104,11 +115,12 @@ def jf_status_string(code: int) -> str:
 
 def jf_tree_attention(q, k_cache, v_cache, prefix_lens, tree_k, tree_v, parents, n_nodes, out,
                       shape: JfShape, workspace, workspace_bytes: Optional[int] = None, status=None,
-                      stream=None, check: bool = True) -> int:
-    """Tree-causal attention over every node of every tree (see jf_tree.h)."""
+                      stream=None, check: bool = True, lib: Optional[ctypes.CDLL] = None) -> int:
+    """Tree-causal attention over every node of every tree (see jf_tree.h).
+    `lib` selects another build of the library (default: the package's)."""
     if workspace_bytes is None:
         workspace_bytes = workspace.numel() * workspace.element_size()
-    rc = load().jf_tree_attention(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(prefix_lens), _ptr(tree_k),
+    rc = (lib or load()).jf_tree_attention(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(prefix_lens), _ptr(tree_k),
                                   _ptr(tree_v), _ptr(parents), _ptr(n_nodes), _ptr(out), ctypes.byref(shape),
                                   _ptr(workspace), int(workspace_bytes), _ptr(status), _stream(stream))
     if check and rc != JF_OK:
@@ -173,10 +185,6 @@ def jf_tree_verify_noalloc(logits, tree_tokens, parents, n_nodes, accept_len_out
     device memory: the scratch is a fixed array inside the library (see
     jf_tree.h for its size limit and for when calls race)."""
     fn = load().jf_tree_verify_noalloc
-    if fn.argtypes is None:
-        P = ctypes.c_void_p
-        fn.argtypes = [P, P, P, P, P, P, P, ctypes.POINTER(JfShape), ctypes.c_int32, P, P]
-        fn.restype = ctypes.c_int32
     rc = fn(_ptr(logits), _ptr(tree_tokens), _ptr(parents), _ptr(n_nodes), _ptr(accept_len_out),
             _ptr(accept_path_out), _ptr(argmax_out), ctypes.byref(shape), int(max_depth), _ptr(status),
             _stream(stream))

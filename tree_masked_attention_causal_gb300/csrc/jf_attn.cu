@@ -91,7 +91,7 @@ struct AttnCfg {
                          B_V_FULL = B_K_EMPTY + NK, B_V_EMPTY = B_V_FULL + NV, B_S_FULL = B_V_EMPTY + NV,
                          B_S_FREE = B_S_FULL + NS, B_P_FULL = B_S_FREE + NS, B_O_FREE = B_P_FULL + NS,
                          B_ITEM_FULL = B_O_FREE + 1, B_ITEM_EMPTY = B_ITEM_FULL + 2, B_PAIR = B_ITEM_EMPTY + 2,
-                         B_HAND = B_PAIR + 4, B_EPI = B_HAND + 8, N_BARS = B_EPI + 1;
+                         B_HAND = B_PAIR + 4, B_EPI = B_HAND + 8, B_DRAIN = B_EPI + 1, N_BARS = B_DRAIN + 2;
     static constexpr uint32_t item_off = bar_off + ((N_BARS * 8 + 15) / 16) * 16;
     static constexpr uint32_t hand_off = item_off + 2 * sizeof(ItemInfo);   // float [4 quadrants][2 slots][32]
     static constexpr uint32_t xchg_off = hand_off + 4 * 2 * 32 * sizeof(float);   // float [2 warps][128 rows]
@@ -160,10 +160,18 @@ __device__ __forceinline__ void producer_loop(const AttnMaps &maps, const Layout
     int ic = 0, qc = 0, kc = 0;
     bool ok = true;
     // K tile t of the current item into the next ring stage.
+    int skipped = -1;                   // a load left out on purpose (stall-test build only)
     auto issue_k = [&](const ItemInfo &info, int t) -> bool {
         const bool tree = t >= info.t_pre;
         const int ks = kc % C::NK;
         if (!mbar_wait(bar(C::B_K_EMPTY + ks), ((kc / C::NK) & 1) ^ 1, abort, a.status)) return false;
+#ifdef JF_STALL_TEST
+        if (kc == 0) {                  // never arrives: the first QK^T waits until its limit
+            skipped = 0;
+            ++kc;
+            return true;
+        }
+#endif
         if (lane == 0) {
             mbar_arrive_expect_tx(bar(C::B_K_FULL + ks), C::kTileBytes);
             for (int dc = 0; dc < C::kBoxes; ++dc) {
@@ -258,8 +266,10 @@ __device__ __forceinline__ void producer_loop(const AttnMaps &maps, const Layout
         // Let every copy this warp started land before the CTA can exit.
         for (int s = 0; s < C::NQ; ++s)
             if (qc > s) mbar_wait_drain(bar(C::B_Q_FULL + s), (((qc - 1 - s) / C::NQ)) & 1);
-        for (int s = 0; s < C::NK; ++s)
-            if (kc > s) mbar_wait_drain(bar(C::B_K_FULL + s), (((kc - 1 - s) / C::NK)) & 1);
+        for (int s = 0; s < C::NK; ++s) {
+            const int k = (kc - 1) - ((kc - 1 - s) % C::NK + C::NK) % C::NK;   // last load into stage (k % NK == s)
+            if (kc > s && k != skipped) mbar_wait_drain(bar(C::B_K_FULL + s), (k / C::NK) & 1);
+        }
     }
 }
 
@@ -334,17 +344,21 @@ __device__ __forceinline__ void qk_loop(const AttnArgs &a, uint32_t sbase, uint3
     const uint64_t k_desc = sdesc_sw128(sbase + C::k_off, 16, 1024);
     int ic = 0, qc = 0, kc = 0, g = 0;
     ItemInfo info;
-    while (next_item<D>(bars, items_s, ic, info, abort, a.status)) {
+    bool ok = true;
+    while (ok && next_item<D>(bars, items_s, ic, info, abort, a.status)) {
         const int slot = (ic - 1) & 1;
         const int qb = qc % C::NQ;
-        if (!mbar_wait(bar(C::B_Q_FULL + qb), (qc / C::NQ) & 1, abort, a.status)) return;
+        if (!mbar_wait(bar(C::B_Q_FULL + qb), (qc / C::NQ) & 1, abort, a.status)) break;
         ++qc;
         const uint64_t qd = q_desc + ((qb * C::kQBytes) >> 4);
         const int nt = info.te - info.tb;
         for (int j = 0; j < nt; ++j, ++kc, ++g) {
             const int ks = kc % C::NK, sb = g % C::NS;
-            if (!mbar_wait(bar(C::B_K_FULL + ks), (kc / C::NK) & 1, abort, a.status)) return;
-            if (!mbar_wait(bar(C::B_S_FREE + sb), ((g / C::NS) & 1) ^ 1, abort, a.status)) return;
+            if (!mbar_wait(bar(C::B_K_FULL + ks), (kc / C::NK) & 1, abort, a.status) ||
+                !mbar_wait(bar(C::B_S_FREE + sb), ((g / C::NS) & 1) ^ 1, abort, a.status)) {
+                ok = false;
+                break;
+            }
             tc_fence_after();
             __syncwarp();
             const uint64_t b0 = k_desc + ((ks * C::kTileBytes) >> 4);
@@ -355,8 +369,13 @@ __device__ __forceinline__ void qk_loop(const AttnArgs &a, uint32_t sbase, uint3
             mma_commit(bar(C::B_S_FULL + sb));
             mma_commit(bar(C::B_K_EMPTY + ks));
         }
-        if (lane == 0) mbar_arrive(bar(C::B_ITEM_EMPTY + slot));
+        if (ok && lane == 0) mbar_arrive(bar(C::B_ITEM_EMPTY + slot));
     }
+    // Every MMA this warp issued has completed before the CTA can free TMEM
+    // or exit, on every path (an abort included).
+    mma_commit(bar(C::B_DRAIN + 0));
+    if (lane == 0) mbar_wait_drain(bar(C::B_DRAIN + 0), 0);
+    __syncwarp();
 }
 
 // PV issuer: O (+)= P(g) V(g); a buffer's S/P slot returns to the QK issuer
@@ -371,19 +390,23 @@ __device__ __forceinline__ void pv_loop(const AttnArgs &a, uint8_t *smem, uint32
     const uint64_t v_desc = sdesc_sw128(sbase + C::v_off, kBN * 128, 1024);
     int ic = 0, vc = 0, g = 0, items = 0;
     ItemInfo info;
-    while (next_item<D>(bars, items_s, ic, info, abort, a.status)) {
+    bool ok = true;
+    while (ok && next_item<D>(bars, items_s, ic, info, abort, a.status)) {
         const int slot = (ic - 1) & 1;
         // The first PV of an item overwrites O: every softmax warp must have
         // read the previous item's O first.
-        if (items > 0 && !mbar_wait(bar(C::B_O_FREE), (items - 1) & 1, abort, a.status)) return;
+        if (items > 0 && !mbar_wait(bar(C::B_O_FREE), (items - 1) & 1, abort, a.status)) break;
         ++items;
         const int nt = info.te - info.tb;
         for (int j = 0; j < nt; ++j, ++vc, ++g) {
             const int vs = vc % C::NV, sb = g % C::NS;
             // V has long landed when P is ready: wait for it first, so that
             // the PV goes out the moment the softmax hands P over.
-            if (!mbar_wait(bar(C::B_V_FULL + vs), (vc / C::NV) & 1, abort, a.status)) return;
-            if (!mbar_wait(bar(C::B_P_FULL + sb), (g / C::NS) & 1, abort, a.status)) return;
+            if (!mbar_wait(bar(C::B_V_FULL + vs), (vc / C::NV) & 1, abort, a.status) ||
+                !mbar_wait(bar(C::B_P_FULL + sb), (g / C::NS) & 1, abort, a.status)) {
+                ok = false;
+                break;
+            }
             // V rows past the prefix length / past n_nodes: zero them so that
             // whatever the caller's memory holds there cannot reach O via 0 * NaN.
             const int t = info.tb + j;
@@ -415,8 +438,13 @@ __device__ __forceinline__ void pv_loop(const AttnArgs &a, uint8_t *smem, uint32
             mma_commit(bar(C::B_S_FREE + sb));
             mma_commit(bar(C::B_V_EMPTY + vs));
         }
-        if (lane == 0) mbar_arrive(bar(C::B_ITEM_EMPTY + slot));
+        if (ok && lane == 0) mbar_arrive(bar(C::B_ITEM_EMPTY + slot));
     }
+    // Every MMA this warp issued has completed before the CTA can free TMEM
+    // or exit, on every path (an abort included).
+    mma_commit(bar(C::B_DRAIN + 1));
+    if (lane == 0) mbar_wait_drain(bar(C::B_DRAIN + 1), 0);
+    __syncwarp();
 }
 
 // Ancestor mask ("JetFlow: Scaling Speculative Decoding with Parallel Tree
@@ -778,6 +806,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int q = 0; q < 4; ++q) init(C::B_PAIR + q, 2); // the two warps that share a row quadrant
         for (int h = 0; h < 8; ++h) init(C::B_HAND + h, 1); // row-max hand-off, [quadrant][tile parity]
         init(C::B_EPI, kSoftmaxWarps);                     // an item's output is staged
+        init(C::B_DRAIN + 0, 1);                           // the QK^T issuer's MMAs have completed
+        init(C::B_DRAIN + 1, 1);                           // the PV issuer's MMAs have completed
         *abort = 0;
         fence_mbar_init();
     }
