@@ -47,10 +47,10 @@ def test_workspace_bytes(lib):
 def _argmax_chunks(rows, V):
     """Chunks per logits row, as include/jf_tree.h and the layout state it:
     pieces of about 76800 elements, more of them for few rows (up to ~4
-    CTAs per SM of 152, within one wave of 5 per SM), multiples of 2048."""
+    CTAs per SM of 152, within one wave of 4 per SM), multiples of 2048."""
     cdiv = lambda a, b: -(-a // b)
     per = cdiv(V, 76800)
-    want = min(cdiv(4 * 152, rows), 5 * 152 // rows)
+    want = min(cdiv(4 * 152, rows), 4 * 152 // rows)
     if want > per:
         per = min(want, cdiv(V, 2048))
     chunk = cdiv(cdiv(V, per), 2048) * 2048

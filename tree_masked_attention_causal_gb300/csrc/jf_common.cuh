@@ -28,7 +28,7 @@ constexpr int kMinTilesPerCta = 2;   // smallest key range a CTA is given
 constexpr int kMaxBatch = 1024;   // sequences per jf_tree_attention call
 constexpr int kArgmaxThreads = 256;
 constexpr int kArgmaxVecs = 8;    // 16-byte loads in flight per thread
-constexpr int kArgmaxCtasPerSm = 5;  // resident argmax CTAs per SM (at most 51 registers)
+constexpr int kArgmaxCtasPerSm = 4;  // resident argmax CTAs per SM (64 registers: no spills)
 constexpr int kArgmaxMaxChunk = 76800;  // target bf16 of one logits row per CTA (150 KB)
 constexpr int kArgmaxGranule = kArgmaxThreads * 8;  // chunks are whole vectors per thread
 constexpr int kSmCount = 152;     // SMs of the part the chunking is tuned for

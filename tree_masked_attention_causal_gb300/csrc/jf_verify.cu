@@ -7,7 +7,7 @@
 //
 //  argmax_chunk_kernel  HBM-bound scan of the logits. Each CTA owns a chunk
 //                       of one row: about 76800 bf16 (two chunks per row of
-//                       151936, one wave of CTAs for 256 rows at 5 CTAs per
+//                       151936, one wave of CTAs for 256 rows at 4 CTAs per
 //                       SM), or shorter chunks when there are few rows, so
 //                       that the grid still fills the SMs. Every thread
 //                       streams 128-bit loads, 8 in flight, and keeps a
