@@ -14,9 +14,11 @@ refused before anything is launched. This file is named to be collected
 last.
 """
 
+import numpy as np
 import pytest
 import torch
 
+import oracle
 from tree_masked_attention_causal_gb300 import _build, binding as jb, synth
 
 A16 = 1 << 20            # fake aligned address, never dereferenced
@@ -68,3 +70,8 @@ def test_noalloc_matches_workspace_variant_on_two_calls_in_a_row():
             assert torch.equal(r, g), name
         assert ref[3] == got[3] == 0
         assert torch.equal(got[0], inp["planted_len"])
+        # and directly against the fp64 oracle's argmax, lengths and paths
+        r_len, r_path, r_am = oracle.tree_verify(inp["logits"], inp["tokens"], inp["parents"], inp["n_nodes"], 16)
+        np.testing.assert_array_equal(got[0].numpy(), r_len)
+        np.testing.assert_array_equal(got[1].numpy(), r_path)
+        np.testing.assert_array_equal(got[2].numpy(), r_am)

@@ -252,18 +252,40 @@ JF_API int32_t jf_tree_verify(const void *logits, const int32_t *tree_tokens, co
 // memory, so the call needs no caller workspace and allocates nothing.
 static __device__ __align__(256) uint8_t g_noalloc_scratch[JF_NOALLOC_SCRATCH_BYTES];
 
+// Current driver context (CUcontext), through the runtime's driver entry
+// point query so that the library needs no link-time dependency on libcuda.
+static void *current_context() {
+    typedef CUresult (*CtxGetFn)(CUcontext *);
+    static CtxGetFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<CtxGetFn>(p);
+    });
+    CUcontext c = nullptr;
+    if (!fn || fn(&c) != CUDA_SUCCESS) return nullptr;
+    return c;
+}
+
 // Device address of g_noalloc_scratch on the current device, looked up once
-// per device. In host code the symbol's name is only a host-side stand-in,
-// so the kernels must be given this address instead.
+// per device and context (a reset device gets a new context, and the module
+// a new address). In host code the symbol's name is only a host-side
+// stand-in, so the kernels must be given this address instead.
 static uint8_t *noalloc_scratch(int dev) {
     static std::mutex mu;
     static uint8_t *addr[64] = {nullptr};
+    static void *ctx[64] = {nullptr};
     if (dev < 0 || dev >= 64) return nullptr;
     std::lock_guard<std::mutex> lk(mu);
-    if (!addr[dev]) {
+    void *cur = current_context();
+    if (!addr[dev] || cur != ctx[dev]) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
         addr[dev] = reinterpret_cast<uint8_t *>(p);
+        ctx[dev] = current_context();   // the lookup may have created the primary context
     }
     return addr[dev];
 }
