@@ -194,10 +194,10 @@ JF_API int32_t jf_tree_verify(const void *logits, const int32_t *tree_tokens,
  * exits. The call itself allocates nothing.
  *  - Limit: rows * chunks * 8 bytes must be <= JF_NOALLOC_SCRATCH_BYTES,
  *    with rows = batch * max_nodes and chunks the argmax pieces per logits
- *    row, at most max(ceil(vocab / 76800), ceil(608 / rows)). For vocab
- *    151936 that is 2 from 304 rows up, so every problem that the row limit
- *    of jf_tree_verify admits (at most 65535 rows) fits. Larger problems
- *    return JF_ERR_SHAPE and launch nothing.
+ *    row, at most max(ceil(vocab / 76800), ceil(4 * SMs / rows)) (608 / rows
+ *    on a 152-SM GB300). For vocab 151936 that is 2 from 304 rows up, so
+ *    every problem that the row limit of jf_tree_verify admits (at most 65535
+ *    rows) fits. Larger problems return JF_ERR_SHAPE and launch nothing.
  *  - The first call on a device looks up the array's device address (with
  *    that device current) and caches it with the device's current context;
  *    a call under another context (after cudaDeviceReset, for example)

@@ -44,25 +44,33 @@ def test_workspace_bytes(lib):
     assert lib.jf_workspace_bytes(None) == 0
 
 
-def _argmax_chunks(rows, V):
+def _argmax_chunks(rows, V, sms=256):
     """Chunks per logits row, as include/jf_tree.h and the layout state it:
     pieces of about 76800 elements, more of them for few rows (up to ~4
-    CTAs per SM of 152, within one wave of 4 per SM), multiples of 2048."""
+    CTAs per SM, within one wave of 4 per SM), multiples of 2048. A call
+    cuts them for its device's SM count; the workspace is sized for 256."""
     cdiv = lambda a, b: -(-a // b)
     per = cdiv(V, 76800)
-    want = min(cdiv(4 * 152, rows), 4 * 152 // rows)
+    want = min(cdiv(4 * sms, rows), 4 * sms // rows)
     if want > per:
         per = min(want, cdiv(V, 2048))
     chunk = cdiv(cdiv(V, per), 2048) * 2048
     return cdiv(V, chunk)
 
 
-@pytest.mark.parametrize("B,N,V,expect", [(1, 256, 151936, 2), (1, 16, 151936, 38), (16, 64, 151936, 2),
-                                          (2, 5, 151936, 38), (1, 16, 1024, 1), (4, 200, 262144, 4),
-                                          (1, 152, 151936, 4)])
+@pytest.mark.parametrize("rows,V,expect", [(256, 151936, 2), (16, 151936, 38), (10, 151936, 38), (152, 151936, 4)])
+def test_argmax_chunks_on_152_sms(rows, V, expect):
+    """The chunking a call on a 152-SM GB300 uses (the rule, restated)."""
+    assert _argmax_chunks(rows, V, sms=152) == expect
+
+
+@pytest.mark.parametrize("B,N,V,expect", [(1, 256, 151936, 4), (1, 16, 151936, 38), (16, 64, 151936, 2),
+                                          (2, 5, 151936, 75), (1, 16, 1024, 1), (4, 200, 262144, 4),
+                                          (1, 152, 151936, 6)])
 def test_argmax_chunk_rule(lib, B, N, V, expect):
     """The verify region of the workspace holds one int2 per (row, chunk):
-    its growth from a one-chunk vocabulary pins the chunk count."""
+    its growth from a one-chunk vocabulary pins the chunk count it is sized
+    for (256 SMs, the bound for any device's chunking)."""
     assert _argmax_chunks(B * N, V) == expect
     align = lambda x: -(-x // 256) * 256
     base = jb.jf_workspace_bytes(jb.make_shape(B, 0, 0, 0, N, 0, 8))

@@ -95,11 +95,13 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 bool attn_shape_ok(const jf_shape *s) { return check_shape(s, false, true) == JF_OK; }
 bool verify_shape_ok(const jf_shape *s) { return check_shape(s, true, false) == JF_OK; }
 
-Layout layout_of(const jf_shape *shape) {
+// `sms`: the device's SM count in a call, kMaxSms for jf_workspace_bytes.
+Layout layout_of(const jf_shape *shape, int sms = kMaxSms) {
     jf_shape s = *shape;
     if (!attn_shape_ok(&s)) { s.n_q_heads = 1; s.n_kv_heads = 1; s.head_dim = 64; s.prefix_cap = 1; }
     if (!verify_shape_ok(&s)) s.vocab = 8;
-    return make_layout(s.batch, s.max_nodes, s.n_q_heads, s.n_kv_heads, s.head_dim, s.prefix_cap, s.vocab);
+    return make_layout(s.batch, s.max_nodes, s.n_q_heads, s.n_kv_heads, s.head_dim, s.prefix_cap, s.vocab,
+                       sms < kMaxSms ? sms : kMaxSms);
 }
 
 // ----------------------------------------------------- device queries
@@ -236,7 +238,11 @@ JF_API int32_t jf_tree_verify(const void *logits, const int32_t *tree_tokens, co
     if (max_depth < 0) return JF_ERR_SHAPE;
     if (!aligned16(logits) || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return JF_ERR_ALIGN;
     if (workspace_bytes < jf_workspace_bytes(shape)) return JF_ERR_WORKSPACE;
-    const Layout L = layout_of(shape);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return JF_ERR_CUDA;
+    const int sms = num_sms_cached(dev);
+    if (sms <= 0) return JF_ERR_CUDA;
+    const Layout L = layout_of(shape, sms);          // the argmax chunking for this device
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     uint8_t *ws = reinterpret_cast<uint8_t *>(workspace);
     if (launch_argmax(L, reinterpret_cast<const __nv_bfloat16 *>(logits), n_nodes, ws, s) != cudaSuccess)
@@ -300,11 +306,19 @@ JF_API int32_t jf_tree_verify_noalloc(const void *logits, const int32_t *tree_to
     if (sc != JF_OK) return sc;
     if (max_depth < 0) return JF_ERR_SHAPE;
     if (!aligned16(logits)) return JF_ERR_ALIGN;
-    Layout L = layout_of(shape);
-    const size_t need = sizeof(int2) * (size_t)L.B * L.Nmax * L.chunks;
-    if (need > (size_t)JF_NOALLOC_SCRATCH_BYTES) return JF_ERR_SHAPE;
+    // rows * chunks int2 must fit the array: refuse what cannot fit even at
+    // one chunk per 76800 elements before any CUDA call, then check the
+    // chunking of this device exactly
+    const long long rows = (long long)shape->batch * shape->max_nodes;
+    if (rows * ceil_div(shape->vocab, kArgmaxMaxChunk) * (long long)sizeof(int2) > (long long)JF_NOALLOC_SCRATCH_BYTES)
+        return JF_ERR_SHAPE;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return JF_ERR_CUDA;
+    const int sms = num_sms_cached(dev);
+    if (sms <= 0) return JF_ERR_CUDA;
+    Layout L = layout_of(shape, sms);
+    const size_t need = sizeof(int2) * (size_t)L.B * L.Nmax * L.chunks;
+    if (need > (size_t)JF_NOALLOC_SCRATCH_BYTES) return JF_ERR_SHAPE;
     uint8_t *scratch = noalloc_scratch(dev);
     if (!scratch) return JF_ERR_CUDA;
     L.amp_off = 0;   // the verify region starts at the array's first byte

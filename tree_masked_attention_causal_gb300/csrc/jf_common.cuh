@@ -31,7 +31,7 @@ constexpr int kArgmaxVecs = 8;    // 16-byte loads in flight per thread
 constexpr int kArgmaxCtasPerSm = 4;  // resident argmax CTAs per SM (64 registers: no spills)
 constexpr int kArgmaxMaxChunk = 76800;  // target bf16 of one logits row per CTA (150 KB)
 constexpr int kArgmaxGranule = kArgmaxThreads * 8;  // chunks are whole vectors per thread
-constexpr int kSmCount = 152;     // SMs of the part the chunking is tuned for
+constexpr int kMaxSms = 256;      // SM count the workspace is sized for (the chunking uses the real one)
 constexpr unsigned long long kTimeoutNs = 2000000000ull;        // 2 s per wait
 
 __host__ __device__ constexpr int ceil_div(int a, int b) { return (a + b - 1) / b; }
@@ -66,7 +66,10 @@ struct Layout {
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // The layout depends only on the shape (never on prefix lengths or trees).
-inline Layout make_layout(int B, int Nmax, int Hq, int Hkv, int D, int Pcap, int V) {
+// `sms` is the SM count the argmax chunking is cut for: the device's own in
+// a call, kMaxSms when sizing a workspace (more SMs never mean fewer
+// chunks, so a call's layout always fits the sized one).
+inline Layout make_layout(int B, int Nmax, int Hq, int Hkv, int D, int Pcap, int V, int sms) {
     Layout L{};
     L.B = B; L.Nmax = Nmax; L.Hq = Hq; L.Hkv = Hkv; L.G = Hq / Hkv; L.D = D; L.Pcap = Pcap; L.V = V;
     L.NB = kRows / L.G;
@@ -82,8 +85,8 @@ inline Layout make_layout(int B, int Nmax, int Hq, int Hkv, int D, int Pcap, int
     int per_row = V > 0 ? ceil_div(V, kArgmaxMaxChunk) : 1;
     const long long rows = (long long)B * Nmax;
     if (V > 0 && rows > 0) {
-        const long long fill = (4LL * kSmCount + rows - 1) / rows;
-        const long long wave = (long long)kArgmaxCtasPerSm * kSmCount / rows;
+        const long long fill = (4LL * sms + rows - 1) / rows;
+        const long long wave = (long long)kArgmaxCtasPerSm * sms / rows;
         const long long want = fill < wave ? fill : wave;
         const long long most = ceil_div(V, kArgmaxGranule);
         if (want > per_row) per_row = (int)(want < most ? want : most);
@@ -398,8 +401,9 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn, b
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T, one CTA. Called by a whole converged
-// warp with warp-uniform operands; one elected lane issues. Issued this way
-// an MMA costs about 87 cycles, from a single-lane branch about 110-150
+// warp with warp-uniform operands; one elected lane issues. Issued this way,
+// back to back, one warp keeps the tensor core at its full rate (64 cycles
+// per 128 x 128 x 16); from a single-lane branch an MMA costs 110-150 cycles
 // (measured on GB300).
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                        uint32_t accumulate) {
