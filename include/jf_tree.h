@@ -76,8 +76,11 @@ enum {
     JF_STATUS_BAD_TREE = 1,  /* a sequence had n_nodes outside [1, max_nodes], a
                                 parent breaking the encoding above, or (for
                                 attention) prefix_lens outside [0, prefix_cap] */
-    JF_STATUS_TIMEOUT = 2    /* a kernel's bounded wait expired; outputs of the
+    JF_STATUS_TIMEOUT = 2,   /* a kernel's bounded wait expired; outputs of the
                                 call are undefined (never expected) */
+    JF_STATUS_CACHE_FULL = 4 /* jf_tree_commit_kv: a sequence's accepted path
+                                did not fit in its KV cache; that sequence
+                                was left unchanged */
 };
 
 /*
@@ -179,6 +182,43 @@ JF_API int32_t jf_tree_verify(const void *logits, const int32_t *tree_tokens,
                               int32_t *argmax_out, const jf_shape *shape, int32_t max_depth,
                               void *workspace, size_t workspace_bytes, int32_t *status,
                               jf_stream_t stream);
+
+/*
+ * Accepted-path KV commit: the step after verification (the paper's section
+ * 2.1 "Background": the prefix the target accepts extends the context). The
+ * keys and values of the accepted nodes were computed by this tree's
+ * attention pass (tree_k / tree_v rows); they become the next rows of each
+ * sequence's KV cache, root first, and the prefix length grows by the
+ * number of nodes.
+ *
+ * For sequence b, with a = accept_len[b] and P = prefix_lens[b]: for k < a
+ * and every kv head h, row P + k of head h of k_cache becomes
+ * tree_k[b, accept_path[b, k], h, :] (v_cache from tree_v alike), bit for
+ * bit, and prefix_lens[b] becomes P + a. With a = 0 (what jf_tree_verify
+ * reports for a malformed tree) nothing changes.
+ *
+ *   tree_k, tree_v   bf16 [B, Nmax, Hkv, d], as for jf_tree_attention
+ *   n_nodes          int32 [B]
+ *   accept_len       int32 [B]           (from jf_tree_verify)
+ *   accept_path      int32 [B, max_depth + 1]  (from jf_tree_verify)
+ *   k_cache, v_cache bf16 [B, Hkv, Pcap, d], updated in place
+ *   prefix_lens      int32 [B], updated in place (the same array the next
+ *                    jf_tree_attention call reads)
+ *   shape, max_depth as for jf_tree_attention / jf_tree_verify
+ *   status           device int32 or NULL
+ * A sequence whose request is malformed (n_nodes outside [1, Nmax],
+ * accept_len outside [0, min(n_nodes, max_depth + 1)], prefix_lens outside
+ * [0, Pcap], or a path entry that is not a node of the tree) raises
+ * JF_STATUS_BAD_TREE; one whose path does not fit (P + a > Pcap) raises
+ * JF_STATUS_CACHE_FULL. Either way that sequence is left unchanged.
+ * Every bf16 pointer must be 16-byte aligned. The call needs no workspace
+ * and allocates nothing.
+ * Returns JF_OK, JF_ERR_NULL, JF_ERR_SHAPE, JF_ERR_ALIGN or JF_ERR_CUDA.
+ */
+JF_API int32_t jf_tree_commit_kv(const void *tree_k, const void *tree_v, const int32_t *n_nodes,
+                                 const int32_t *accept_len, const int32_t *accept_path, void *k_cache,
+                                 void *v_cache, int32_t *prefix_lens, const jf_shape *shape,
+                                 int32_t max_depth, int32_t *status, jf_stream_t stream);
 
 /*
  * Allocation-free variant of jf_tree_verify. The paper has no counterpart:

@@ -55,6 +55,8 @@ def _load():
             lib.oracle_tree_verify.restype = None
             lib.oracle_tree_is_valid.argtypes = [P, i32, i32]
             lib.oracle_tree_is_valid.restype = ctypes.c_int
+            lib.oracle_commit_kv.argtypes = [P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, P]
+            lib.oracle_commit_kv.restype = None
             _lib = lib
     return _lib
 
@@ -135,3 +137,20 @@ def tree_is_valid(parents_row, n: int, max_nodes: int) -> bool:
     lib = _load()
     p = _i32(np.asarray(parents_row))
     return bool(lib.oracle_tree_is_valid(_ptr(p), int(n), int(max_nodes)))
+
+
+def commit_kv(tree_k, tree_v, n_nodes, accept_len, accept_path, k_cache, v_cache, prefix_lens, max_depth: int):
+    """Accepted-path KV commit. Returns (k_cache, v_cache, prefix_lens, flags)
+    as new arrays (bf16 bits as uint16, int32); the inputs are not modified.
+    flags[b]: 0 done (or nothing to do), 1 malformed request, 2 no room."""
+    lib = _load()
+    tk, tv = _u16(tree_k), _u16(tree_v)
+    kc, vc = _u16(k_cache).copy(), _u16(v_cache).copy()
+    B, Nmax, Hkv, d = tk.shape
+    Pcap = kc.shape[2]
+    nn, al, ap = _i32(n_nodes), _i32(accept_len), _i32(accept_path)
+    pl = _i32(prefix_lens).copy()
+    flags = np.zeros(B, dtype=np.int32)
+    lib.oracle_commit_kv(_ptr(tk), _ptr(tv), _ptr(nn), _ptr(al), _ptr(ap), _ptr(kc), _ptr(vc), _ptr(pl),
+                         B, Nmax, Hkv, d, Pcap, int(max_depth), _ptr(flags))
+    return kc, vc, pl, flags

@@ -241,3 +241,59 @@ void oracle_tree_verify(const uint16_t *logits, const int32_t *tokens, const int
     free(am);
     free(chain);
 }
+
+/*
+ * Accepted-path KV commit ([paper] section 2.1: the prefix that the target
+ * accepts extends the context). The accepted nodes' keys and values, taken
+ * from the tree's own rows, become the next rows of the sequence's cache,
+ * root first, and the prefix length grows by the number of nodes.
+ *
+ * For sequence b, with a = accept_len[b], P = prefix_lens[b], n = n_nodes[b]:
+ *  - a == 0 (a malformed tree, as the verification reports it): nothing
+ *    changes and flags[b] = 0;
+ *  - the request is malformed if n is outside [1, Nmax], a outside
+ *    [0, max_depth + 1] or above n (a path of tree nodes is no longer than
+ *    the tree), P outside [0, Pcap], or a path entry path[b][k] (k < a)
+ *    outside [0, n): nothing changes and flags[b] = 1;
+ *  - the cache lacks room if P + a > Pcap: nothing changes and flags[b] = 2;
+ *  - otherwise, for k < a and every kv head h, row P + k of head h of
+ *    k_cache (v_cache) becomes tree_k[b][path[b][k]][h] (tree_v), bit for
+ *    bit, prefix_lens[b] becomes P + a, and flags[b] = 0.
+ * Layouts: tree_k/tree_v [B, Nmax, Hkv, d], k_cache/v_cache [B, Hkv, Pcap, d]
+ * (bf16 bits), accept_path [B, max_depth + 1].
+ */
+void oracle_commit_kv(const uint16_t *tree_k, const uint16_t *tree_v, const int32_t *n_nodes,
+                      const int32_t *accept_len, const int32_t *accept_path, uint16_t *k_cache,
+                      uint16_t *v_cache, int32_t *prefix_lens, int32_t B, int32_t Nmax, int32_t Hkv,
+                      int32_t d, int32_t Pcap, int32_t max_depth, int32_t *flags)
+{
+    for (int32_t b = 0; b < B; ++b) {
+        const int32_t a = accept_len[b], P = prefix_lens[b], n = n_nodes[b];
+        const int32_t *path = accept_path + (int64_t)b * (max_depth + 1);
+        flags[b] = 0;
+        if (a == 0) continue;
+        int bad = n < 1 || n > Nmax || a < 0 || a > n || a > max_depth + 1 || P < 0 || P > Pcap;
+        for (int32_t k = 0; !bad && k < a; ++k)
+            if (path[k] < 0 || path[k] >= n) bad = 1;
+        if (bad) {
+            flags[b] = 1;
+            continue;
+        }
+        if (P + a > Pcap) {
+            flags[b] = 2;
+            continue;
+        }
+        for (int32_t k = 0; k < a; ++k) {
+            const int32_t node = path[k];
+            for (int32_t h = 0; h < Hkv; ++h) {
+                const int64_t src = (((int64_t)b * Nmax + node) * Hkv + h) * d;
+                const int64_t dst = (((int64_t)b * Hkv + h) * Pcap + P + k) * d;
+                for (int32_t e = 0; e < d; ++e) {
+                    k_cache[dst + e] = tree_k[src + e];
+                    v_cache[dst + e] = tree_v[src + e];
+                }
+            }
+        }
+        prefix_lens[b] = P + a;
+    }
+}

@@ -146,6 +146,33 @@ def test_verify_bad_depth_alignment_workspace(lib):
     assert verify(s, ws_bytes=jb.jf_workspace_bytes(s) - 1) == jb.JF_ERR_WORKSPACE
 
 
+def commit(shape, max_depth=16, **over):
+    args = dict(tree_k=A16, tree_v=A16, n_nodes=A16, alen=A16, path=A16, k_cache=A16, v_cache=A16,
+                prefix_lens=A16)
+    args.update(over)
+    return jb.jf_tree_commit_kv(args["tree_k"], args["tree_v"], args["n_nodes"], args["alen"], args["path"],
+                                args["k_cache"], args["v_cache"], args["prefix_lens"], shape, max_depth, stream=0,
+                                check=False)
+
+
+@pytest.mark.parametrize("name", ["tree_k", "tree_v", "n_nodes", "alen", "path", "k_cache", "v_cache",
+                                  "prefix_lens"])
+def test_commit_null_pointer(lib, name):
+    assert commit(good_shape(), **{name: None}) == jb.JF_ERR_NULL
+
+
+@pytest.mark.parametrize("bad", [dict(batch=0), dict(head_dim=96), dict(max_nodes=300), dict(prefix_cap=0),
+                                 dict(n_kv_heads=0)])
+def test_commit_bad_shape(lib, bad):
+    assert commit(good_shape(**bad)) == jb.JF_ERR_SHAPE
+
+
+@pytest.mark.parametrize("name", ["tree_k", "tree_v", "k_cache", "v_cache"])
+def test_commit_misaligned_and_depth(lib, name):
+    assert commit(good_shape(), **{name: A16 + 8}) == jb.JF_ERR_ALIGN
+    assert commit(good_shape(), max_depth=-1) == jb.JF_ERR_SHAPE
+
+
 def test_status_strings(lib):
     for code in range(6):
         assert jb.jf_status_string(code)

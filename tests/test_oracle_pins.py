@@ -360,3 +360,85 @@ def test_tree_validity_rule():
     assert not oracle.tree_is_valid([-1], 0, 1)
     assert not oracle.tree_is_valid([-1, 0], 3, 2)
     assert oracle.tree_is_valid([-1, 0, 77], 2, 3)          # padding is not checked
+
+
+# ----------------------------------------------------------- KV commit
+
+
+def _commit_cases():
+    path = os.path.join(os.path.dirname(__file__), "golden", "commit_cases.txt")
+    cases, cur = [], None
+    for line in open(path):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        key, *vals = line.split()
+        if key == "case":
+            cur = {"name": vals[0], "rows": []}
+            cases.append(cur)
+        elif key == "row":
+            cur["rows"].append((int(vals[0]), int(vals[3])))
+        elif key == "path":
+            cur["path"] = [int(v) for v in vals]
+        else:
+            cur[key] = int(vals[0])
+    return cases
+
+
+@pytest.mark.parametrize("case", _commit_cases(), ids=lambda c: c["name"])
+def test_commit_kv_golden_cases(case):
+    """Hand-worked commits (tests/golden/commit_cases.txt): which cache rows
+    change, from which node, the new prefix length and the flag."""
+    Hkv, d, Pcap, Nmax = case["Hkv"], 2, 6, 4
+    val = np.zeros((1, Nmax, Hkv, d), dtype=np.float32)
+    for i in range(Nmax):
+        for h in range(Hkv):
+            for e in range(d):
+                val[0, i, h, e] = i + h / 4 + e / 8
+    tk = torch.from_numpy(val).to(torch.bfloat16)
+    tv = torch.from_numpy(-val).to(torch.bfloat16)
+    kc = torch.full((1, Hkv, Pcap, d), 0.5, dtype=torch.bfloat16)
+    vc = torch.full((1, Hkv, Pcap, d), 0.5, dtype=torch.bfloat16)
+    k2, v2, pl, flags = oracle.commit_kv(tk, tv, torch.tensor([case["n"]], dtype=torch.int32),
+                                         torch.tensor([case["a"]], dtype=torch.int32),
+                                         torch.tensor([case["path"]], dtype=torch.int32), kc, vc,
+                                         torch.tensor([case["P"]], dtype=torch.int32), case["max_depth"])
+    assert int(flags[0]) == case["flag"]
+    assert int(pl[0]) == case["new_P"]
+    half = np.uint16(0x3F00)                      # bf16 0.5
+    want_k = np.full((1, Hkv, Pcap, d), half, dtype=np.uint16)
+    want_v = want_k.copy()
+    tkb = tk.view(torch.int16).numpy().view(np.uint16)
+    tvb = tv.view(torch.int16).numpy().view(np.uint16)
+    for r, i in case["rows"]:
+        want_k[0, :, r] = tkb[0, i]
+        want_v[0, :, r] = tvb[0, i]
+    np.testing.assert_array_equal(k2, want_k)
+    np.testing.assert_array_equal(v2, want_v)
+
+
+def test_commit_then_attention_equals_chain_attention():
+    """Composition with the attention's definition: commit a whole chain
+    (path 0..N-1) and node i's tree attention over the original prefix
+    equals attention over the committed cache cut at P + i (rows of nodes
+    0..i-1) with a one-node tree holding node i. A wrong row order, offset
+    or head in the commit changes the key sequence and fails this."""
+    g = torch.Generator().manual_seed(77)
+    B, N, Hq, Hkv, d, P, Pcap = 2, 6, 4, 2, 64, 5, 16
+    bf = lambda *s: torch.randn(*s, generator=g).to(torch.bfloat16)
+    q, tk, tv = bf(B, N, Hq, d), bf(B, N, Hkv, d), bf(B, N, Hkv, d)
+    kc, vc = bf(B, Hkv, Pcap, d), bf(B, Hkv, Pcap, d)
+    chain = torch.tensor([[-1] + list(range(N - 1))] * B, dtype=torch.int32)
+    pl = torch.full((B,), P, dtype=torch.int32)
+    nn = torch.full((B,), N, dtype=torch.int32)
+    ref = oracle.tree_attention(q, kc, vc, pl, tk, tv, chain, nn)
+    k2, v2, pl2, flags = oracle.commit_kv(tk, tv, nn, nn, torch.arange(N, dtype=torch.int32).repeat(B, 1), kc, vc,
+                                          pl, N - 1)
+    assert (flags == 0).all() and (pl2 == P + N).all()
+    k2 = torch.from_numpy(k2.view(np.int16)).view(torch.bfloat16)
+    v2 = torch.from_numpy(v2.view(np.int16)).view(torch.bfloat16)
+    one = torch.full((B, 1), -1, dtype=torch.int32)
+    for i in range(N):
+        got = oracle.tree_attention(q[:, i:i + 1], k2, v2, torch.full((B,), P + i, dtype=torch.int32),
+                                    tk[:, i:i + 1], tv[:, i:i + 1], one, torch.ones(B, dtype=torch.int32))
+        np.testing.assert_allclose(got[:, 0], ref[:, i], rtol=0, atol=1e-12)

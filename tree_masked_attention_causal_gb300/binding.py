@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(PKG, "libjf_tree.so")
 HEADER = os.path.join(os.path.dirname(PKG), "include", "jf_tree.h")
 
 JF_OK, JF_ERR_NULL, JF_ERR_SHAPE, JF_ERR_ALIGN, JF_ERR_WORKSPACE, JF_ERR_CUDA = range(6)
-JF_STATUS_BAD_TREE, JF_STATUS_TIMEOUT = 1, 2
+JF_STATUS_BAD_TREE, JF_STATUS_TIMEOUT, JF_STATUS_CACHE_FULL = 1, 2, 4
 
 
 class JfShape(ctypes.Structure):
@@ -75,6 +75,8 @@ def _configure(lib: ctypes.CDLL) -> ctypes.CDLL:
         lib.jf_trace_name.restype = ctypes.c_char_p
         lib.jf_tree_verify_noalloc.argtypes = [P, P, P, P, P, P, P, sp, i32, P, P]
         lib.jf_tree_verify_noalloc.restype = i32
+        lib.jf_tree_commit_kv.argtypes = [P, P, P, P, P, P, P, P, sp, i32, P, P]
+        lib.jf_tree_commit_kv.restype = i32
     return lib
 
 
@@ -140,6 +142,17 @@ def jf_tree_verify(logits, tree_tokens, parents, n_nodes, accept_len_out, accept
                                _ptr(status), _stream(stream))
     if check and rc != JF_OK:
         raise JfError("jf_tree_verify", rc)
+    return rc
+
+
+def jf_tree_commit_kv(tree_k, tree_v, n_nodes, accept_len, accept_path, k_cache, v_cache, prefix_lens,
+                      shape: JfShape, max_depth: int, status=None, stream=None, check: bool = True) -> int:
+    """Append each sequence's accepted path to its KV cache (see jf_tree.h)."""
+    rc = load().jf_tree_commit_kv(_ptr(tree_k), _ptr(tree_v), _ptr(n_nodes), _ptr(accept_len), _ptr(accept_path),
+                                  _ptr(k_cache), _ptr(v_cache), _ptr(prefix_lens), ctypes.byref(shape),
+                                  int(max_depth), _ptr(status), _stream(stream))
+    if check and rc != JF_OK:
+        raise JfError("jf_tree_commit_kv", rc)
     return rc
 
 

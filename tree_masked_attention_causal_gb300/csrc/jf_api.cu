@@ -253,6 +253,27 @@ JF_API int32_t jf_tree_verify(const void *logits, const int32_t *tree_tokens, co
     return JF_OK;
 }
 
+JF_API int32_t jf_tree_commit_kv(const void *tree_k, const void *tree_v, const int32_t *n_nodes,
+                                 const int32_t *accept_len, const int32_t *accept_path, void *k_cache,
+                                 void *v_cache, int32_t *prefix_lens, const jf_shape *shape, int32_t max_depth,
+                                 int32_t *status, jf_stream_t stream) {
+    if (!tree_k || !tree_v || !n_nodes || !accept_len || !accept_path || !k_cache || !v_cache || !prefix_lens ||
+        !shape)
+        return JF_ERR_NULL;
+    const int32_t sc = check_shape(shape, false, true);
+    if (sc != JF_OK) return sc;
+    if (max_depth < 0) return JF_ERR_SHAPE;
+    if (!aligned16(tree_k) || !aligned16(tree_v) || !aligned16(k_cache) || !aligned16(v_cache)) return JF_ERR_ALIGN;
+    const Layout L = layout_of(shape);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (launch_commit_kv(L, reinterpret_cast<const __nv_bfloat16 *>(tree_k),
+                         reinterpret_cast<const __nv_bfloat16 *>(tree_v), n_nodes, accept_len, accept_path,
+                         reinterpret_cast<__nv_bfloat16 *>(k_cache), reinterpret_cast<__nv_bfloat16 *>(v_cache),
+                         prefix_lens, max_depth, status, s) != cudaSuccess)
+        return JF_ERR_CUDA;
+    return JF_OK;
+}
+
 // ------------------------------------------------ allocation-free verify
 // Scratch for jf_tree_verify_noalloc: lives in the library's own device
 // memory, so the call needs no caller workspace and allocates nothing.

@@ -1,0 +1,80 @@
+// jf_commit.cu - accepted-path KV commit on sm_103a.
+//
+// The paper's section 2.1 "Background": the prefix the target accepts
+// extends the context. After greedy verification the accepted path's nodes
+// (root first) become the next rows of each sequence's KV cache: their keys
+// and values are the tree's own rows, already computed by the attention pass
+// with the right positions, so committing them is a copy, and the prefix
+// length grows by the path length.
+//
+// One block per sequence (so that reading and raising prefix_lens[b] cannot
+// race with another block), 256 threads. The block checks the request, then
+// copies a * Hkv key rows and as many value rows in 16-byte pieces, one
+// piece per thread per step, and raises the length last.
+#include "jf_common.cuh"
+
+namespace jf {
+namespace {
+
+constexpr int kCommitThreads = 256;
+
+__global__ void __launch_bounds__(kCommitThreads)
+    commit_kv_kernel(const __nv_bfloat16 *__restrict__ tree_k, const __nv_bfloat16 *__restrict__ tree_v,
+                     const int32_t *__restrict__ n_nodes, const int32_t *__restrict__ accept_len,
+                     const int32_t *__restrict__ accept_path, __nv_bfloat16 *__restrict__ k_cache,
+                     __nv_bfloat16 *__restrict__ v_cache, int32_t *__restrict__ prefix_lens, int Nmax, int Hkv,
+                     int D, int Pcap, int max_depth, int32_t *status) {
+    __shared__ int s_node[kMaxNodes + 1];
+    const int b = blockIdx.x, tid = threadIdx.x;
+    const int a = accept_len[b], P = prefix_lens[b], n = n_nodes[b];
+    const int32_t *path = accept_path + (size_t)b * (max_depth + 1);
+    if (a == 0) return;                                   // nothing accepted (a malformed tree)
+    // The request: n in [1, Nmax], a in [0, min(n, max_depth + 1)] (a path of
+    // tree nodes is no longer than the tree), P in [0, Pcap], every path
+    // entry a node of the tree; then room for a more rows.
+    bool bad = n < 1 || n > Nmax || a < 0 || a > n || a > max_depth + 1 || P < 0 || P > Pcap;
+    for (int k = tid; !bad && k < a; k += kCommitThreads) {
+        const int node = path[k];
+        if (node < 0 || node >= n) bad = true;
+        else s_node[k] = node;
+    }
+    bad = __syncthreads_or(bad);
+    if (bad || P + a > Pcap) {
+        if (tid == 0) set_status(status, bad ? JF_STATUS_BAD_TREE : JF_STATUS_CACHE_FULL);
+        return;
+    }
+    // a rows x Hkv heads x (K, V), d / 8 sixteen-byte pieces each: piece e
+    // of row (k, h) of K (kv = 0) or V (kv = 1)
+    const int pieces = D / 8;
+    const int total = a * Hkv * 2 * pieces;
+    for (int idx = tid; idx < total; idx += kCommitThreads) {
+        const int e = idx % pieces;
+        int r = idx / pieces;
+        const int kv = r & 1;
+        r >>= 1;
+        const int h = r % Hkv, k = r / Hkv;
+        const size_t src = (((size_t)b * Nmax + s_node[k]) * Hkv + h) * D + e * 8;
+        const size_t dst = (((size_t)b * Hkv + h) * Pcap + P + k) * D + e * 8;
+        const uint4 *s = reinterpret_cast<const uint4 *>((kv ? tree_v : tree_k) + src);
+        uint4 *t = reinterpret_cast<uint4 *>((kv ? v_cache : k_cache) + dst);
+        *t = __ldg(s);
+    }
+    __syncthreads();
+    if (tid == 0) prefix_lens[b] = P + a;                 // last: every row is written
+}
+
+}  // namespace
+
+cudaError_t launch_commit_kv(const Layout &L, const __nv_bfloat16 *tree_k, const __nv_bfloat16 *tree_v,
+                             const int32_t *n_nodes, const int32_t *accept_len, const int32_t *accept_path,
+                             __nv_bfloat16 *k_cache, __nv_bfloat16 *v_cache, int32_t *prefix_lens, int32_t max_depth,
+                             int32_t *status, cudaStream_t s) {
+    trace_begin("commit_kv", s);
+    commit_kv_kernel<<<L.B, kCommitThreads, 0, s>>>(tree_k, tree_v, n_nodes, accept_len, accept_path, k_cache, v_cache,
+                                                     prefix_lens, L.Nmax, L.Hkv, L.D, L.Pcap, max_depth, status);
+    cudaError_t e = cudaGetLastError();
+    trace_end(s);
+    return e;
+}
+
+}  // namespace jf

@@ -599,6 +599,10 @@ struct AttnArgs {
 cudaError_t launch_tree_attention(const Layout &L, const AttnMaps &m, const AttnArgs &a,
                                   cudaStream_t s);
 cudaError_t launch_split_combine(const Layout &L, const AttnArgs &a, cudaStream_t s);
+cudaError_t launch_commit_kv(const Layout &L, const __nv_bfloat16 *tree_k, const __nv_bfloat16 *tree_v,
+                             const int32_t *n_nodes, const int32_t *accept_len, const int32_t *accept_path,
+                             __nv_bfloat16 *k_cache, __nv_bfloat16 *v_cache, int32_t *prefix_lens, int32_t max_depth,
+                             int32_t *status, cudaStream_t s);
 cudaError_t launch_argmax(const Layout &L, const __nv_bfloat16 *logits, const int32_t *n_nodes,
                           uint8_t *ws, cudaStream_t s);
 cudaError_t launch_accept_walk(const Layout &L, const int32_t *tokens, const int32_t *parents,
