@@ -143,6 +143,24 @@ def test_long_ragged_prefixes_split_kv():
     check_attention(inp)
 
 
+@pytest.mark.parametrize("vscale", [1e5, 1e30])
+def test_values_beyond_fp16_in_split_units(vscale):
+    """V far beyond fp16's largest value (65504), on prefixes long enough
+    that every unit is split: the split pieces keep their rows in fp16
+    scaled by a power of two per half row, so split and whole units alike
+    must match the oracle (compared after dividing both by the scale)."""
+    inp = small_inputs(8, B=3, N=24, Hq=32, Hkv=8, d=128, Pcap=9000,
+                       prefixes=torch.tensor([9000, 1, 4097], dtype=torch.int32))
+    inp["v_cache"] = (inp["v_cache"].float() * vscale).to(torch.bfloat16)
+    inp["tree_v"] = (inp["tree_v"].float() * vscale).to(torch.bfloat16)
+    out, status = run_attention(to_dev(inp), shape_of(inp))
+    assert status == 0
+    got = out_f64(out)
+    assert np.isfinite(got[:, :24]).all()
+    ref = oracle_attention(inp)
+    assert_attention_close(got / vscale, ref / vscale, valid_rows(inp), f"V x {vscale:g}")
+
+
 def test_malformed_tree_flags_and_nans():
     inp = small_inputs(9, B=3, N=16, Pcap=100)
     inp["parents"][1, 5] = 7                           # parent not earlier

@@ -505,7 +505,7 @@ __device__ __forceinline__ void softmax_loop(const AttnMaps &maps, const Layout 
     const uint32_t t_row = tmem + ((uint32_t)(q * 32) << 16);
     const uint32_t t_o = t_row + C::kColO;
     __half *opart = reinterpret_cast<__half *>(a.ws + L.opart_off);
-    float2 *mlpart = reinterpret_cast<float2 *>(a.ws + L.ml_off);
+    float *mlpart = reinterpret_cast<float *>(a.ws + L.ml_off);   // (m, l, e0, e1) per piece row
     float *hand_q = hand + q * 64;
     const float sl2 = a.scale_log2;
     int ic = 0, g = 0, xc = 0, items = 0;
@@ -695,16 +695,26 @@ __device__ __forceinline__ void softmax_loop(const AttnMaps &maps, const Layout 
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(C::B_O_FREE));
-        // Final rows are bf16; the pieces of a split unit are fp16 rows already
-        // divided by their own l, with (m, l) beside them for the merge.
+        // Final rows are bf16. The pieces of a split unit are fp16 rows divided
+        // by their own l and scaled by 2^-e, e chosen per half row (this
+        // warp's columns) so that the largest magnitude lies in [2^14, 2^15):
+        // fp16's range then holds any bf16 value, and the merge multiplies by
+        // 2^e again. (m, l, e0, e1) go beside them.
         const bool split = info.ns > 1;
         const float inv_l = 1.0f / l_run;
+        int e_half = 0;
         // Scaled and packed in place: ov[2k] holds the pair for columns 2k, 2k+1.
         if (split) {
+            float amax = 0.f;
+#pragma unroll
+            for (int k = 0; k < kOHalf; ++k) amax = fmaxf(amax, fabsf(__uint_as_float(ov[k])));
+            amax *= inv_l;
+            if (amax > 0.f && amax <= 3.4e38f)
+                e_half = min(max(((__float_as_int(amax) >> 23) & 0xFF) - 127 - 14, -100), 100);
+            const float sc = inv_l * __int_as_float((127 - e_half) << 23);    // inv_l * 2^-e, exact
 #pragma unroll
             for (int e = 0; e < kOHalf / 2; ++e) {
-                const __half2 h = __floats2half2_rn(__uint_as_float(ov[2 * e]) * inv_l,
-                                                    __uint_as_float(ov[2 * e + 1]) * inv_l);
+                const __half2 h = __floats2half2_rn(__uint_as_float(ov[2 * e]) * sc, __uint_as_float(ov[2 * e + 1]) * sc);
                 ov[e] = *reinterpret_cast<const uint32_t *>(&h);
             }
         } else {
@@ -734,7 +744,14 @@ __device__ __forceinline__ void softmax_loop(const AttnMaps &maps, const Layout 
 #pragma unroll
             for (int k = 0; k < kOHalf / 8; ++k) dst[k] = pack8(k);
         }
-        if (split && par == 0) mlpart[(size_t)info.slot * kRows + r] = make_float2(m_fin, l_run);
+        if (split) {
+            float *rec = mlpart + 4 * ((size_t)info.slot * kRows + r);
+            if (par == 0) {
+                rec[0] = m_fin;
+                rec[1] = l_run;
+            }
+            rec[2 + par] = (float)e_half;
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(C::B_EPI));
         bool ok_epi = true;

@@ -8,9 +8,10 @@
 // has computed those rows without checking, and they are overwritten here.
 //
 // A work unit whose keys were split over several CTAs has, per split s, a
-// row o_s = O_s / l_s in fp16 plus (m_s, l_s) in fp32, with m in the exp2
+// row o_s = O_s / l_s in fp16, scaled by 2^-e per half row so that fp16
+// holds any bf16 magnitude, plus (m_s, l_s, e) in fp32, with m in the exp2
 // domain. The merged row is the log-sum-exp rescale:
-//   O = sum_s w_s o_s / sum_s w_s,   w_s = 2^(m_s - M) l_s,   M = max_s m_s.
+//   O = sum_s w_s 2^e o_s / sum_s w_s,   w_s = 2^(m_s - M) l_s,   M = max_s m_s.
 // The sums run in split order, so the result is deterministic.
 //
 // Grid (units, 128 / 16 rows), two rows per warp (16 lanes each, lane k
@@ -91,7 +92,7 @@ __global__ void __launch_bounds__(kCombineThreads, 4) split_combine_kernel(const
     // split s sits in slot 2c + 1 at c = c_first when the unit is not that
     // CTA's first item, else in slot 2c, c = c_first + s
     auto slot_of = [&](int sidx) { return 2 * (qi.c_first + sidx) + ((sidx == 0 && !qi.first_item) ? 1 : 0); };
-    const float2 *ml = reinterpret_cast<const float2 *>(a.ws + L.ml_off);
+    const float4 *ml = reinterpret_cast<const float4 *>(a.ws + L.ml_off);   // (m, l, e0, e1)
     const __half *op = reinterpret_cast<const __half *>(a.ws + L.opart_off);
     constexpr float kNegInf = -__builtin_huge_valf();
     // The first batch of O pieces is requested together with (m, l).
@@ -99,10 +100,12 @@ __global__ void __launch_bounds__(kCombineThreads, 4) split_combine_kernel(const
 #pragma unroll
     for (int k = 0; k < kCombineBatch; ++k)
         if (k < ns) v[k].load(op + ((size_t)slot_of(k) * kRows + r) * D + g * E);
-    // (m_s, l_s): lane g of the group holds split g (more are folded in below)
-    float2 mine = make_float2(kNegInf, 0.f);
-    if (g < ns) mine = __ldcg(&ml[(size_t)slot_of(g) * kRows + r]);
-    float M = mine.x;
+    // (m_s, l_s, e): lane g of the group holds split g (more are folded in
+    // below); e is the exponent of the half row that holds this lane's columns
+    const int half = (g * E) / (D / 2);
+    float4 rec = make_float4(kNegInf, 0.f, 0.f, 0.f);
+    if (g < ns) rec = __ldcg(&ml[(size_t)slot_of(g) * kRows + r]);
+    float M = rec.x;
     for (int s = kGroup + g; s < ns; s += kGroup) M = fmaxf(M, __ldcg(&ml[(size_t)slot_of(s) * kRows + r]).x);
 #pragma unroll
     for (int o = kGroup / 2; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(gmask, M, o));
@@ -122,18 +125,27 @@ __global__ void __launch_bounds__(kCombineThreads, 4) split_combine_kernel(const
         for (int k = 0; k < kCombineBatch; ++k) {          // weighted sums, in split order
             const int s = s0 + k;
             if (s < ns) {
-                const float2 mls = s < kGroup ? make_float2(__shfl_sync(gmask, mine.x, gbase + s),
-                                                            __shfl_sync(gmask, mine.y, gbase + s))
-                                              : __ldcg(&ml[(size_t)slot_of(s) * kRows + r]);
-                // the piece is O_s / l_s: its weight in the sum is 2^(m_s - M) l_s
-                const float w = ex2_approx(mls.x - M) * mls.y;
+                float4 r4;
+                if (s < kGroup) {
+                    r4.x = __shfl_sync(gmask, rec.x, gbase + s);
+                    r4.y = __shfl_sync(gmask, rec.y, gbase + s);
+                    r4.z = __shfl_sync(gmask, rec.z, gbase + s);
+                    r4.w = __shfl_sync(gmask, rec.w, gbase + s);
+                } else {
+                    r4 = __ldcg(&ml[(size_t)slot_of(s) * kRows + r]);
+                }
+                // the piece is O_s / (l_s 2^e): its weight in the sum is
+                // 2^(m_s - M) l_s, and its values count 2^e times
+                const float w = ex2_approx(r4.x - M) * r4.y;
                 Lsum += w;
+                const int eh = __float2int_rz(half ? r4.w : r4.z);
+                const float we = w * __int_as_float((127 + eh) << 23);            // w * 2^e, exact
 #pragma unroll
                 for (int e = 0; e < E / 2; ++e) {
                     const uint32_t h2 = v[k].word(e);
                     const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&h2));
-                    acc[2 * e] += w * f.x;
-                    acc[2 * e + 1] += w * f.y;
+                    acc[2 * e] += we * f.x;
+                    acc[2 * e + 1] += we * f.y;
                 }
             }
         }

@@ -96,8 +96,8 @@ inline Layout make_layout(int B, int Nmax, int Hq, int Hkv, int D, int Pcap, int
     size_t off = 0;
     auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 256); return o; };
     L.qtab_off = take(sizeof(QTile) * (size_t)L.n_qtiles);
-    L.ml_off = take(sizeof(float2) * (size_t)L.max_pieces * kRows);
-    L.opart_off = take(2 * (size_t)L.max_pieces * kRows * D);   // fp16 rows, already divided by their l
+    L.ml_off = take(sizeof(float4) * (size_t)L.max_pieces * kRows);   // (m, l, e0, e1)
+    L.opart_off = take(2 * (size_t)L.max_pieces * kRows * D);   // fp16 rows, divided by l, scaled by 2^-e per half
     L.amp_off = take(sizeof(int2) * (size_t)B * Nmax * L.chunks);
     L.total = off;
     return L;
