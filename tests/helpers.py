@@ -94,24 +94,34 @@ def half_ulp_bf16(x):
     return np.ldexp(1.0, np.floor(np.log2(ax)).astype(np.int64) - 8)
 
 
+# (what, max-abs error, mean-abs error, elements that needed the half-ulp
+# allowance) of every comparison in this process; printed at the end of a
+# run with JF_PARITY_REPORT=1 (tests/conftest.py).
+REPORT = []
+
+
 def assert_attention_close(got, ref, rows, what="", strict=False):
     """Element-wise comparison on the given (b, i) rows (all heads, all d).
 
     The bound is max-abs 1e-2 and mean-abs 1e-3 against fp64. The output is
-    bf16 by contract, and a row that sees only a few keys can have outputs
-    above 1 in magnitude, where bf16's half-ulp alone is 0.004-0.016. So
-    unless `strict`, each element may also differ by half a bf16 ulp of its
-    reference value. The five workloads run strict.
+    bf16 by contract: where |ref| >= 1, bf16's half-ulp alone (0.0039 and
+    up) takes a large part of that budget, on top of the bf16 rounding of
+    the attention weights that feed the PV product (few keys: it does not
+    average out). So unless `strict`, those elements (and only those) may
+    also differ by half a bf16 ulp of their reference value. Rows that see
+    few keys reach such magnitudes; the five workloads stay far below and
+    run strict.
     """
     g = np.stack([got[b, i] for b, i in rows]).astype(np.float64)
     r = np.stack([ref[b, i] for b, i in rows])
     assert np.isfinite(g).all(), f"{what}: non-finite output"
     err = np.abs(g - r)
-    bound = ATOL_MAX if strict else ATOL_MAX + half_ulp_bf16(r)
+    bound = ATOL_MAX if strict else ATOL_MAX + np.where(np.abs(r) >= 1.0, half_ulp_bf16(r), 0.0)
     worst = np.unravel_index(np.argmax(err - bound), err.shape)
     assert (err <= bound).all(), (f"{what}: |err| {err[worst]:.3e} > bound {np.broadcast_to(bound, err.shape)[worst]:.3e}"
                                   f" at row {rows[worst[0]]}, head {worst[1]}, d {worst[2]} (ref {r[worst]:.4f})")
     assert err.mean() <= ATOL_MEAN, f"{what}: mean-abs {err.mean():.3e} > {ATOL_MEAN}"
+    REPORT.append((what, float(err.max()), float(err.mean()), int((err > ATOL_MAX).sum())))
     return float(err.max()), float(err.mean())
 
 
