@@ -57,6 +57,14 @@ def _load():
             lib.oracle_tree_is_valid.restype = ctypes.c_int
             lib.oracle_commit_kv.argtypes = [P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, P]
             lib.oracle_commit_kv.restype = None
+            u64 = ctypes.c_uint64
+            lib.oracle_philox4x64_10.argtypes = [P, P, P]
+            lib.oracle_philox4x64_10.restype = None
+            lib.oracle_uniform.argtypes = [u64, u64, ctypes.c_uint32, i32, i64]
+            lib.oracle_uniform.restype = f64
+            lib.oracle_tree_verify_sample.argtypes = [P, P, P, P, P, i32, i32, i64, i32, f64, u64, u64,
+                                                      P, P, P, P]
+            lib.oracle_tree_verify_sample.restype = None
             _lib = lib
     return _lib
 
@@ -154,3 +162,40 @@ def commit_kv(tree_k, tree_v, n_nodes, accept_len, accept_path, k_cache, v_cache
     lib.oracle_commit_kv(_ptr(tk), _ptr(tv), _ptr(nn), _ptr(al), _ptr(ap), _ptr(kc), _ptr(vc), _ptr(pl),
                          B, Nmax, Hkv, d, Pcap, int(max_depth), _ptr(flags))
     return kc, vc, pl, flags
+
+
+def philox4x64_10(counter, key) -> np.ndarray:
+    """One Philox4x64-10 block: 4 uint64 words for a 4-word counter and a
+    2-word key."""
+    c = np.ascontiguousarray(np.asarray(counter, dtype=np.uint64).reshape(4))
+    k = np.ascontiguousarray(np.asarray(key, dtype=np.uint64).reshape(2))
+    out = np.empty(4, dtype=np.uint64)
+    _load().oracle_philox4x64_10(_ptr(c), _ptr(k), _ptr(out))
+    return out
+
+
+def uniform(seed: int, offset: int, purpose: int, b: int, index: int) -> float:
+    """The uniform in (0, 1) of stream `purpose` (0: acceptance, 1: sampling)
+    for sequence b and item `index`."""
+    return float(_load().oracle_uniform(seed, offset, purpose, b, index))
+
+
+def tree_verify_sample(target_logits, draft_logits, tokens, parents, n_nodes, max_depth: int,
+                       temperature: float, seed: int, offset: int):
+    """Stochastic tree verification. Returns (accept_len [B], accept_path
+    [B, max_depth+1], next_token [B], margins [B, 3]) where margins holds
+    the smallest acceptance-test margin, the smallest residual mass and the
+    Gumbel top-2 gap of each sequence."""
+    lib = _load()
+    tg, dr = _u16(target_logits), _u16(draft_logits)
+    B, N, V = tg.shape
+    assert dr.shape == tg.shape
+    tok, par, nn = _i32(tokens), _i32(parents), _i32(n_nodes)
+    alen = np.empty(B, dtype=np.int32)
+    path = np.empty((B, max_depth + 1), dtype=np.int32)
+    nxt = np.empty(B, dtype=np.int32)
+    margins = np.empty((B, 3), dtype=np.float64)
+    lib.oracle_tree_verify_sample(_ptr(tg), _ptr(dr), _ptr(tok), _ptr(par), _ptr(nn), B, N, V, max_depth,
+                                  float(temperature), int(seed), int(offset), _ptr(alen), _ptr(path),
+                                  _ptr(nxt), _ptr(margins))
+    return alen, path, nxt, margins

@@ -35,7 +35,13 @@
  * values (closed form); relabelling or deleting non-ancestor nodes leaves a
  * node's output bit-identical; torch.argmax; brute-force path enumeration
  * on every tree with up to 6 nodes; hand-worked walk cases in
- * tests/golden/walk_cases.txt.
+ * tests/golden/walk_cases.txt; hand-worked KV-commit cases in
+ * tests/golden/commit_cases.txt. Stochastic verification
+ * (tests/test_oracle_sample_pins.py): Philox4x64-10 word for word against
+ * numpy's Philox generator; the emitted tokens' distribution equals the
+ * target's (chi-square) when children are drawn from the draft, at the
+ * root and one level down; draft = target accepts every first child; a
+ * near-zero temperature with a flat draft gives the greedy walk.
  */
 #include <math.h>
 #include <stdint.h>
@@ -296,4 +302,176 @@ void oracle_commit_kv(const uint16_t *tree_k, const uint16_t *tree_v, const int3
         }
         prefix_lens[b] = P + a;
     }
+}
+
+/*
+ * Philox4x64-10, the counter-based generator of Salmon, Moraes, Dror and
+ * Shaw, "Parallel random numbers: as easy as 1, 2, 3" (SC 2011): ten
+ * rounds of two 64 x 64 -> 128-bit products on a 4-word counter, with the
+ * 2-word key bumped by two Weyl constants after every round.
+ */
+void oracle_philox4x64_10(const uint64_t *ctr_in, const uint64_t *key, uint64_t *out)
+{
+    const uint64_t M0 = 0xD2E7470EE14C6C93ull, M1 = 0xCA5A826395121157ull;
+    const uint64_t W0 = 0x9E3779B97F4A7C15ull, W1 = 0xBB67AE8584CAA73Bull;
+    uint64_t c[4] = {ctr_in[0], ctr_in[1], ctr_in[2], ctr_in[3]};
+    uint64_t k0 = key[0], k1 = key[1];
+    for (int round = 0; round < 10; ++round) {
+        const unsigned __int128 p0 = (unsigned __int128)M0 * c[0];
+        const unsigned __int128 p1 = (unsigned __int128)M1 * c[2];
+        const uint64_t hi0 = (uint64_t)(p0 >> 64), lo0 = (uint64_t)p0;
+        const uint64_t hi1 = (uint64_t)(p1 >> 64), lo1 = (uint64_t)p1;
+        const uint64_t n0 = hi1 ^ c[1] ^ k0, n2 = hi0 ^ c[3] ^ k1;
+        c[0] = n0;
+        c[1] = lo1;
+        c[2] = n2;
+        c[3] = lo0;
+        k0 += W0;
+        k1 += W1;
+    }
+    for (int i = 0; i < 4; ++i) out[i] = c[i];
+}
+
+/*
+ * The uniform number of stream `purpose` (0: acceptance tests, one per
+ * node; 1: the Gumbel noise of the final sample, one per vocabulary entry)
+ * for sequence b and item `index`: word index % 4 of the Philox block at
+ * counter (index / 4, b, purpose, 0) under key (seed, offset), its top 23
+ * bits as (k + 1/2) * 2^-23, strictly inside (0, 1).
+ */
+double oracle_uniform(uint64_t seed, uint64_t offset, uint32_t purpose, int32_t b, int64_t index)
+{
+    const uint64_t ctr[4] = {(uint64_t)index / 4, (uint64_t)(uint32_t)b, purpose, 0};
+    const uint64_t key[2] = {seed, offset};
+    uint64_t out[4];
+    oracle_philox4x64_10(ctr, key, out);
+    const uint64_t w = out[index % 4];
+    return ((double)(w >> 41) + 0.5) * ldexp(1.0, -23);
+}
+
+/* softmax(z / T) of one bf16 logits row, in double. */
+static void softmax_row(const uint16_t *z, int64_t V, double T, double *p)
+{
+    double m = -INFINITY;
+    for (int64_t v = 0; v < V; ++v) {
+        const double x = bf16_to_double(z[v]) / T;
+        if (x > m) m = x;
+    }
+    double s = 0.0;
+    for (int64_t v = 0; v < V; ++v) {
+        p[v] = exp(bf16_to_double(z[v]) / T - m);
+        s += p[v];
+    }
+    for (int64_t v = 0; v < V; ++v) p[v] /= s;
+}
+
+/*
+ * Stochastic tree verification at temperature T > 0: speculative sampling
+ * ([paper] section 2.1 cites Leviathan et al. 2023 for the draft-then-verify
+ * rule) applied at every accepted node to its children in index order.
+ *
+ * For sequence b, p_u = softmax(target[b][u] / T) is the target's
+ * distribution after node u's path and q_u = softmax(draft[b][u] / T) the
+ * draft's distribution from which u's children were drawn. Starting with
+ * u = root and r = p_u, each child c of u (index order) with token x is
+ * accepted iff U(c) < min(1, r(x) / q_u(x)), U(c) the acceptance uniform of
+ * node c; on acceptance the walk moves to c with r = p_c. A rejected child
+ * replaces r by the residual max(r - q_u, 0) / sum(max(r - q_u, 0)); if that
+ * sum is 0 the remaining children are rejected and r = p_u. The walk also
+ * stops at depth max_depth. The next token is then drawn from r by the
+ * Gumbel-max rule: the v with r(v) > 0 maximising log r(v) + g(v),
+ * g(v) = -log(-log U(v)) with U(v) the sampling uniform of entry v, the
+ * lowest index on ties.
+ *
+ * Outputs: accept_len[b] (path nodes, root included), accept_path[b]
+ * (root first, -1 padded), next_token[b]. A malformed tree gives 0, all -1
+ * and -1. margins (may be NULL) gets per sequence the smallest
+ * |U - min(1, ratio)| of the acceptance tests, the smallest residual mass,
+ * and the gap between the two largest Gumbel keys, so that a test can tell
+ * decisions that another precision could take differently (1 where none).
+ */
+void oracle_tree_verify_sample(const uint16_t *target, const uint16_t *draft, const int32_t *tokens,
+                               const int32_t *parents, const int32_t *n_nodes, int32_t B, int32_t Nmax,
+                               int64_t V, int32_t max_depth, double temperature, uint64_t seed,
+                               uint64_t offset, int32_t *accept_len, int32_t *accept_path,
+                               int32_t *next_token, double *margins)
+{
+    double *p = (double *)malloc(sizeof(double) * (size_t)V);
+    double *q = (double *)malloc(sizeof(double) * (size_t)V);
+    double *r = (double *)malloc(sizeof(double) * (size_t)V);
+    for (int32_t b = 0; b < B; ++b) {
+        const int32_t *par = parents + (int64_t)b * Nmax;
+        const int32_t *tok = tokens + (int64_t)b * Nmax;
+        const int32_t n = n_nodes[b];
+        int32_t *path = accept_path + (int64_t)b * (max_depth + 1);
+        for (int32_t k = 0; k <= max_depth; ++k) path[k] = -1;
+        double m_acc = 1.0, m_mass = 1.0, m_gap = 1.0;
+        if (!oracle_tree_is_valid(par, n, Nmax)) {
+            accept_len[b] = 0;
+            next_token[b] = -1;
+            if (margins) margins[3 * b] = margins[3 * b + 1] = margins[3 * b + 2] = 1.0;
+            continue;
+        }
+        int32_t u = 0, depth = 0;
+        path[0] = 0;
+        for (;;) {
+            const int64_t row = ((int64_t)b * Nmax + u) * V;
+            softmax_row(target + row, V, temperature, p);
+            for (int64_t v = 0; v < V; ++v) r[v] = p[v];
+            int32_t next = -1;
+            if (depth < max_depth) {
+                softmax_row(draft + row, V, temperature, q);
+                for (int32_t c = u + 1; c < n && next < 0; ++c) {
+                    if (par[c] != u) continue;
+                    const int32_t x = tok[c];
+                    double ratio = (x >= 0 && x < V) ? (q[x] > 0.0 ? r[x] / q[x] : (r[x] > 0.0 ? 1.0 : 0.0)) : 0.0;
+                    if (ratio > 1.0) ratio = 1.0;
+                    const double U = oracle_uniform(seed, offset, 0, b, c);
+                    if (fabs(U - ratio) < m_acc) m_acc = fabs(U - ratio);
+                    if (U < ratio) {
+                        next = c;
+                        break;
+                    }
+                    double s = 0.0;
+                    for (int64_t v = 0; v < V; ++v) {
+                        r[v] = r[v] > q[v] ? r[v] - q[v] : 0.0;
+                        s += r[v];
+                    }
+                    if (s < m_mass) m_mass = s;
+                    if (!(s > 0.0)) {           /* the residual vanished */
+                        for (int64_t v = 0; v < V; ++v) r[v] = p[v];
+                        break;
+                    }
+                    for (int64_t v = 0; v < V; ++v) r[v] /= s;
+                }
+            }
+            if (next < 0) break;
+            u = next;
+            path[++depth] = u;
+        }
+        double best = -INFINITY, second = -INFINITY;
+        int32_t arg = -1;
+        for (int64_t v = 0; v < V; ++v) {
+            if (!(r[v] > 0.0)) continue;
+            const double key = log(r[v]) - log(-log(oracle_uniform(seed, offset, 1, b, v)));
+            if (key > best) {
+                second = best;
+                best = key;
+                arg = (int32_t)v;
+            } else if (key > second) {
+                second = key;
+            }
+        }
+        if (arg >= 0 && second > -INFINITY) m_gap = best - second;
+        accept_len[b] = depth + 1;
+        next_token[b] = arg;
+        if (margins) {
+            margins[3 * b] = m_acc;
+            margins[3 * b + 1] = m_mass;
+            margins[3 * b + 2] = m_gap;
+        }
+    }
+    free(p);
+    free(q);
+    free(r);
 }
