@@ -285,6 +285,16 @@ class Calls:
         self.pl_slots = self.pl_saved.clone()
         self.c_alen = torch.empty_like(self.alen)
         self.c_path = torch.empty_like(self.path)
+        # stochastic verification: target and draft logits with trees whose
+        # tokens a sampling draft proposed, rotated like the other inputs
+        sinp = synth.make_sample_inputs(w)
+        snames = ["target_logits", "draft_logits", "tokens", "parents", "n_nodes"]
+        self.sample_bytes = sum(sinp[k].numel() * sinp[k].element_size() for k in snames)
+        self.RS = min(G, max(2, math.ceil(3 * L2_BYTES / self.sample_bytes)))
+        self.scopies = [{k: sinp[k].to(dev) for k in snames} for _ in range(self.RS)]
+        self.s_next = torch.empty(B, dtype=torch.int32, device=dev)
+        self.s_alen = torch.empty_like(self.alen)
+        self.s_path = torch.empty_like(self.path)
 
     def attn(self, i):
         c = self.acopies[i % self.RA]
@@ -309,6 +319,12 @@ class Calls:
         self.jb.jf_tree_commit_kv(c["tree_k"], c["tree_v"], c["n_nodes"], self.c_alen, self.c_path, self.kc, self.vc,
                                   self.pl_slots[i % self.G], self.shape_c, MAX_DEPTH, status=self.status)
 
+    def sample(self, i):
+        c = self.scopies[i % self.RS]
+        self.jb.jf_tree_verify_sample(c["target_logits"], c["draft_logits"], c["tokens"], c["parents"], c["n_nodes"],
+                                      1.0, 1234, i, self.s_alen, self.s_path, self.s_next, self.shape, MAX_DEPTH,
+                                      self.ws, status=self.status)
+
     def warm(self, n):
         for i in range(n):
             self.step(i)
@@ -321,6 +337,7 @@ class Calls:
         for i in range(min(n, self.G)):
             self.attn(i)
             self.commit(i)
+            self.sample(i)
         self.torch.cuda.synchronize()
         assert int(self.status.item()) == 0, f"{self.w.name}: device status flag raised by the commit"
 
@@ -338,7 +355,7 @@ class Calls:
         rows = int(self.inp["planted_len"].sum())
         return 2 * 2 * rows * Hkv * d * 2 + 4 * self.B * (MAX_DEPTH + 4)
 
-    def rooflines(self, attn_ms, verify_ms, commit_ms, pk, synth):
+    def rooflines(self, attn_ms, verify_ms, commit_ms, pk, synth, sample_ms=None):
         inp, w = self.inp, self.w
         flops = synth.attention_flops(inp["parents"], inp["n_nodes"], inp["prefix_lens"], w.n_q_heads, w.head_dim)
         abytes = synth.attention_bytes(inp["prefix_lens"], inp["n_nodes"], w.n_q_heads, w.n_kv_heads, w.head_dim)
@@ -356,6 +373,10 @@ class Calls:
             "verify_hbm_frac": vbytes / (verify_ms * 1e-3) / (pk["hbm_gbs"] * 1e9),
             "verify_nodes_per_s": nodes / (verify_ms * 1e-3), "verify_bytes": vbytes,
             "commit_us": commit_ms * 1e3, "commit_gbs": cbytes / (commit_ms * 1e-3) / 1e9, "commit_bytes": cbytes,
+            **({} if sample_ms is None else {
+                "sample_us": sample_ms * 1e3, "sample_bytes": 2 * vbytes,
+                "sample_gbs": 2 * vbytes / (sample_ms * 1e-3) / 1e9,
+                "sample_hbm_frac": 2 * vbytes / (sample_ms * 1e-3) / (pk["hbm_gbs"] * 1e9)}),
         }
 
 
@@ -404,7 +425,7 @@ def run_gpu(args, rank, world, local):
     launches0 = jb.jf_kernel_launch_count()
     graph = H.graph(H.step)
     launches_per_step = (jb.jf_kernel_launch_count() - launches0) / G
-    g_attn, g_verify, g_commit = H.graph(H.attn), H.graph(H.verify), H.graph(H.commit)
+    g_attn, g_verify, g_commit, g_sample = H.graph(H.attn), H.graph(H.verify), H.graph(H.commit), H.graph(H.sample)
     max_kernels = 8
     events = [torch.cuda.Event(enable_timing=True) for _ in range(2 * max_kernels * G)]
     jb.jf_trace_kernels(events, max_kernels * G)
@@ -412,7 +433,7 @@ def run_gpu(args, rank, world, local):
     n_traced = jb.jf_trace_count()
     trace_names = [jb.jf_trace_name(k) for k in range(n_traced)]
     jb.jf_trace_kernels(None, 0)
-    for g in (graph, g_attn, g_verify, g_commit, traced):      # untimed
+    for g in (graph, g_attn, g_verify, g_commit, g_sample, traced):      # untimed
         g.replay()
     torch.cuda.synchronize()
 
@@ -420,15 +441,16 @@ def run_gpu(args, rank, world, local):
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize()
-        t_step, t_attn, t_verify, t_commit = time_graphs([graph, g_attn, g_verify, g_commit], M, torch)
+        t_step, t_attn, t_verify, t_commit, t_sample = time_graphs([graph, g_attn, g_verify, g_commit, g_sample], M,
+                                                                   torch)
         traced.replay()
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
     clocks = clk.summary()
     assert int(H.status.item()) == 0, "device status flag raised in the timed region"
-    total_ms, attn_ms, verify_ms, commit_ms = max_over_ranks(
-        [t_step, t_attn / K, t_verify / K, t_commit / K], world, dev)
+    total_ms, attn_ms, verify_ms, commit_ms, sample_ms = max_over_ranks(
+        [t_step, t_attn / K, t_verify / K, t_commit / K, t_sample / K], world, dev)
 
     # per-kernel durations of the traced replay: each includes its launch
     # gap after the previous event, without programmatic overlap
@@ -490,7 +512,7 @@ def run_gpu(args, rank, world, local):
     e2e_ms = max_over_ranks([e0.elapsed_time(e1)], world, dev)[0]
     assert h_alen.tolist() == H.inp["planted_len"].tolist()
 
-    head = H.rooflines(attn_ms, verify_ms, commit_ms, pk, synth)
+    head = H.rooflines(attn_ms, verify_ms, commit_ms, pk, synth, sample_ms)
     head["step_us"] = total_ms * 1e3 / K
     traffic = stored_traffic()
     cpu = time_oracle(H.inp, target_s=args.cpu_seconds) if rank == 0 else None
@@ -503,7 +525,7 @@ def run_gpu(args, rank, world, local):
     if args.configs:
         Kc = min(K, args.config_steps)
         Gc = graph_size(Kc)
-        del graph, g_attn, g_verify, g_commit, traced
+        del graph, g_attn, g_verify, g_commit, g_sample, traced
         with ClockSampler(local) as clk2:
             for name, wc in synth.WORKLOADS.items():
                 if name == args.workload:
@@ -512,7 +534,7 @@ def run_gpu(args, rank, world, local):
                 else:
                     Hc = Calls(wc, dev, Gc, torch, jb, synth)
                     Hc.warm(3)
-                    gs = [Hc.graph(f) for f in (Hc.step, Hc.attn, Hc.verify, Hc.commit)]
+                    gs = [Hc.graph(f) for f in (Hc.step, Hc.attn, Hc.verify, Hc.commit, Hc.sample)]
                     for g in gs:
                         g.replay()
                     torch.cuda.synchronize()
@@ -521,7 +543,7 @@ def run_gpu(args, rank, world, local):
                     ts = time_graphs(gs, Kc // Gc, torch)
                     assert int(Hc.status.item()) == 0, f"{name}: device status flag raised"
                     ts = max_over_ranks([t / Kc for t in ts], world, dev)
-                    rec = Hc.rooflines(ts[1], ts[2], ts[3], pk, synth)
+                    rec = Hc.rooflines(ts[1], ts[2], ts[3], pk, synth, ts[4])
                     rec.update({"step_us": ts[0] * 1e3, "steps": Kc,
                                 "l2": f"inputs rotate over {Hc.R} device copies "
                                       f"({Hc.R * Hc.step_bytes / 2**20:.0f} MB); attention-only calls over "
@@ -548,9 +570,10 @@ def run_gpu(args, rank, world, local):
                           "note": "all replicas together; value and e2e are per step of one replica "
                                   "(the slowest rank)"},
             "attn_us": head["attn_us"], "verify_us": head["verify_us"], "commit_us": head["commit_us"],
-            "call_timing": "graphs of back-to-back jf_tree_attention calls, of jf_tree_verify calls and of "
-                           "jf_tree_commit_kv calls, K each, events on the launch stream, same clock window "
-                           "as the steps",
+            "sample_us": head["sample_us"],
+            "call_timing": "graphs of back-to-back jf_tree_attention calls, of jf_tree_verify calls, of "
+                           "jf_tree_commit_kv calls and of jf_tree_verify_sample calls (T = 1, a new Philox "
+                           "offset each), K each, events on the launch stream, same clock window as the steps",
             "kernel_us": {n: v * 1e3 for n, v in avg.items()},
             "kernel_timing": "event pair around each kernel in a traced copy of the step graph; each figure "
                              "includes the kernel's launch gap and loses the programmatic overlap",

@@ -184,6 +184,55 @@ JF_API int32_t jf_tree_verify(const void *logits, const int32_t *tree_tokens,
                               jf_stream_t stream);
 
 /*
+ * Stochastic tree verification at temperature T > 0: speculative sampling
+ * (the paper's section 2.1 "Background" cites Leviathan et al. 2023 for the
+ * draft-then-verify rule) applied along the tree.
+ *
+ * For sequence b, p_u = softmax(target_logits[b, u] / T) is the target's
+ * distribution after node u's path and q_u = softmax(draft_logits[b, u] / T)
+ * the draft's distribution from which u's children were drawn. From the
+ * root, with r = p_u, each child c of the current node u (index order)
+ * with token x = tree_tokens[b, c] is accepted iff U(c) < min(1, r(x) /
+ * q_u(x)); the walk then moves to c with r = p_c. A rejected child replaces
+ * r by max(r - q_u, 0) renormalised; if that residual is 0 everywhere the
+ * remaining children are rejected and r = p_u. The walk stops at a node
+ * with no accepted child or at depth max_depth, and next_token_out[b] is
+ * drawn from r by the Gumbel-max rule: the v with r(v) > 0 maximising
+ * ln r(v) - ln(-ln U'(v)), the lowest index on ties. A token outside
+ * [0, V) is always rejected.
+ *
+ * Random numbers: Philox4x64-10 (Salmon et al., "Parallel random numbers:
+ * as easy as 1, 2, 3", SC 2011) under the key (seed, offset). U(c) is word
+ * c % 4 of the block at counter (c / 4, b, 0, 0); U'(v) is word v % 4 of
+ * the block at counter (v / 4, b, 1, 0); a word w gives the uniform
+ * (floor(w / 2^41) + 1/2) / 2^23. Pass a new offset (e.g. the decoding
+ * step) for fresh numbers. The arithmetic is fp32 (normalisers from
+ * chunked sums), so a decision whose margin is within rounding of fp32
+ * may differ from an exact evaluation.
+ *
+ *   target_logits, draft_logits  bf16 [B, Nmax, V], finite values
+ *   tree_tokens, parents, n_nodes as for jf_tree_verify
+ *   temperature      > 0 and finite, else JF_ERR_SHAPE
+ *   seed, offset     the Philox key
+ *   accept_len_out   int32 [B]: path nodes including the root (>= 1),
+ *                    0 for a malformed tree
+ *   accept_path_out  int32 [B, max_depth + 1], root first, -1 padded
+ *   next_token_out   int32 [B]: the token sampled after the path, -1 for a
+ *                    malformed tree
+ *   max_depth        >= 0: the walk goes no deeper
+ * The workspace is the one jf_workspace_bytes(shape) sizes. Each sequence
+ * is walked by a cluster of 8 CTAs. Returns as jf_tree_verify; a malformed
+ * tree raises JF_STATUS_BAD_TREE.
+ */
+JF_API int32_t jf_tree_verify_sample(const void *target_logits, const void *draft_logits,
+                                     const int32_t *tree_tokens, const int32_t *parents,
+                                     const int32_t *n_nodes, float temperature, uint64_t seed,
+                                     uint64_t offset, int32_t *accept_len_out,
+                                     int32_t *accept_path_out, int32_t *next_token_out,
+                                     const jf_shape *shape, int32_t max_depth, void *workspace,
+                                     size_t workspace_bytes, int32_t *status, jf_stream_t stream);
+
+/*
  * Accepted-path KV commit: the step after verification (the paper's section
  * 2.1 "Background": the prefix the target accepts extends the context). The
  * keys and values of the accepted nodes were computed by this tree's

@@ -68,14 +68,16 @@ def test_argmax_chunks_on_152_sms(rows, V, expect):
                                           (2, 5, 151936, 75), (1, 16, 1024, 1), (4, 200, 262144, 4),
                                           (1, 152, 151936, 6)])
 def test_argmax_chunk_rule(lib, B, N, V, expect):
-    """The verify region of the workspace holds one int2 per (row, chunk):
-    its growth from a one-chunk vocabulary pins the chunk count it is sized
-    for (256 SMs, the bound for any device's chunking)."""
+    """The verify region of the workspace holds one int2 per (row, chunk),
+    and the sampling region two float2 (target and draft): their growth from
+    a one-chunk vocabulary pins the chunk count they are sized for (256 SMs,
+    the bound for any device's chunking)."""
     assert _argmax_chunks(B * N, V) == expect
     align = lambda x: -(-x // 256) * 256
     base = jb.jf_workspace_bytes(jb.make_shape(B, 0, 0, 0, N, 0, 8))
     ws = jb.jf_workspace_bytes(jb.make_shape(B, 0, 0, 0, N, 0, V))
-    assert ws - base == align(B * N * expect * 8) - align(B * N * 8)
+    rows = B * N
+    assert ws - base == (align(rows * expect * 8) + align(2 * rows * expect * 8)) - (align(rows * 8) + align(2 * rows * 8))
 
 
 A16 = 1 << 20            # fake 16-byte-aligned addresses: never dereferenced
@@ -146,6 +148,42 @@ def test_verify_bad_depth_alignment_workspace(lib):
     assert verify(s, ws_bytes=jb.jf_workspace_bytes(s) - 1) == jb.JF_ERR_WORKSPACE
 
 
+def sample(shape, max_depth=16, temperature=1.0, ws_bytes=None, **over):
+    args = dict(target=A16, draft=A16, tokens=A16, parents=A16, n_nodes=A16, alen=A16, path=A16, nxt=A16,
+                workspace=A16 * 2)
+    args.update(over)
+    if ws_bytes is None:
+        ws_bytes = jb.jf_workspace_bytes(shape)
+    return jb.jf_tree_verify_sample(args["target"], args["draft"], args["tokens"], args["parents"], args["n_nodes"],
+                                    temperature, 1, 0, args["alen"], args["path"], args["nxt"], shape, max_depth,
+                                    args["workspace"], ws_bytes, stream=0, check=False)
+
+
+@pytest.mark.parametrize("name", ["target", "draft", "tokens", "parents", "n_nodes", "alen", "path", "nxt",
+                                  "workspace"])
+def test_sample_null_pointer(lib, name):
+    assert sample(good_shape(), **{name: None}) == jb.JF_ERR_NULL
+
+
+@pytest.mark.parametrize("bad", [dict(vocab=0), dict(vocab=1001), dict(max_nodes=257), dict(batch=0)])
+def test_sample_bad_shape(lib, bad):
+    assert sample(good_shape(**bad)) == jb.JF_ERR_SHAPE
+
+
+@pytest.mark.parametrize("T", [0.0, -1.0, float("nan"), float("inf")])
+def test_sample_bad_temperature(lib, T):
+    assert sample(good_shape(), temperature=T) == jb.JF_ERR_SHAPE
+
+
+def test_sample_depth_alignment_workspace(lib):
+    s = good_shape()
+    assert sample(s, max_depth=-1) == jb.JF_ERR_SHAPE
+    assert sample(s, target=A16 + 2) == jb.JF_ERR_ALIGN
+    assert sample(s, draft=A16 + 8) == jb.JF_ERR_ALIGN
+    assert sample(s, workspace=A16 + 16) == jb.JF_ERR_ALIGN
+    assert sample(s, ws_bytes=jb.jf_workspace_bytes(s) - 1) == jb.JF_ERR_WORKSPACE
+
+
 def commit(shape, max_depth=16, **over):
     args = dict(tree_k=A16, tree_v=A16, n_nodes=A16, alen=A16, path=A16, k_cache=A16, v_cache=A16,
                 prefix_lens=A16)
@@ -184,3 +222,14 @@ def test_trace_arm_disarm_without_gpu(lib):
     assert jb.jf_trace_count() == 0
     assert jb.jf_trace_name(0) is None
     assert jb.jf_kernel_launch_count() == 0   # nothing was launched on this machine
+
+
+def test_binding_refuses_strided_tensors(lib):
+    """Every array is read as dense row-major memory: the binding refuses a
+    tensor with other strides instead of passing its address."""
+    import torch
+    t = torch.zeros(4, 8, dtype=torch.bfloat16).t()
+    assert not t.is_contiguous()
+    with pytest.raises(ValueError):
+        jb.jf_tree_verify(t, A16, A16, A16, A16, A16, None, good_shape(), 4, A16 * 2, workspace_bytes=1 << 30,
+                          stream=0, check=False)

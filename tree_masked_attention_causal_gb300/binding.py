@@ -77,6 +77,10 @@ def _configure(lib: ctypes.CDLL) -> ctypes.CDLL:
         lib.jf_tree_verify_noalloc.restype = i32
         lib.jf_tree_commit_kv.argtypes = [P, P, P, P, P, P, P, P, sp, i32, P, P]
         lib.jf_tree_commit_kv.restype = i32
+        u64 = ctypes.c_uint64
+        lib.jf_tree_verify_sample.argtypes = [P, P, P, P, P, ctypes.c_float, u64, u64, P, P, P, sp, i32, P, sz,
+                                              P, P]
+        lib.jf_tree_verify_sample.restype = i32
     return lib
 
 
@@ -91,10 +95,15 @@ def make_shape(batch, n_q_heads, n_kv_heads, head_dim, max_nodes, prefix_cap, vo
 
 
 def _ptr(t) -> Optional[int]:
+    """The address of a tensor's first element. The library reads every
+    array as dense row-major memory, so a tensor with other strides is
+    refused rather than read wrongly."""
     if t is None:
         return None
     if isinstance(t, int):
         return t
+    if not t.is_contiguous():
+        raise ValueError("jf_tree: tensor arguments must be contiguous (row-major)")
     return t.data_ptr()
 
 
@@ -142,6 +151,23 @@ def jf_tree_verify(logits, tree_tokens, parents, n_nodes, accept_len_out, accept
                                _ptr(status), _stream(stream))
     if check and rc != JF_OK:
         raise JfError("jf_tree_verify", rc)
+    return rc
+
+
+def jf_tree_verify_sample(target_logits, draft_logits, tree_tokens, parents, n_nodes, temperature: float,
+                          seed: int, offset: int, accept_len_out, accept_path_out, next_token_out, shape: JfShape,
+                          max_depth: int, workspace, workspace_bytes: Optional[int] = None, status=None,
+                          stream=None, check: bool = True) -> int:
+    """Stochastic tree verification by speculative sampling (see jf_tree.h)."""
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    rc = load().jf_tree_verify_sample(_ptr(target_logits), _ptr(draft_logits), _ptr(tree_tokens), _ptr(parents),
+                                      _ptr(n_nodes), float(temperature), int(seed) & (2 ** 64 - 1),
+                                      int(offset) & (2 ** 64 - 1), _ptr(accept_len_out), _ptr(accept_path_out),
+                                      _ptr(next_token_out), ctypes.byref(shape), int(max_depth), _ptr(workspace),
+                                      int(workspace_bytes), _ptr(status), _stream(stream))
+    if check and rc != JF_OK:
+        raise JfError("jf_tree_verify_sample", rc)
     return rc
 
 

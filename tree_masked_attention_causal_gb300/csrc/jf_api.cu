@@ -253,6 +253,46 @@ JF_API int32_t jf_tree_verify(const void *logits, const int32_t *tree_tokens, co
     return JF_OK;
 }
 
+JF_API int32_t jf_tree_verify_sample(const void *target_logits, const void *draft_logits, const int32_t *tree_tokens,
+                                     const int32_t *parents, const int32_t *n_nodes, float temperature,
+                                     uint64_t seed, uint64_t offset, int32_t *accept_len_out,
+                                     int32_t *accept_path_out, int32_t *next_token_out, const jf_shape *shape,
+                                     int32_t max_depth, void *workspace, size_t workspace_bytes, int32_t *status,
+                                     jf_stream_t stream) {
+    if (!target_logits || !draft_logits || !tree_tokens || !parents || !n_nodes || !accept_len_out ||
+        !accept_path_out || !next_token_out || !shape || !workspace)
+        return JF_ERR_NULL;
+    const int32_t sc = check_shape(shape, true, false);
+    if (sc != JF_OK) return sc;
+    if (max_depth < 0 || !(temperature > 0.0f) || isinf(temperature)) return JF_ERR_SHAPE;
+    if (!aligned16(target_logits) || !aligned16(draft_logits) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return JF_ERR_ALIGN;
+    if (workspace_bytes < jf_workspace_bytes(shape)) return JF_ERR_WORKSPACE;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return JF_ERR_CUDA;
+    const int sms = num_sms_cached(dev);
+    if (sms <= 0) return JF_ERR_CUDA;
+    const Layout L = layout_of(shape, sms);
+    SampleArgs a{};
+    a.target = reinterpret_cast<const __nv_bfloat16 *>(target_logits);
+    a.draft = reinterpret_cast<const __nv_bfloat16 *>(draft_logits);
+    a.tokens = tree_tokens;
+    a.parents = parents;
+    a.n_nodes = n_nodes;
+    a.accept_len = accept_len_out;
+    a.accept_path = accept_path_out;
+    a.next_token = next_token_out;
+    a.status = status;
+    a.k2 = 1.4426950408889634f / temperature;
+    a.seed = seed;
+    a.offset = offset;
+    a.max_depth = max_depth;
+    if (launch_sample(L, a, reinterpret_cast<uint8_t *>(workspace), reinterpret_cast<cudaStream_t>(stream)) !=
+        cudaSuccess)
+        return JF_ERR_CUDA;
+    return JF_OK;
+}
+
 JF_API int32_t jf_tree_commit_kv(const void *tree_k, const void *tree_v, const int32_t *n_nodes,
                                  const int32_t *accept_len, const int32_t *accept_path, void *k_cache,
                                  void *v_cache, int32_t *prefix_lens, const jf_shape *shape, int32_t max_depth,

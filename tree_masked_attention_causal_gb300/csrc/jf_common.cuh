@@ -60,6 +60,7 @@ struct Layout {
     int32_t chunks;      // argmax chunks per logits row
     size_t qtab_off, ml_off, opart_off;
     size_t amp_off;
+    size_t lse_off;      // stochastic verify: (max, sum) per (target | draft, row, chunk)
     size_t total;
 };
 
@@ -99,6 +100,7 @@ inline Layout make_layout(int B, int Nmax, int Hq, int Hkv, int D, int Pcap, int
     L.ml_off = take(sizeof(float4) * (size_t)L.max_pieces * kRows);   // (m, l, e0, e1)
     L.opart_off = take(2 * (size_t)L.max_pieces * kRows * D);   // fp16 rows, divided by l, scaled by 2^-e per half
     L.amp_off = take(sizeof(int2) * (size_t)B * Nmax * L.chunks);
+    L.lse_off = take(2 * sizeof(float2) * (size_t)B * Nmax * L.chunks);
     L.total = off;
     return L;
 }
@@ -609,6 +611,18 @@ cudaError_t launch_accept_walk(const Layout &L, const int32_t *tokens, const int
                                const int32_t *n_nodes, int32_t *accept_len, int32_t *accept_path,
                                int32_t *argmax_out, int32_t max_depth, uint8_t *ws, int32_t *status,
                                cudaStream_t s);
+
+// Stochastic verification (jf_sample.cu): the per-row normalisers of the
+// target and draft logits, then the walk and the final sample.
+struct SampleArgs {
+    const __nv_bfloat16 *target, *draft;
+    const int32_t *tokens, *parents, *n_nodes;
+    int32_t *accept_len, *accept_path, *next_token, *status;
+    float k2;                 // log2(e) / temperature
+    uint64_t seed, offset;    // Philox key
+    int32_t max_depth;
+};
+cudaError_t launch_sample(const Layout &L, const SampleArgs &a, uint8_t *ws, cudaStream_t s);
 
 // Host-side launch bookkeeping (jf_api.cu): counts launches and records the
 // armed trace events around each one.

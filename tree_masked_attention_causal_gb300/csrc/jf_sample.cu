@@ -1,0 +1,560 @@
+// jf_sample.cu - stochastic tree verification on sm_103a.
+//
+// The paper's section 2.1 "Background" has the target verify the drafted
+// tokens in parallel, citing Leviathan et al. (2023) for the rule. At a
+// temperature T > 0 that rule is speculative sampling: a drafted token x
+// drawn from the draft's distribution q is accepted with probability
+// min(1, p(x) / q(x)), p the target's distribution; on rejection the
+// target's residual max(p - q, 0), renormalised, takes p's place. In a
+// tree it is applied at each accepted node u to u's children in index
+// order, the residual carried from one rejected sibling to the next, and
+// the walk moves to the first accepted child. When no child is accepted
+// the next token is drawn from the final residual.
+//
+// After k rejections at u the residual is max(p - c_k q, 0) / N_k with
+// c_0 = 0, N_0 = 1, c_{k+1} = c_k + N_k and N_k the mass of
+// max(p - c_k q, 0): two scalars replace the residual vector, the
+// acceptance ratio of token x is max(p(x) / q(x) - c_k, 0) / N_k, and
+// each rejection costs one pass over the vocabulary for the new mass.
+//
+//  lse_chunk_kernel    HBM-bound scan of both logits arrays, chunked like
+//                      the argmax: each CTA reduces its chunk of one row
+//                      to (max z, sum 2^((z - max) log2(e) / T)).
+//  sample_walk_kernel  a cluster of kSampleCluster CTAs per sequence,
+//                      launched programmatically after the scan. CTA 0
+//                      validates the tree, merges the row normalisers,
+//                      walks the tree and takes every decision; each pass
+//                      over the vocabulary (a residual mass, or the final
+//                      Gumbel-max sample) is split over the cluster's CTAs,
+//                      whose partial results CTA 0 reads through
+//                      distributed shared memory and combines in rank
+//                      order. The other CTAs only run the commands CTA 0
+//                      posts, so every CTA meets the same sequence of
+//                      cluster barriers.
+//
+// Random numbers: Philox4x64-10 (Salmon, Moraes, Dror and Shaw, "Parallel
+// random numbers: as easy as 1, 2, 3", SC 2011) under key (seed, offset).
+// Node c's acceptance uniform is word c % 4 of the block at counter
+// (c / 4, b, 0, 0); vocabulary entry v's sampling uniform is word v % 4 at
+// counter (v / 4, b, 1, 0). A word w gives (floor(w / 2^41) + 1/2) 2^-23.
+// The sample is the v maximising ln r(v) - ln(-ln U(v)) over r(v) > 0,
+// the lowest index on ties.
+#include "jf_common.cuh"
+
+namespace jf {
+namespace {
+
+constexpr int kSampleCluster = 8;     // CTAs sharing one sequence's vocabulary passes
+constexpr int kSampleThreads = 512;
+constexpr int kSampleVecs = 4;        // 16-byte loads of each row in flight per thread
+
+constexpr uint64_t kPhiloxM0 = 0xD2E7470EE14C6C93ull, kPhiloxM1 = 0xCA5A826395121157ull;
+constexpr uint64_t kPhiloxW0 = 0x9E3779B97F4A7C15ull, kPhiloxW1 = 0xBB67AE8584CAA73Bull;
+constexpr float kLn2 = 0.69314718055994531f;
+
+// Ten Philox4x64 rounds on counter c under key (k0, k1).
+__device__ __forceinline__ void philox4x64_10(uint64_t (&c)[4], uint64_t k0, uint64_t k1) {
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        const uint64_t hi0 = __umul64hi(kPhiloxM0, c[0]), lo0 = kPhiloxM0 * c[0];
+        const uint64_t hi1 = __umul64hi(kPhiloxM1, c[2]), lo1 = kPhiloxM1 * c[2];
+        const uint64_t n0 = hi1 ^ c[1] ^ k0, n2 = hi0 ^ c[3] ^ k1;
+        c[0] = n0;
+        c[1] = lo1;
+        c[2] = n2;
+        c[3] = lo0;
+        k0 += kPhiloxW0;
+        k1 += kPhiloxW1;
+    }
+}
+
+// The 23-bit integer k of a word; the uniform is (k + 1/2) 2^-23, exact in fp32.
+__device__ __forceinline__ uint32_t top23(uint64_t w) { return (uint32_t)(w >> 41); }
+__device__ __forceinline__ float uniform_of(uint32_t k) { return ((float)k + 0.5f) * 0x1p-23f; }
+
+// -ln(-ln U) for U = (k + 1/2) 2^-23: 1 - U = (2^23 - k - 1/2) 2^-23 is
+// exact, so -ln U = -log1p(-(1 - U)) keeps full precision near U = 1.
+__device__ __forceinline__ float gumbel_of(uint32_t k) {
+    const float one_minus = ((float)(0x800000u - k) - 0.5f) * 0x1p-23f;
+    return -logf(-log1pf(-one_minus));
+}
+
+__device__ float accept_uniform(uint64_t seed, uint64_t offset, int b, int c) {
+    uint64_t w[4] = {(uint64_t)(c >> 2), (uint64_t)(uint32_t)b, 0ull, 0ull};
+    philox4x64_10(w, seed, offset);
+    const int j = c & 3;
+    const uint64_t x = j == 0 ? w[0] : j == 1 ? w[1] : j == 2 ? w[2] : w[3];
+    return uniform_of(top23(x));
+}
+
+__device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void unpack8(const uint4 &v, float (&z)[8]) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        z[2 * j] = __uint_as_float(w[j] << 16);
+        z[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+    }
+}
+
+__device__ __forceinline__ float bf16_at(const __nv_bfloat16 *p) {
+    return __uint_as_float((uint32_t)__ldg(reinterpret_cast<const unsigned short *>(p)) << 16);
+}
+
+// (m1, s1) and (m2, s2) are (max, sum 2^((z - max) k2)) of two sets; their union's.
+__device__ __forceinline__ float2 lse_merge(float2 a, float2 b, float k2) {
+    const float M = fmaxf(a.x, b.x);
+    if (M == -__int_as_float(0x7f800000)) return make_float2(M, 0.f);
+    return make_float2(M, a.y * ex2_approx((a.x - M) * k2) + b.y * ex2_approx((b.x - M) * k2));
+}
+
+__global__ void __launch_bounds__(kArgmaxThreads, kArgmaxCtasPerSm)
+    lse_chunk_kernel(const __nv_bfloat16 *__restrict__ target, const __nv_bfloat16 *__restrict__ draft,
+                     const int32_t *__restrict__ n_nodes, float2 *__restrict__ part, int Nmax, int V, int chunk,
+                     int chunks, float k2) {
+    const int row = blockIdx.y, which = blockIdx.z;
+    const int b = row / Nmax, i = row - b * Nmax;
+    const int n = n_nodes[b];
+    if (n < 1 || n > Nmax || i >= n) {                       // padding row
+        pdl_launch_dependents();
+        return;
+    }
+    const int tid = threadIdx.x;
+    const int e0 = blockIdx.x * chunk;
+    const int nvec = (min(V, e0 + chunk) - e0) >> 3;         // V % 8 == 0
+    const uint4 *src = reinterpret_cast<const uint4 *>((which ? draft : target) + (size_t)row * V + e0);
+    float2 acc = make_float2(-__int_as_float(0x7f800000), 0.f);
+    for (int k0 = tid; k0 < nvec; k0 += kArgmaxThreads * kArgmaxVecs) {
+        uint4 v[kArgmaxVecs];
+#pragma unroll
+        for (int u = 0; u < kArgmaxVecs; ++u) {
+            const int k = k0 + u * kArgmaxThreads;
+            if (k < nvec) v[u] = ld_stream(src + k);
+        }
+#pragma unroll
+        for (int u = 0; u < kArgmaxVecs; ++u) {
+            const int k = k0 + u * kArgmaxThreads;
+            if (k < nvec) {
+                float z[8];
+                unpack8(v[u], z);
+                float vm = z[0];
+#pragma unroll
+                for (int j = 1; j < 8; ++j) vm = fmaxf(vm, z[j]);
+                if (vm > acc.x) {
+                    acc.y *= ex2_approx((acc.x - vm) * k2);
+                    acc.x = vm;
+                }
+                float s = 0.f;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) s += ex2_approx((z[j] - acc.x) * k2);
+                acc.y += s;
+            }
+        }
+    }
+    pdl_launch_dependents();
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float2 other = make_float2(__shfl_xor_sync(0xffffffffu, acc.x, o), __shfl_xor_sync(0xffffffffu, acc.y, o));
+        acc = lse_merge(acc, other, k2);
+    }
+    __shared__ float2 sred[kArgmaxThreads / 32];
+    const int warp = tid >> 5, lane = tid & 31;
+    if (lane == 0) sred[warp] = acc;
+    __syncthreads();
+    if (tid == 0) {
+        float2 t = sred[0];
+        for (int w = 1; w < kArgmaxThreads / 32; ++w) t = lse_merge(t, sred[w], k2);
+        const size_t rows = gridDim.y;
+        part[((size_t)which * rows + row) * chunks + blockIdx.x] = t;
+    }
+}
+
+// ------------------------------------------------------------- the cluster
+
+enum : int { kOpExit = 0, kOpMass = 1, kOpSample = 2 };
+
+// A command CTA 0 posts to every CTA of its cluster: the pass and the row
+// it runs over, with the residual's scale c and the row normalisers
+// (max, log2 sum) of the target (p) and the draft (q).
+struct Cmd {
+    int op, row;
+    float c, Mp, Lp, Mq, Lq, pad;
+};
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Every thread of every CTA of the cluster; orders shared-memory writes
+// before it with reads after it, across the cluster.
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ void st_cluster(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_cluster(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+struct WalkShared {
+    Cmd cmd;                     // this CTA's command (written by CTA 0)
+    float part_f;                // this CTA's partial: residual mass, or the best Gumbel key
+    int part_i;                  //   and its index
+    float red_f[kSampleThreads / 32];
+    int red_i[kSampleThreads / 32];
+    float bcast_f[6];
+    int bcast_i[2];
+    int par[kMaxNodes], tok[kMaxNodes], path[kMaxNodes];
+};
+
+// (a, ia) beats (b, ib): the larger key, then the lower index.
+__device__ __forceinline__ bool beats(float a, int ia, float b, int ib) {
+    return a > b || (a == b && ia >= 0 && (ib < 0 || ia < ib));
+}
+
+// This CTA's share of a pass over row cmd.row: the residual mass of its
+// vocabulary slice, or the best (key, index) of the Gumbel-max sample.
+__device__ void run_slice(const Cmd &cmd, const SampleArgs &a, int V, int b, uint32_t rank, WalkShared &sh,
+                          float &out_f, int &out_i) {
+    const int tid = threadIdx.x;
+    const int nv = V >> 3;
+    const int lo = (int)((long long)rank * nv / kSampleCluster);
+    const int hi = (int)((long long)(rank + 1) * nv / kSampleCluster);
+    const uint4 *rp = reinterpret_cast<const uint4 *>(a.target + (size_t)cmd.row * V);
+    const uint4 *rq = reinterpret_cast<const uint4 *>(a.draft + (size_t)cmd.row * V);
+    const float k2 = a.k2, c = cmd.c;
+    const float Mp = cmd.Mp, Lp = cmd.Lp, Mq = cmd.Mq, Lq = cmd.Lq;
+    float best = -__int_as_float(0x7f800000);
+    int best_i = -1;
+    float mass = 0.f;
+    for (int k0 = lo + tid; k0 < hi; k0 += kSampleThreads * kSampleVecs) {
+        uint4 vp[kSampleVecs], vq[kSampleVecs];
+#pragma unroll
+        for (int u = 0; u < kSampleVecs; ++u) {
+            const int k = k0 + u * kSampleThreads;
+            if (k < hi) {
+                vp[u] = ld_stream(rp + k);
+                if (c > 0.f) vq[u] = ld_stream(rq + k);
+            }
+        }
+#pragma unroll 1
+        for (int u = 0; u < kSampleVecs; ++u) {
+            const int k = k0 + u * kSampleThreads;
+            if (k >= hi) break;
+            float zp[8], zq[8];
+            unpack8(vp[u], zp);
+            if (c > 0.f) unpack8(vq[u], zq);
+            if (cmd.op == kOpMass) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float p = ex2_approx((zp[j] - Mp) * k2 - Lp);
+                    const float q = ex2_approx((zq[j] - Mq) * k2 - Lq);
+                    mass += fmaxf(p - c * q, 0.f);
+                }
+            } else {
+                uint64_t w[8];
+                uint64_t c0[4] = {(uint64_t)(2 * k), (uint64_t)(uint32_t)b, 1ull, 0ull};
+                uint64_t c1[4] = {(uint64_t)(2 * k + 1), (uint64_t)(uint32_t)b, 1ull, 0ull};
+                philox4x64_10(c0, a.seed, a.offset);
+                philox4x64_10(c1, a.seed, a.offset);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    w[j] = c0[j];
+                    w[4 + j] = c1[j];
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    // log2 of p, then of the residual p - c q where it is positive
+                    float lr = (zp[j] - Mp) * k2 - Lp;
+                    bool keep = true;
+                    if (c > 0.f) {
+                        const float lq = (zq[j] - Mq) * k2 - Lq;
+                        const float x = c * ex2_approx(lq - lr);
+                        keep = x < 1.f;
+                        lr += log1pf(-x) * 1.4426950408889634f;
+                    }
+                    if (keep) {
+                        const float key = lr * kLn2 + gumbel_of(top23(w[j]));
+                        if (key > best) {               // strictly: the first (lowest) index keeps a tie
+                            best = key;
+                            best_i = 8 * k + j;
+                        }
+                    }
+                }
+            }
+        }
+    }
+    // block reduction in a fixed order
+    const int warp = tid >> 5, lane = tid & 31;
+    if (cmd.op == kOpMass) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mass += __shfl_xor_sync(0xffffffffu, mass, o);
+        if (lane == 0) sh.red_f[warp] = mass;
+        __syncthreads();
+        if (tid == 0) {
+            float t = 0.f;
+            for (int w2 = 0; w2 < kSampleThreads / 32; ++w2) t += sh.red_f[w2];
+            out_f = t;
+            out_i = 0;
+        }
+    } else {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ob = __shfl_xor_sync(0xffffffffu, best, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, best_i, o);
+            if (beats(ob, oi, best, best_i)) {
+                best = ob;
+                best_i = oi;
+            }
+        }
+        if (lane == 0) {
+            sh.red_f[warp] = best;
+            sh.red_i[warp] = best_i;
+        }
+        __syncthreads();
+        if (tid == 0) {
+            float t = sh.red_f[0];
+            int ti = sh.red_i[0];
+            for (int w2 = 1; w2 < kSampleThreads / 32; ++w2)
+                if (beats(sh.red_f[w2], sh.red_i[w2], t, ti)) {
+                    t = sh.red_f[w2];
+                    ti = sh.red_i[w2];
+                }
+            out_f = t;
+            out_i = ti;
+        }
+    }
+    __syncthreads();
+}
+
+// CTA 0 only: post a command to every CTA of the cluster (itself included).
+__device__ void post(WalkShared &sh, int op, int row, float c, const float *lse) {
+    const int tid = threadIdx.x;
+    if (tid < kSampleCluster) {
+        const uint32_t base = map_to_rank(smem_u32(&sh.cmd), tid);
+        st_cluster(base + 0, (uint32_t)op);
+        st_cluster(base + 4, (uint32_t)row);
+        st_cluster(base + 8, __float_as_uint(c));
+        for (int j = 0; j < 4; ++j) st_cluster(base + 12 + 4 * j, __float_as_uint(lse[j]));
+    }
+}
+
+// CTA 0 only: one pass over row `row` split over the cluster. Returns the
+// combined result (mass, or (key, index)) to every thread of CTA 0.
+__device__ void cluster_pass(WalkShared &sh, const SampleArgs &a, int V, int b, int op, int row, float c,
+                             const float *lse, float &res_f, int &res_i) {
+    post(sh, op, row, c, lse);
+    cluster_sync_all();                                      // commands visible
+    float f = 0.f;
+    int i = 0;
+    run_slice(sh.cmd, a, V, b, 0, sh, f, i);
+    if (threadIdx.x == 0) {
+        sh.part_f = f;
+        sh.part_i = i;
+    }
+    cluster_sync_all();                                      // partials visible
+    if (threadIdx.x == 0) {
+        float t = op == kOpMass ? 0.f : -__int_as_float(0x7f800000);
+        int ti = -1;
+        for (uint32_t r = 0; r < kSampleCluster; ++r) {
+            const float pf = __uint_as_float(ld_cluster(map_to_rank(smem_u32(&sh.part_f), r)));
+            const int pi = (int)ld_cluster(map_to_rank(smem_u32(&sh.part_i), r));
+            if (op == kOpMass) {
+                t += pf;
+            } else if (beats(pf, pi, t, ti)) {
+                t = pf;
+                ti = pi;
+            }
+        }
+        sh.bcast_f[0] = t;
+        sh.bcast_i[0] = ti;
+    }
+    __syncthreads();
+    res_f = sh.bcast_f[0];
+    res_i = sh.bcast_i[0];
+    __syncthreads();
+}
+
+// Warp 0 of CTA 0: (max, log2 sum) of the target and draft rows `row`,
+// merged from the scan's chunks in chunk order, into lse[0..3].
+__device__ void row_normalisers(const float2 *part, int rows, int row, int chunks, float k2, float *lse) {
+    const int lane = threadIdx.x & 31;
+    for (int which = 0; which < 2; ++which) {
+        float2 acc = make_float2(-__int_as_float(0x7f800000), 0.f);
+        for (int ch = lane; ch < chunks; ch += 32)
+            acc = lse_merge(acc, part[((size_t)which * rows + row) * chunks + ch], k2);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float2 other =
+                make_float2(__shfl_xor_sync(0xffffffffu, acc.x, o), __shfl_xor_sync(0xffffffffu, acc.y, o));
+            acc = lse_merge(acc, other, k2);
+        }
+        if (lane == 0) {
+            lse[2 * which] = acc.x;
+            lse[2 * which + 1] = log2f(acc.y);
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kSampleThreads)
+    sample_walk_kernel(const Layout L, const SampleArgs a, const float2 *__restrict__ part) {
+    __shared__ WalkShared sh;
+    const uint32_t rank = cluster_rank();
+    const int b = blockIdx.y, tid = threadIdx.x;
+    const int V = L.V, Nmax = L.Nmax, rows = L.B * L.Nmax;
+    if (rank != 0) {
+        // the cluster's workers: run each posted pass until told to stop
+        pdl_wait_prior_grid();
+        for (;;) {
+            cluster_sync_all();                              // a command is posted
+            const Cmd cmd = sh.cmd;                          // posted before the barrier
+            if (cmd.op == kOpExit) break;
+            float f = 0.f;
+            int i = 0;
+            run_slice(cmd, a, V, b, rank, sh, f, i);
+            if (tid == 0) {
+                sh.part_f = f;
+                sh.part_i = i;
+            }
+            cluster_sync_all();                              // the partial is posted
+        }
+        return;
+    }
+    // CTA 0. Before the scan completes: the tree (inputs only).
+    const int n = a.n_nodes[b];
+    bool bad = n < 1 || n > Nmax;
+    for (int i = tid; !bad && i < n; i += kSampleThreads) {
+        const int p = a.parents[(size_t)b * Nmax + i];
+        sh.par[i] = p;
+        sh.tok[i] = a.tokens[(size_t)b * Nmax + i];
+        bad = (i == 0) ? (p != -1) : (p < 0 || p >= i);
+    }
+    bad = __syncthreads_or(bad);
+    pdl_wait_prior_grid();
+    int32_t *path_out = a.accept_path + (size_t)b * (a.max_depth + 1);
+    float lse[4] = {0.f, 0.f, 0.f, 0.f};
+    if (bad) {
+        for (int k = tid; k <= a.max_depth; k += kSampleThreads) path_out[k] = -1;
+        if (tid == 0) {
+            a.accept_len[b] = 0;
+            a.next_token[b] = -1;
+            set_status(a.status, JF_STATUS_BAD_TREE);
+        }
+        post(sh, kOpExit, 0, 0.f, lse);
+        cluster_sync_all();
+        return;
+    }
+    int u = 0, depth = 0;
+    float c = 0.f, N = 1.f;
+    for (;;) {
+        const int row = b * Nmax + u;
+        if (tid < 32) row_normalisers(part, rows, row, L.chunks, a.k2, sh.bcast_f + 2);
+        __syncthreads();
+        for (int j = 0; j < 4; ++j) lse[j] = sh.bcast_f[2 + j];
+        __syncthreads();
+        c = 0.f;
+        N = 1.f;
+        int next = -1;
+        if (depth < a.max_depth) {
+            for (int ch = u + 1; ch < n; ++ch) {
+                if (sh.par[ch] != u) continue;
+                if (tid == 0) {
+                    const int x = sh.tok[ch];
+                    float ratio = 0.f;
+                    if (x >= 0 && x < V) {
+                        const float lp = (bf16_at(a.target + (size_t)row * V + x) - lse[0]) * a.k2 - lse[1];
+                        const float lq = (bf16_at(a.draft + (size_t)row * V + x) - lse[2]) * a.k2 - lse[3];
+                        ratio = fmaxf(ex2_approx(lp - lq) - c, 0.f) / N;
+                    }
+                    const float U = accept_uniform(a.seed, a.offset, b, ch);
+                    sh.bcast_i[1] = U < fminf(ratio, 1.f) ? 1 : 0;
+                }
+                __syncthreads();
+                const int accepted = sh.bcast_i[1];
+                __syncthreads();
+                if (accepted) {
+                    next = ch;
+                    break;
+                }
+                c += N;                                      // the residual after this rejection
+                float mass;
+                int unused;
+                cluster_pass(sh, a, V, b, kOpMass, row, c, lse, mass, unused);
+                N = mass;
+                if (!(N > 0.f)) {                            // the residual vanished: sample from p
+                    c = 0.f;
+                    N = 1.f;
+                    break;
+                }
+            }
+        }
+        if (next < 0) break;
+        u = next;
+        ++depth;
+        if (tid == 0) sh.path[depth] = u;
+    }
+    float key;
+    int token;
+    cluster_pass(sh, a, V, b, kOpSample, b * Nmax + u, c, lse, key, token);
+    __syncthreads();
+    for (int k = tid; k <= a.max_depth; k += kSampleThreads) path_out[k] = k == 0 ? 0 : (k <= depth ? sh.path[k] : -1);
+    if (tid == 0) {
+        a.accept_len[b] = depth + 1;
+        a.next_token[b] = token;
+    }
+    post(sh, kOpExit, 0, 0.f, lse);
+    cluster_sync_all();
+}
+
+}  // namespace
+
+cudaError_t launch_sample(const Layout &L, const SampleArgs &a, uint8_t *ws, cudaStream_t s) {
+    const int rows = L.B * L.Nmax;
+    float2 *part = reinterpret_cast<float2 *>(ws + L.lse_off);
+    trace_begin("lse_chunk", s);
+    lse_chunk_kernel<<<dim3(L.chunks, rows, 2), kArgmaxThreads, 0, s>>>(a.target, a.draft, a.n_nodes, part, L.Nmax,
+                                                                        L.V, L.chunk, L.chunks, a.k2);
+    cudaError_t e = cudaGetLastError();
+    trace_end(s);
+    if (e != cudaSuccess) return e;
+    trace_begin("sample_walk", s);
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(kSampleCluster, L.B, 1);
+    cfg.blockDim = dim3(kSampleThreads, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kSampleCluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    e = cudaLaunchKernelEx(&cfg, sample_walk_kernel, L, a, static_cast<const float2 *>(part));
+    trace_end(s);
+    return e;
+}
+
+}  // namespace jf

@@ -219,6 +219,42 @@ def make_logits(gen: torch.Generator, B: int, N: int, vocab: int,
     return logits
 
 
+# Draft logits of the sampling inputs are N(0, SAMPLE_SCALE^2); the
+# target's are the draft's plus SAMPLE_NOISE * N(0, 1), so that the target
+# agrees with the draft often but not always.
+SAMPLE_SCALE = 2.0
+SAMPLE_NOISE = 0.5
+
+
+def make_sample_inputs(w: Workload, seed: Optional[int] = None, temperature: float = 1.0,
+                       noise: float = SAMPLE_NOISE) -> Dict[str, torch.Tensor]:
+    """Inputs of one stochastic verification call on workload w's shapes.
+
+      draft_logits   bf16 [B, Nmax, V]: N(0, SAMPLE_SCALE^2) clamped to [-8, 8]
+      target_logits  bf16 [B, Nmax, V]: draft + noise * N(0,1), clamped alike
+      parents        int32 [B, Nmax]: trees drawn like make_inputs' trees
+      tokens         int32 [B, Nmax]: node c's token is a draw from the
+                     draft's distribution at its parent, softmax(draft_logits
+                     [b, parent(c)] / temperature), as a sampling draft
+                     proposes it; node 0's token is 0
+      n_nodes        int32 [B] = Nmax
+    """
+    gen = torch.Generator().manual_seed((w.seed if seed is None else seed) + 7919)
+    B, N, V = w.batch, w.max_nodes, w.vocab
+    parents = torch.tensor([random_tree(gen, N, w.depth_limit, w.branch_limit) for _ in range(B)],
+                           dtype=torch.int32)
+    draft = (SAMPLE_SCALE * torch.randn((B, N, V), generator=gen)).clamp(-CLAMP, CLAMP).to(torch.bfloat16)
+    target = (draft.float() + noise * torch.randn((B, N, V), generator=gen)).clamp(-CLAMP, CLAMP)
+    target = target.to(torch.bfloat16)
+    tokens = torch.zeros((B, N), dtype=torch.int32)
+    for b in range(B):
+        probs = torch.softmax(draft[b].float() / temperature, dim=-1)
+        rows = probs[parents[b, 1:].long()]
+        tokens[b, 1:] = torch.multinomial(rows, 1, generator=gen).reshape(-1).to(torch.int32)
+    return dict(target_logits=target, draft_logits=draft, parents=parents, tokens=tokens,
+                n_nodes=torch.full((B,), N, dtype=torch.int32))
+
+
 def attention_flops(parents: torch.Tensor, n_nodes: torch.Tensor, prefix_lens: torch.Tensor,
                     n_q_heads: int, head_dim: int) -> int:
     """Algorithmic FLOP of one tree-attention call: only the (node, key) pairs
