@@ -287,7 +287,7 @@ JF_API int32_t jf_tree_verify_sample(const void *target_logits, const void *draf
     a.seed = seed;
     a.offset = offset;
     a.max_depth = max_depth;
-    if (launch_sample(L, a, reinterpret_cast<uint8_t *>(workspace), reinterpret_cast<cudaStream_t>(stream)) !=
+    if (launch_sample(L, a, reinterpret_cast<uint8_t *>(workspace), sms, reinterpret_cast<cudaStream_t>(stream)) !=
         cudaSuccess)
         return JF_ERR_CUDA;
     return JF_OK;

@@ -622,7 +622,7 @@ struct SampleArgs {
     uint64_t seed, offset;    // Philox key
     int32_t max_depth;
 };
-cudaError_t launch_sample(const Layout &L, const SampleArgs &a, uint8_t *ws, cudaStream_t s);
+cudaError_t launch_sample(const Layout &L, const SampleArgs &a, uint8_t *ws, int sms, cudaStream_t s);
 
 // Host-side launch bookkeeping (jf_api.cu): counts launches and records the
 // armed trace events around each one.

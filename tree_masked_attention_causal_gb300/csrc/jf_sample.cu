@@ -45,6 +45,8 @@ namespace jf {
 namespace {
 
 constexpr int kSampleCluster = 8;     // CTAs sharing one sequence's vocabulary passes
+constexpr int kSampleClusterBig = 16; // the same when the batch is small enough
+constexpr size_t kSampleNoiseMax = 192 * 1024;  // dynamic shared memory for a slice's Gumbel noise
 constexpr int kSampleThreads = 512;
 constexpr int kSampleVecs = 4;        // 16-byte loads of each row in flight per thread
 
@@ -119,13 +121,13 @@ __global__ void __launch_bounds__(kArgmaxThreads, kArgmaxCtasPerSm)
     lse_chunk_kernel(const __nv_bfloat16 *__restrict__ target, const __nv_bfloat16 *__restrict__ draft,
                      const int32_t *__restrict__ n_nodes, float2 *__restrict__ part, int Nmax, int V, int chunk,
                      int chunks, float k2) {
+    // the walk's clusters may start now: their work before the wait (the
+    // tree, the Gumbel noise) overlaps this scan
+    pdl_launch_dependents();
     const int row = blockIdx.y, which = blockIdx.z;
     const int b = row / Nmax, i = row - b * Nmax;
     const int n = n_nodes[b];
-    if (n < 1 || n > Nmax || i >= n) {                       // padding row
-        pdl_launch_dependents();
-        return;
-    }
+    if (n < 1 || n > Nmax || i >= n) return;                 // padding row
     const int tid = threadIdx.x;
     const int e0 = blockIdx.x * chunk;
     const int nvec = (min(V, e0 + chunk) - e0) >> 3;         // V % 8 == 0
@@ -158,7 +160,6 @@ __global__ void __launch_bounds__(kArgmaxThreads, kArgmaxCtasPerSm)
             }
         }
     }
-    pdl_launch_dependents();
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         const float2 other = make_float2(__shfl_xor_sync(0xffffffffu, acc.x, o), __shfl_xor_sync(0xffffffffu, acc.y, o));
@@ -194,6 +195,12 @@ __device__ __forceinline__ uint32_t cluster_rank() {
     return r;
 }
 
+__device__ __forceinline__ uint32_t cluster_size() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+
 // Every thread of every CTA of the cluster; orders shared-memory writes
 // before it with reads after it, across the cluster.
 __device__ __forceinline__ void cluster_sync_all() {
@@ -210,21 +217,26 @@ __device__ __forceinline__ void st_cluster(uint32_t addr, uint32_t v) {
     asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
-__device__ __forceinline__ uint32_t ld_cluster(uint32_t addr) {
-    uint32_t v;
-    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
-    return v;
-}
-
 struct WalkShared {
     Cmd cmd;                     // this CTA's command (written by CTA 0)
-    float part_f;                // this CTA's partial: residual mass, or the best Gumbel key
-    int part_i;                  //   and its index
+    float part_f[kSampleClusterBig];   // CTA 0 only: each CTA's partial, stored there by that CTA:
+    int part_i[kSampleClusterBig];     //   a residual mass, or the best Gumbel key and its index
     float red_f[kSampleThreads / 32];
     int red_i[kSampleThreads / 32];
-    float bcast_f[6];
+    float bcast_f[2];
     int bcast_i[2];
-    int par[kMaxNodes], tok[kMaxNodes], path[kMaxNodes];
+    // CTA 0's copy of the tree, gathered before the scan completes: each
+    // node's parent, first child and next sibling (index order, -1 when
+    // none), its acceptance uniform, and the target and draft logits of
+    // its token in its parent's rows (NaN for a token outside [0, V))
+    int par[kMaxNodes], first_child[kMaxNodes], next_sib[kMaxNodes], path[kMaxNodes];
+    uint32_t kids[kMaxNodes][8];
+    float u[kMaxNodes], zp[kMaxNodes], zq[kMaxNodes];
+    // per node row: (max, log2 sum) of the target and the draft
+    float lse[kMaxNodes][4];
+    // the walk's state, handed from thread 0 to the CTA
+    int st_u, st_depth, st_next, st_op;
+    float st_c, st_N;
 };
 
 // (a, ia) beats (b, ib): the larger key, then the lower index.
@@ -232,14 +244,56 @@ __device__ __forceinline__ bool beats(float a, int ia, float b, int ib) {
     return a > b || (a == b && ia >= 0 && (ib < 0 || ia < ib));
 }
 
+// The vectors (8 entries each) of the vocabulary that cluster CTA `rank` covers.
+__device__ __forceinline__ void slice_of(int V, uint32_t rank, int &lo, int &hi) {
+    const int nv = V >> 3, kc = (int)cluster_size();
+    lo = (int)((long long)rank * nv / kc);
+    hi = (int)((long long)(rank + 1) * nv / kc);
+}
+
+__device__ __forceinline__ uint32_t dynamic_smem_bytes() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%dynamic_smem_size;" : "=r"(r));
+    return r;
+}
+
+// Dynamic shared memory: the Gumbel noise of this CTA's vocabulary slice,
+// when the launch gave it room (else the final pass draws it on the fly).
+extern __shared__ float s_noise[];
+
+__device__ __forceinline__ void philox_vec(int k, int b, uint64_t seed, uint64_t offset, uint64_t (&w)[8]) {
+    uint64_t c0[4] = {(uint64_t)(2 * k), (uint64_t)(uint32_t)b, 1ull, 0ull};
+    uint64_t c1[4] = {(uint64_t)(2 * k + 1), (uint64_t)(uint32_t)b, 1ull, 0ull};
+    philox4x64_10(c0, seed, offset);
+    philox4x64_10(c1, seed, offset);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        w[j] = c0[j];
+        w[4 + j] = c1[j];
+    }
+}
+
+// Before the scan completes: the noise of the slice into shared memory.
+__device__ void precompute_noise(const SampleArgs &a, int V, int b, uint32_t rank) {
+    int lo, hi;
+    slice_of(V, rank, lo, hi);
+    if ((uint32_t)(hi - lo) * 32u > dynamic_smem_bytes()) return;
+    for (int k = lo + (int)threadIdx.x; k < hi; k += kSampleThreads) {
+        uint64_t w[8];
+        philox_vec(k, b, a.seed, a.offset, w);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) s_noise[(k - lo) * 8 + j] = gumbel_of(top23(w[j]));
+    }
+}
+
 // This CTA's share of a pass over row cmd.row: the residual mass of its
 // vocabulary slice, or the best (key, index) of the Gumbel-max sample.
 __device__ void run_slice(const Cmd &cmd, const SampleArgs &a, int V, int b, uint32_t rank, WalkShared &sh,
                           float &out_f, int &out_i) {
     const int tid = threadIdx.x;
-    const int nv = V >> 3;
-    const int lo = (int)((long long)rank * nv / kSampleCluster);
-    const int hi = (int)((long long)(rank + 1) * nv / kSampleCluster);
+    int lo, hi;
+    slice_of(V, rank, lo, hi);
+    const bool stored = (uint32_t)(hi - lo) * 32u <= dynamic_smem_bytes();
     const uint4 *rp = reinterpret_cast<const uint4 *>(a.target + (size_t)cmd.row * V);
     const uint4 *rq = reinterpret_cast<const uint4 *>(a.draft + (size_t)cmd.row * V);
     const float k2 = a.k2, c = cmd.c;
@@ -273,15 +327,7 @@ __device__ void run_slice(const Cmd &cmd, const SampleArgs &a, int V, int b, uin
                 }
             } else {
                 uint64_t w[8];
-                uint64_t c0[4] = {(uint64_t)(2 * k), (uint64_t)(uint32_t)b, 1ull, 0ull};
-                uint64_t c1[4] = {(uint64_t)(2 * k + 1), (uint64_t)(uint32_t)b, 1ull, 0ull};
-                philox4x64_10(c0, a.seed, a.offset);
-                philox4x64_10(c1, a.seed, a.offset);
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    w[j] = c0[j];
-                    w[4 + j] = c1[j];
-                }
+                if (!stored) philox_vec(k, b, a.seed, a.offset, w);
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     // log2 of p, then of the residual p - c q where it is positive
@@ -294,7 +340,8 @@ __device__ void run_slice(const Cmd &cmd, const SampleArgs &a, int V, int b, uin
                         lr += log1pf(-x) * 1.4426950408889634f;
                     }
                     if (keep) {
-                        const float key = lr * kLn2 + gumbel_of(top23(w[j]));
+                        const float g = stored ? s_noise[(k - lo) * 8 + j] : gumbel_of(top23(w[j]));
+                        const float key = lr * kLn2 + g;
                         if (key > best) {               // strictly: the first (lowest) index keeps a tie
                             best = key;
                             best_i = 8 * k + j;
@@ -350,7 +397,7 @@ __device__ void run_slice(const Cmd &cmd, const SampleArgs &a, int V, int b, uin
 // CTA 0 only: post a command to every CTA of the cluster (itself included).
 __device__ void post(WalkShared &sh, int op, int row, float c, const float *lse) {
     const int tid = threadIdx.x;
-    if (tid < kSampleCluster) {
+    if (tid < (int)cluster_size()) {
         const uint32_t base = map_to_rank(smem_u32(&sh.cmd), tid);
         st_cluster(base + 0, (uint32_t)op);
         st_cluster(base + 4, (uint32_t)row);
@@ -369,16 +416,17 @@ __device__ void cluster_pass(WalkShared &sh, const SampleArgs &a, int V, int b, 
     int i = 0;
     run_slice(sh.cmd, a, V, b, 0, sh, f, i);
     if (threadIdx.x == 0) {
-        sh.part_f = f;
-        sh.part_i = i;
+        sh.part_f[0] = f;
+        sh.part_i[0] = i;
     }
-    cluster_sync_all();                                      // partials visible
+    cluster_sync_all();                                      // every partial is in place
     if (threadIdx.x == 0) {
         float t = op == kOpMass ? 0.f : -__int_as_float(0x7f800000);
         int ti = -1;
-        for (uint32_t r = 0; r < kSampleCluster; ++r) {
-            const float pf = __uint_as_float(ld_cluster(map_to_rank(smem_u32(&sh.part_f), r)));
-            const int pi = (int)ld_cluster(map_to_rank(smem_u32(&sh.part_i), r));
+        const uint32_t kc = cluster_size();
+        for (uint32_t r = 0; r < kc; ++r) {
+            const float pf = sh.part_f[r];
+            const int pi = sh.part_i[r];
             if (op == kOpMass) {
                 t += pf;
             } else if (beats(pf, pi, t, ti)) {
@@ -395,28 +443,10 @@ __device__ void cluster_pass(WalkShared &sh, const SampleArgs &a, int V, int b, 
     __syncthreads();
 }
 
-// Warp 0 of CTA 0: (max, log2 sum) of the target and draft rows `row`,
-// merged from the scan's chunks in chunk order, into lse[0..3].
-__device__ void row_normalisers(const float2 *part, int rows, int row, int chunks, float k2, float *lse) {
-    const int lane = threadIdx.x & 31;
-    for (int which = 0; which < 2; ++which) {
-        float2 acc = make_float2(-__int_as_float(0x7f800000), 0.f);
-        for (int ch = lane; ch < chunks; ch += 32)
-            acc = lse_merge(acc, part[((size_t)which * rows + row) * chunks + ch], k2);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float2 other =
-                make_float2(__shfl_xor_sync(0xffffffffu, acc.x, o), __shfl_xor_sync(0xffffffffu, acc.y, o));
-            acc = lse_merge(acc, other, k2);
-        }
-        if (lane == 0) {
-            lse[2 * which] = acc.x;
-            lse[2 * which + 1] = log2f(acc.y);
-        }
-    }
-}
+// The walk's states, as thread 0 hands them to the CTA.
+enum : int { kWalkMass = 0, kWalkDone = 1 };
 
-__global__ void __launch_bounds__(kSampleThreads)
+__global__ void __launch_bounds__(kSampleThreads, 2)
     sample_walk_kernel(const Layout L, const SampleArgs a, const float2 *__restrict__ part) {
     __shared__ WalkShared sh;
     const uint32_t rank = cluster_rank();
@@ -424,6 +454,7 @@ __global__ void __launch_bounds__(kSampleThreads)
     const int V = L.V, Nmax = L.Nmax, rows = L.B * L.Nmax;
     if (rank != 0) {
         // the cluster's workers: run each posted pass until told to stop
+        precompute_noise(a, V, b, rank);
         pdl_wait_prior_grid();
         for (;;) {
             cluster_sync_all();                              // a command is posted
@@ -432,24 +463,57 @@ __global__ void __launch_bounds__(kSampleThreads)
             float f = 0.f;
             int i = 0;
             run_slice(cmd, a, V, b, rank, sh, f, i);
-            if (tid == 0) {
-                sh.part_f = f;
-                sh.part_i = i;
+            if (tid == 0) {                                  // into CTA 0's slot for this rank
+                st_cluster(map_to_rank(smem_u32(&sh.part_f[rank]), 0), __float_as_uint(f));
+                st_cluster(map_to_rank(smem_u32(&sh.part_i[rank]), 0), (uint32_t)i);
             }
             cluster_sync_all();                              // the partial is posted
         }
         return;
     }
-    // CTA 0. Before the scan completes: the tree (inputs only).
+    // CTA 0. Before the scan completes (inputs only): the tree, its child
+    // lists, every node's acceptance uniform and its token's two logits.
     const int n = a.n_nodes[b];
     bool bad = n < 1 || n > Nmax;
-    for (int i = tid; !bad && i < n; i += kSampleThreads) {
-        const int p = a.parents[(size_t)b * Nmax + i];
-        sh.par[i] = p;
-        sh.tok[i] = a.tokens[(size_t)b * Nmax + i];
-        bad = (i == 0) ? (p != -1) : (p < 0 || p >= i);
+    const size_t seq = (size_t)b * Nmax;
+    if (!bad && tid < n) {
+        const int p = a.parents[seq + tid];
+        sh.par[tid] = p;
+        bad = (tid == 0) ? (p != -1) : (p < 0 || p >= tid);
     }
     bad = __syncthreads_or(bad);
+    if (!bad) {
+        // children of each node as a bit set, then first child and next
+        // sibling in index order from the set bits
+        for (int k = tid; k < kMaxNodes * 8; k += kSampleThreads) (&sh.kids[0][0])[k] = 0u;
+        __syncthreads();
+        if (tid > 0 && tid < n) atomicOr(&sh.kids[sh.par[tid]][tid >> 5], 1u << (tid & 31));
+        __syncthreads();
+    }
+    if (!bad && tid < n) {
+        auto lowest_from = [&](const uint32_t *set, int from) {   // lowest member >= from, or -1
+            for (int w = from >> 5; w < 8; ++w) {
+                const uint32_t m = set[w] & (0xFFFFFFFFu << (w == (from >> 5) ? (from & 31) : 0));
+                if (m) return 32 * w + __ffs(m) - 1;
+            }
+            return -1;
+        };
+        sh.first_child[tid] = lowest_from(sh.kids[tid], 0);
+        sh.next_sib[tid] = tid > 0 && tid < kMaxNodes - 1 ? lowest_from(sh.kids[sh.par[tid]], tid + 1) : -1;
+        float zp = __int_as_float(0x7fc00000), zq = zp;
+        if (tid > 0) {
+            const int x = a.tokens[seq + tid];
+            if (x >= 0 && x < V) {
+                const size_t at = (seq + sh.par[tid]) * (size_t)V + x;
+                zp = bf16_at(a.target + at);
+                zq = bf16_at(a.draft + at);
+            }
+            sh.u[tid] = accept_uniform(a.seed, a.offset, b, tid);
+        }
+        sh.zp[tid] = zp;
+        sh.zq[tid] = zq;
+    }
+    precompute_noise(a, V, b, 0);
     pdl_wait_prior_grid();
     int32_t *path_out = a.accept_path + (size_t)b * (a.max_depth + 1);
     float lse[4] = {0.f, 0.f, 0.f, 0.f};
@@ -464,60 +528,87 @@ __global__ void __launch_bounds__(kSampleThreads)
         cluster_sync_all();
         return;
     }
-    int u = 0, depth = 0;
-    float c = 0.f, N = 1.f;
+    // every node row's normalisers, merged from the scan's chunks in chunk order
+    for (int t = tid; t < 2 * n; t += kSampleThreads) {
+        const int i = t >> 1, which = t & 1;
+        const float2 *pr = part + ((size_t)which * rows + seq + i) * L.chunks;
+        float2 acc = make_float2(-__int_as_float(0x7f800000), 0.f);
+#pragma unroll 4
+        for (int ch = 0; ch < L.chunks; ++ch) acc = lse_merge(acc, pr[ch], a.k2);
+        sh.lse[i][2 * which] = acc.x;
+        sh.lse[i][2 * which + 1] = log2f(acc.y);
+    }
+    if (tid == 0) {
+        sh.st_u = 0;
+        sh.st_depth = 0;
+        sh.st_next = sh.first_child[0];
+        sh.st_c = 0.f;
+        sh.st_N = 1.f;
+        sh.path[0] = 0;
+    }
+    __syncthreads();
+    // Thread 0 walks the tree from shared memory until a rejection needs the
+    // residual's new mass (a pass over the vocabulary by the whole cluster)
+    // or the walk ends; the CTA then runs that pass and thread 0 goes on.
     for (;;) {
-        const int row = b * Nmax + u;
-        if (tid < 32) row_normalisers(part, rows, row, L.chunks, a.k2, sh.bcast_f + 2);
-        __syncthreads();
-        for (int j = 0; j < 4; ++j) lse[j] = sh.bcast_f[2 + j];
-        __syncthreads();
-        c = 0.f;
-        N = 1.f;
-        int next = -1;
-        if (depth < a.max_depth) {
-            for (int ch = u + 1; ch < n; ++ch) {
-                if (sh.par[ch] != u) continue;
-                if (tid == 0) {
-                    const int x = sh.tok[ch];
-                    float ratio = 0.f;
-                    if (x >= 0 && x < V) {
-                        const float lp = (bf16_at(a.target + (size_t)row * V + x) - lse[0]) * a.k2 - lse[1];
-                        const float lq = (bf16_at(a.draft + (size_t)row * V + x) - lse[2]) * a.k2 - lse[3];
-                        ratio = fmaxf(ex2_approx(lp - lq) - c, 0.f) / N;
-                    }
-                    const float U = accept_uniform(a.seed, a.offset, b, ch);
-                    sh.bcast_i[1] = U < fminf(ratio, 1.f) ? 1 : 0;
+        if (tid == 0) {
+            int u = sh.st_u, depth = sh.st_depth, ch = sh.st_next;
+            float c = sh.st_c, N = sh.st_N;
+            int op = kWalkDone;
+            while (depth < a.max_depth && ch >= 0) {
+                const float *ls = sh.lse[u];
+                const float zp = sh.zp[ch], zq = sh.zq[ch];
+                float ratio = 0.f;
+                if (zp == zp) {                              // the token is in [0, V)
+                    const float lp = (zp - ls[0]) * a.k2 - ls[1];
+                    const float lq = (zq - ls[2]) * a.k2 - ls[3];
+                    ratio = fmaxf(ex2_approx(lp - lq) - c, 0.f) / N;
                 }
-                __syncthreads();
-                const int accepted = sh.bcast_i[1];
-                __syncthreads();
-                if (accepted) {
-                    next = ch;
-                    break;
-                }
-                c += N;                                      // the residual after this rejection
-                float mass;
-                int unused;
-                cluster_pass(sh, a, V, b, kOpMass, row, c, lse, mass, unused);
-                N = mass;
-                if (!(N > 0.f)) {                            // the residual vanished: sample from p
+                if (sh.u[ch] < fminf(ratio, 1.f)) {          // accepted: go down
+                    u = ch;
+                    sh.path[++depth] = u;
+                    ch = sh.first_child[u];
                     c = 0.f;
                     N = 1.f;
-                    break;
+                    continue;
                 }
+                c += N;                                      // rejected: the residual needs its mass
+                ch = sh.next_sib[ch];
+                op = kWalkMass;
+                break;
+            }
+            sh.st_u = u;
+            sh.st_depth = depth;
+            sh.st_next = ch;
+            sh.st_c = c;
+            sh.st_N = N;
+            sh.st_op = op;
+        }
+        __syncthreads();
+        const int op = sh.st_op, u = sh.st_u;
+        for (int j = 0; j < 4; ++j) lse[j] = sh.lse[u][j];
+        const float c = sh.st_c;
+        __syncthreads();
+        if (op == kWalkDone) break;
+        float mass;
+        int unused;
+        cluster_pass(sh, a, V, b, kOpMass, (int)(seq + u), c, lse, mass, unused);
+        if (tid == 0) {
+            if (mass > 0.f) {
+                sh.st_N = mass;
+            } else {                                         // the residual vanished: sample from p
+                sh.st_c = 0.f;
+                sh.st_N = 1.f;
+                sh.st_next = -1;
             }
         }
-        if (next < 0) break;
-        u = next;
-        ++depth;
-        if (tid == 0) sh.path[depth] = u;
+        __syncthreads();
     }
+    const int u = sh.st_u, depth = sh.st_depth;
     float key;
     int token;
-    cluster_pass(sh, a, V, b, kOpSample, b * Nmax + u, c, lse, key, token);
-    __syncthreads();
-    for (int k = tid; k <= a.max_depth; k += kSampleThreads) path_out[k] = k == 0 ? 0 : (k <= depth ? sh.path[k] : -1);
+    cluster_pass(sh, a, V, b, kOpSample, (int)(seq + u), sh.st_c, lse, key, token);
+    for (int k = tid; k <= a.max_depth; k += kSampleThreads) path_out[k] = k <= depth ? sh.path[k] : -1;
     if (tid == 0) {
         a.accept_len[b] = depth + 1;
         a.next_token[b] = token;
@@ -528,7 +619,7 @@ __global__ void __launch_bounds__(kSampleThreads)
 
 }  // namespace
 
-cudaError_t launch_sample(const Layout &L, const SampleArgs &a, uint8_t *ws, cudaStream_t s) {
+cudaError_t launch_sample(const Layout &L, const SampleArgs &a, uint8_t *ws, int sms, cudaStream_t s) {
     const int rows = L.B * L.Nmax;
     float2 *part = reinterpret_cast<float2 *>(ws + L.lse_off);
     trace_begin("lse_chunk", s);
@@ -538,14 +629,48 @@ cudaError_t launch_sample(const Layout &L, const SampleArgs &a, uint8_t *ws, cud
     trace_end(s);
     if (e != cudaSuccess) return e;
     trace_begin("sample_walk", s);
+    // 16 CTAs a sequence when the device schedules clusters of 16 and the
+    // batch leaves SMs for them, else 8 (the portable size)
+    static int big_ok = -1;
+    if (big_ok < 0) {
+        big_ok = 0;
+        if (cudaFuncSetAttribute(sample_walk_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+            cudaSuccess) {
+            cudaLaunchConfig_t probe{};
+            probe.gridDim = dim3(kSampleClusterBig, 1, 1);
+            probe.blockDim = dim3(kSampleThreads, 1, 1);
+            cudaLaunchAttribute ca[1];
+            ca[0].id = cudaLaunchAttributeClusterDimension;
+            ca[0].val.clusterDim.x = kSampleClusterBig;
+            ca[0].val.clusterDim.y = 1;
+            ca[0].val.clusterDim.z = 1;
+            probe.attrs = ca;
+            probe.numAttrs = 1;
+            int clusters = 0;
+            if (cudaOccupancyMaxActiveClusters(&clusters, sample_walk_kernel, &probe) == cudaSuccess && clusters > 0)
+                big_ok = 1;
+        }
+        cudaGetLastError();                                  // a refused query leaves no error behind
+    }
+    const int kc = (big_ok && L.B * kSampleClusterBig <= sms) ? kSampleClusterBig : kSampleCluster;
+    // room for the Gumbel noise of one CTA's vocabulary slice, if it fits
+    const size_t noise = (size_t)((L.V / 8 + kc - 1) / kc) * 32;
+    const size_t dyn = noise <= kSampleNoiseMax ? noise : 0;
+    static bool dyn_set = false;
+    if (!dyn_set) {
+        if (cudaFuncSetAttribute(sample_walk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kSampleNoiseMax) != cudaSuccess)
+            return cudaGetLastError();
+        dyn_set = true;
+    }
     cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(kSampleCluster, L.B, 1);
+    cfg.gridDim = dim3(kc, L.B, 1);
     cfg.blockDim = dim3(kSampleThreads, 1, 1);
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = dyn;
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kSampleCluster;
+    attr[0].val.clusterDim.x = kc;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
