@@ -120,7 +120,7 @@ constexpr float kNegInf = -__builtin_huge_valf();
 __device__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
     const unsigned long long t0 = globaltimer();
     while (!mbar_try_wait(bar, parity))
-        if (globaltimer() - t0 > kTimeoutNs / 8) return false;
+        if (globaltimer() - t0 > kDrainTimeoutNs) return false;
     return true;
 }
 

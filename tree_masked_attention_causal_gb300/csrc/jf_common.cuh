@@ -32,7 +32,13 @@ constexpr int kArgmaxCtasPerSm = 4;  // resident argmax CTAs per SM (64 register
 constexpr int kArgmaxMaxChunk = 76800;  // target bf16 of one logits row per CTA (150 KB)
 constexpr int kArgmaxGranule = kArgmaxThreads * 8;  // chunks are whole vectors per thread
 constexpr int kMaxSms = 256;      // SM count the workspace is sized for (the chunking uses the real one)
-constexpr unsigned long long kTimeoutNs = 2000000000ull;        // 2 s per wait
+// The limit of one wait. A test build shortens it (JF_WAIT_NS) to make a
+// wait run out; the drains at exit keep their own, longer limit.
+#ifndef JF_WAIT_NS
+#define JF_WAIT_NS 2000000000ull
+#endif
+constexpr unsigned long long kTimeoutNs = JF_WAIT_NS;             // 2 s per wait
+constexpr unsigned long long kDrainTimeoutNs = 250000000ull;      // 250 ms for a drain at exit
 
 __host__ __device__ constexpr int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
