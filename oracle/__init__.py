@@ -65,6 +65,8 @@ def _load():
             lib.oracle_tree_verify_sample.argtypes = [P, P, P, P, P, i32, i32, i64, i32, f64, u64, u64,
                                                       P, P, P, P]
             lib.oracle_tree_verify_sample.restype = None
+            lib.oracle_tree_score.argtypes = [P, P, P, P, i32, i32, i64, f64, i32, i32, P, P, P, P, P, P, P, P]
+            lib.oracle_tree_score.restype = None
             _lib = lib
     return _lib
 
@@ -199,3 +201,29 @@ def tree_verify_sample(target_logits, draft_logits, tokens, parents, n_nodes, ma
                                   float(temperature), int(seed), int(offset), _ptr(alen), _ptr(path),
                                   _ptr(nxt), _ptr(margins))
     return alen, path, nxt, margins
+
+
+def tree_score(draft_logits, tokens, parents, n_nodes, temperature: float, top_k: int = 0, budget: int = 0):
+    """Draft-side path scoring. Returns a dict with node_lp, path_lp [B, N]
+    (float64), topk_tok [B, N, top_k] (int32), topk_lp [B, N, top_k],
+    cand_parent, cand_token [B, budget] (int32), cand_score [B, budget] and
+    gaps [B] (the smallest score gap in and around each selection)."""
+    lib = _load()
+    dr = _u16(draft_logits)
+    B, N, V = dr.shape
+    tok, par, nn = _i32(tokens), _i32(parents), _i32(n_nodes)
+    k = max(0, int(top_k))
+    bud = max(0, int(budget))
+    out = dict(node_lp=np.empty((B, N)), path_lp=np.empty((B, N)),
+               topk_tok=np.empty((B, N, max(k, 1)), dtype=np.int32), topk_lp=np.empty((B, N, max(k, 1))),
+               cand_parent=np.empty((B, max(bud, 1)), dtype=np.int32),
+               cand_token=np.empty((B, max(bud, 1)), dtype=np.int32), cand_score=np.empty((B, max(bud, 1))),
+               gaps=np.empty(B))
+    lib.oracle_tree_score(_ptr(dr), _ptr(tok), _ptr(par), _ptr(nn), B, N, V, float(temperature), k, bud,
+                          _ptr(out["node_lp"]), _ptr(out["path_lp"]), _ptr(out["topk_tok"]), _ptr(out["topk_lp"]),
+                          _ptr(out["cand_parent"]), _ptr(out["cand_token"]), _ptr(out["cand_score"]),
+                          _ptr(out["gaps"]))
+    out["topk_tok"], out["topk_lp"] = out["topk_tok"][:, :, :k], out["topk_lp"][:, :, :k]
+    for key in ("cand_parent", "cand_token", "cand_score"):
+        out[key] = out[key][:, :bud]
+    return out

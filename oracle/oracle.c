@@ -41,7 +41,12 @@
  * numpy's Philox generator; the emitted tokens' distribution equals the
  * target's (chi-square) when children are drawn from the draft, at the
  * root and one level down; draft = target accepts every first child; a
- * near-zero temperature with a flat draft gives the greedy walk.
+ * near-zero temperature with a flat draft gives the greedy walk. Path
+ * scoring (tests/test_oracle_score_pins.py): torch.log_softmax gathered at
+ * the tokens; an ancestor-indicator matrix built by transitive closure;
+ * the frequency of drawing a path level by level; -depth ln V for uniform
+ * logits; a stable descending torch.sort for the top-k; a brute-force sort
+ * of every candidate for the budgeted expansion.
  */
 #include <math.h>
 #include <stdint.h>
@@ -474,4 +479,154 @@ void oracle_tree_verify_sample(const uint16_t *target, const uint16_t *draft, co
     free(p);
     free(q);
     free(r);
+}
+
+/*
+ * Draft-side path scoring. The blog's section "What JetFlow Does
+ * Differently": the draft probability of a path is a product of
+ * conditional distributions, each conditioned on the concrete ancestor
+ * tokens of that branch.
+ *
+ * For sequence b, node u's row draft[b][u] holds the draft's logits for u's
+ * children: log q_u(v) = z_v / T - log sum_w exp(z_w / T). Outputs:
+ *  - node_lp[b][c] = log q_{parent(c)}(tokens[b][c]) for 0 < c < n, 0 for
+ *    the root, -inf for a token outside [0, V); NaN on padding and on every
+ *    node of a malformed tree;
+ *  - path_lp[b][c] = the sum of node_lp over c's root path (the log of the
+ *    product of conditionals), the same conventions;
+ *  - with top_k > 0: the top_k most probable tokens of each node's row
+ *    (larger logit first, the lower index on ties) and their log q_u,
+ *    [B, Nmax, top_k] (-1 and NaN on padding / malformed);
+ *  - with budget > 0: the expansion under a budget, the `budget` best
+ *    candidates (u, v) among every node u < n and its top_k tokens v, by
+ *    path score path_lp[u] + log q_u(v), larger first, ties to the lower
+ *    (u, rank of v); [B, budget] parent node, token and score (-1, -1, NaN
+ *    when fewer candidates exist or the tree is malformed).
+ * Returns the smallest nonzero gap between consecutive candidate scores
+ * in each sequence's selection and at its boundary in gaps[b] (may be
+ * NULL), so that a test can tell orders another precision could make
+ * differently (exactly equal scores come from equal logits of one row and
+ * are ordered by rank in any precision).
+ */
+void oracle_tree_score(const uint16_t *draft, const int32_t *tokens, const int32_t *parents,
+                       const int32_t *n_nodes, int32_t B, int32_t Nmax, int64_t V, double temperature,
+                       int32_t top_k, int32_t budget, double *node_lp, double *path_lp, int32_t *topk_tok,
+                       double *topk_lp, int32_t *cand_parent, int32_t *cand_token, double *cand_score,
+                       double *gaps)
+{
+    double *lse = (double *)malloc(sizeof(double) * (size_t)Nmax);
+    int32_t *chain = (int32_t *)malloc(sizeof(int32_t) * (size_t)Nmax);
+    int64_t ncand_max = (int64_t)Nmax * (top_k > 0 ? top_k : 1);
+    double *cs = (double *)malloc(sizeof(double) * (size_t)ncand_max);
+    int32_t *cu = (int32_t *)malloc(sizeof(int32_t) * (size_t)ncand_max);
+    int32_t *cj = (int32_t *)malloc(sizeof(int32_t) * (size_t)ncand_max);
+    for (int32_t b = 0; b < B; ++b) {
+        const int32_t *par = parents + (int64_t)b * Nmax;
+        const int32_t *tok = tokens + (int64_t)b * Nmax;
+        const int32_t n = n_nodes[b];
+        const int ok = oracle_tree_is_valid(par, n, Nmax);
+        for (int32_t i = 0; i < Nmax; ++i) {
+            node_lp[(int64_t)b * Nmax + i] = NAN;
+            path_lp[(int64_t)b * Nmax + i] = NAN;
+            for (int32_t j = 0; j < top_k; ++j) {
+                topk_tok[((int64_t)b * Nmax + i) * top_k + j] = -1;
+                topk_lp[((int64_t)b * Nmax + i) * top_k + j] = NAN;
+            }
+        }
+        for (int32_t j = 0; j < budget; ++j) {
+            cand_parent[(int64_t)b * budget + j] = -1;
+            cand_token[(int64_t)b * budget + j] = -1;
+            cand_score[(int64_t)b * budget + j] = NAN;
+        }
+        if (gaps) gaps[b] = INFINITY;
+        if (!ok) continue;
+        for (int32_t u = 0; u < n; ++u) {
+            const uint16_t *z = draft + ((int64_t)b * Nmax + u) * V;
+            double m = -INFINITY, s = 0.0;
+            for (int64_t v = 0; v < V; ++v) {
+                const double x = bf16_to_double(z[v]) / temperature;
+                if (x > m) m = x;
+            }
+            for (int64_t v = 0; v < V; ++v) s += exp(bf16_to_double(z[v]) / temperature - m);
+            lse[u] = m + log(s);
+        }
+        for (int32_t c = 0; c < n; ++c) {
+            double lp = 0.0;
+            if (c > 0) {
+                const int32_t x = tok[c];
+                lp = (x >= 0 && x < V)
+                         ? bf16_to_double(draft[((int64_t)b * Nmax + par[c]) * V + x]) / temperature - lse[par[c]]
+                         : -INFINITY;
+            }
+            node_lp[(int64_t)b * Nmax + c] = lp;
+        }
+        for (int32_t c = 0; c < n; ++c) {          /* the product of conditionals along the root path */
+            const int32_t len = ancestor_chain(par, c, chain);
+            double sum = 0.0;
+            for (int32_t k = 0; k < len; ++k) sum += node_lp[(int64_t)b * Nmax + chain[k]];
+            path_lp[(int64_t)b * Nmax + c] = sum;
+        }
+        /* top_k of each row: a list kept sorted while the row is read in
+         * index order; an entry moves ahead only of strictly smaller ones,
+         * so among equal logits the lower index stays first */
+        for (int32_t u = 0; u < n && top_k > 0; ++u) {
+            const uint16_t *z = draft + ((int64_t)b * Nmax + u) * V;
+            int32_t *lt = topk_tok + ((int64_t)b * Nmax + u) * top_k;
+            double *lv = topk_lp + ((int64_t)b * Nmax + u) * top_k;   /* holds logits until the end */
+            int32_t cnt = 0;
+            for (int64_t v = 0; v < V; ++v) {
+                const double x = bf16_to_double(z[v]);
+                if (cnt == top_k && !(x > lv[top_k - 1])) continue;
+                int32_t pos = cnt < top_k ? cnt : top_k - 1;
+                while (pos > 0 && x > lv[pos - 1]) {
+                    lv[pos] = lv[pos - 1];
+                    lt[pos] = lt[pos - 1];
+                    --pos;
+                }
+                lv[pos] = x;
+                lt[pos] = (int32_t)v;
+                if (cnt < top_k) ++cnt;
+            }
+            for (int32_t j = 0; j < cnt; ++j) lv[j] = lv[j] / temperature - lse[u];
+        }
+        if (budget > 0 && top_k > 0) {
+            int64_t nc = 0;
+            for (int32_t u = 0; u < n; ++u)
+                for (int32_t j = 0; j < top_k; ++j) {
+                    if (topk_tok[((int64_t)b * Nmax + u) * top_k + j] < 0) continue;
+                    cs[nc] = path_lp[(int64_t)b * Nmax + u] + topk_lp[((int64_t)b * Nmax + u) * top_k + j];
+                    cu[nc] = u;
+                    cj[nc] = j;
+                    ++nc;
+                }
+            /* selection: take the best remaining candidate `budget` times */
+            char *used = (char *)calloc((size_t)(nc > 0 ? nc : 1), 1);
+            double prev = INFINITY;
+            for (int32_t r = 0; r < budget && r < nc; ++r) {
+                int64_t best = -1;
+                for (int64_t k = 0; k < nc; ++k) {
+                    if (used[k]) continue;
+                    if (best < 0 || cs[k] > cs[best]) best = k;   /* ties: the earlier (u, j) */
+                }
+                used[best] = 1;
+                cand_parent[(int64_t)b * budget + r] = cu[best];
+                cand_token[(int64_t)b * budget + r] = topk_tok[((int64_t)b * Nmax + cu[best]) * top_k + cj[best]];
+                cand_score[(int64_t)b * budget + r] = cs[best];
+                if (gaps && r > 0 && prev - cs[best] > 0.0 && prev - cs[best] < gaps[b]) gaps[b] = prev - cs[best];
+                prev = cs[best];
+            }
+            if (gaps && budget < nc) {               /* the boundary: the best candidate left out */
+                double out = -INFINITY;
+                for (int64_t k = 0; k < nc; ++k)
+                    if (!used[k] && cs[k] > out) out = cs[k];
+                if (prev - out > 0.0 && prev - out < gaps[b]) gaps[b] = prev - out;
+            }
+            free(used);
+        }
+    }
+    free(lse);
+    free(chain);
+    free(cs);
+    free(cu);
+    free(cj);
 }
