@@ -293,6 +293,15 @@ class Calls:
         self.RS = min(G, max(2, math.ceil(3 * L2_BYTES / self.sample_bytes)))
         self.scopies = [{k: sinp[k].to(dev) for k in snames} for _ in range(self.RS)]
         self.s_next = torch.empty(B, dtype=torch.int32, device=dev)
+        # path scoring on the same draft logits and trees: top 8 per node, 64 candidates
+        self.sc_k, self.sc_budget = 8, min(64, N * 8)
+        f32 = dict(dtype=torch.float32, device=dev)
+        self.sc_node, self.sc_path = torch.empty(B, N, **f32), torch.empty(B, N, **f32)
+        self.sc_ttok = torch.empty(B, N, self.sc_k, dtype=torch.int32, device=dev)
+        self.sc_tlp = torch.empty(B, N, self.sc_k, **f32)
+        self.sc_cpar = torch.empty(B, self.sc_budget, dtype=torch.int32, device=dev)
+        self.sc_ctok = torch.empty_like(self.sc_cpar)
+        self.sc_cscore = torch.empty(B, self.sc_budget, **f32)
         self.s_alen = torch.empty_like(self.alen)
         self.s_path = torch.empty_like(self.path)
 
@@ -325,6 +334,12 @@ class Calls:
                                       1.0, 1234, i, self.s_alen, self.s_path, self.s_next, self.shape, MAX_DEPTH,
                                       self.ws, status=self.status)
 
+    def score(self, i):
+        c = self.scopies[i % self.RS]
+        self.jb.jf_tree_score(c["draft_logits"], c["tokens"], c["parents"], c["n_nodes"], 1.0, self.sc_k,
+                              self.sc_budget, self.sc_node, self.sc_path, self.sc_ttok, self.sc_tlp, self.sc_cpar,
+                              self.sc_ctok, self.sc_cscore, self.shape, self.ws, status=self.status)
+
     def warm(self, n):
         for i in range(n):
             self.step(i)
@@ -338,6 +353,7 @@ class Calls:
             self.attn(i)
             self.commit(i)
             self.sample(i)
+            self.score(i)
         self.torch.cuda.synchronize()
         assert int(self.status.item()) == 0, f"{self.w.name}: device status flag raised by the commit"
 
@@ -355,7 +371,7 @@ class Calls:
         rows = int(self.inp["planted_len"].sum())
         return 2 * 2 * rows * Hkv * d * 2 + 4 * self.B * (MAX_DEPTH + 4)
 
-    def rooflines(self, attn_ms, verify_ms, commit_ms, pk, synth, sample_ms=None):
+    def rooflines(self, attn_ms, verify_ms, commit_ms, pk, synth, sample_ms=None, score_ms=None):
         inp, w = self.inp, self.w
         flops = synth.attention_flops(inp["parents"], inp["n_nodes"], inp["prefix_lens"], w.n_q_heads, w.head_dim)
         abytes = synth.attention_bytes(inp["prefix_lens"], inp["n_nodes"], w.n_q_heads, w.n_kv_heads, w.head_dim)
@@ -377,6 +393,10 @@ class Calls:
                 "sample_us": sample_ms * 1e3, "sample_bytes": 2 * vbytes,
                 "sample_gbs": 2 * vbytes / (sample_ms * 1e-3) / 1e9,
                 "sample_hbm_frac": 2 * vbytes / (sample_ms * 1e-3) / (pk["hbm_gbs"] * 1e9)}),
+            **({} if score_ms is None else {
+                "score_us": score_ms * 1e3, "score_bytes": vbytes,
+                "score_gbs": vbytes / (score_ms * 1e-3) / 1e9,
+                "score_hbm_frac": vbytes / (score_ms * 1e-3) / (pk["hbm_gbs"] * 1e9)}),
         }
 
 
@@ -426,6 +446,7 @@ def run_gpu(args, rank, world, local):
     graph = H.graph(H.step)
     launches_per_step = (jb.jf_kernel_launch_count() - launches0) / G
     g_attn, g_verify, g_commit, g_sample = H.graph(H.attn), H.graph(H.verify), H.graph(H.commit), H.graph(H.sample)
+    g_score = H.graph(H.score)
     max_kernels = 8
     events = [torch.cuda.Event(enable_timing=True) for _ in range(2 * max_kernels * G)]
     jb.jf_trace_kernels(events, max_kernels * G)
@@ -433,7 +454,7 @@ def run_gpu(args, rank, world, local):
     n_traced = jb.jf_trace_count()
     trace_names = [jb.jf_trace_name(k) for k in range(n_traced)]
     jb.jf_trace_kernels(None, 0)
-    for g in (graph, g_attn, g_verify, g_commit, g_sample, traced):      # untimed
+    for g in (graph, g_attn, g_verify, g_commit, g_sample, g_score, traced):      # untimed
         g.replay()
     torch.cuda.synchronize()
 
@@ -441,16 +462,16 @@ def run_gpu(args, rank, world, local):
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize()
-        t_step, t_attn, t_verify, t_commit, t_sample = time_graphs([graph, g_attn, g_verify, g_commit, g_sample], M,
-                                                                   torch)
+        t_step, t_attn, t_verify, t_commit, t_sample, t_score = time_graphs(
+            [graph, g_attn, g_verify, g_commit, g_sample, g_score], M, torch)
         traced.replay()
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
     clocks = clk.summary()
     assert int(H.status.item()) == 0, "device status flag raised in the timed region"
-    total_ms, attn_ms, verify_ms, commit_ms, sample_ms = max_over_ranks(
-        [t_step, t_attn / K, t_verify / K, t_commit / K, t_sample / K], world, dev)
+    total_ms, attn_ms, verify_ms, commit_ms, sample_ms, score_ms = max_over_ranks(
+        [t_step, t_attn / K, t_verify / K, t_commit / K, t_sample / K, t_score / K], world, dev)
 
     # per-kernel durations of the traced replay: each includes its launch
     # gap after the previous event, without programmatic overlap
@@ -512,7 +533,7 @@ def run_gpu(args, rank, world, local):
     e2e_ms = max_over_ranks([e0.elapsed_time(e1)], world, dev)[0]
     assert h_alen.tolist() == H.inp["planted_len"].tolist()
 
-    head = H.rooflines(attn_ms, verify_ms, commit_ms, pk, synth, sample_ms)
+    head = H.rooflines(attn_ms, verify_ms, commit_ms, pk, synth, sample_ms, score_ms)
     head["step_us"] = total_ms * 1e3 / K
     traffic = stored_traffic()
     cpu = time_oracle(H.inp, target_s=args.cpu_seconds) if rank == 0 else None
@@ -525,7 +546,7 @@ def run_gpu(args, rank, world, local):
     if args.configs:
         Kc = min(K, args.config_steps)
         Gc = graph_size(Kc)
-        del graph, g_attn, g_verify, g_commit, g_sample, traced
+        del graph, g_attn, g_verify, g_commit, g_sample, g_score, traced
         with ClockSampler(local) as clk2:
             for name, wc in synth.WORKLOADS.items():
                 if name == args.workload:
@@ -534,7 +555,7 @@ def run_gpu(args, rank, world, local):
                 else:
                     Hc = Calls(wc, dev, Gc, torch, jb, synth)
                     Hc.warm(3)
-                    gs = [Hc.graph(f) for f in (Hc.step, Hc.attn, Hc.verify, Hc.commit, Hc.sample)]
+                    gs = [Hc.graph(f) for f in (Hc.step, Hc.attn, Hc.verify, Hc.commit, Hc.sample, Hc.score)]
                     for g in gs:
                         g.replay()
                     torch.cuda.synchronize()
@@ -543,7 +564,7 @@ def run_gpu(args, rank, world, local):
                     ts = time_graphs(gs, Kc // Gc, torch)
                     assert int(Hc.status.item()) == 0, f"{name}: device status flag raised"
                     ts = max_over_ranks([t / Kc for t in ts], world, dev)
-                    rec = Hc.rooflines(ts[1], ts[2], ts[3], pk, synth, ts[4])
+                    rec = Hc.rooflines(ts[1], ts[2], ts[3], pk, synth, ts[4], ts[5])
                     rec.update({"step_us": ts[0] * 1e3, "steps": Kc,
                                 "l2": f"inputs rotate over {Hc.R} device copies "
                                       f"({Hc.R * Hc.step_bytes / 2**20:.0f} MB); attention-only calls over "
@@ -570,10 +591,11 @@ def run_gpu(args, rank, world, local):
                           "note": "all replicas together; value and e2e are per step of one replica "
                                   "(the slowest rank)"},
             "attn_us": head["attn_us"], "verify_us": head["verify_us"], "commit_us": head["commit_us"],
-            "sample_us": head["sample_us"],
+            "sample_us": head["sample_us"], "score_us": head["score_us"],
             "call_timing": "graphs of back-to-back jf_tree_attention calls, of jf_tree_verify calls, of "
-                           "jf_tree_commit_kv calls and of jf_tree_verify_sample calls (T = 1, a new Philox "
-                           "offset each), K each, events on the launch stream, same clock window as the steps",
+                           "jf_tree_commit_kv calls, of jf_tree_verify_sample calls (T = 1, a new Philox "
+                           "offset each) and of jf_tree_score calls (top 8, 64 candidates), K each, events on the "
+                           "launch stream, same clock window as the steps",
             "kernel_us": {n: v * 1e3 for n, v in avg.items()},
             "kernel_timing": "event pair around each kernel in a traced copy of the step graph; each figure "
                              "includes the kernel's launch gap and loses the programmatic overlap",

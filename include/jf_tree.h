@@ -233,6 +233,45 @@ JF_API int32_t jf_tree_verify_sample(const void *target_logits, const void *draf
                                      size_t workspace_bytes, int32_t *status, jf_stream_t stream);
 
 /*
+ * Draft-side path scoring: the step before verification. The blog's
+ * section "What JetFlow Does Differently": a path's draft probability is
+ * the product of conditional distributions, each on the concrete ancestor
+ * tokens of its branch. Row u of draft_logits holds the draft's logits for
+ * node u's children: log q_u(v) = z_v / T - log sum_w exp(z_w / T).
+ *
+ *   draft_logits     bf16 [B, Nmax, V], finite values
+ *   tree_tokens, parents, n_nodes as for jf_tree_verify
+ *   temperature      > 0 and finite
+ *   top_k            0..16: how many of each row's most probable tokens to
+ *                    report (the larger logit first, the lower index on ties)
+ *   budget           0..Nmax * top_k (0 when top_k = 0): how many expansion
+ *                    candidates to select
+ *   node_logprob_out float32 [B, Nmax]: log q_{parent(c)}(tree_tokens[c]),
+ *                    0 for the root, -inf for a token outside [0, V)
+ *   path_logprob_out float32 [B, Nmax]: the sum of node_logprob over the
+ *                    node's root path (the log of the path's probability)
+ *   topk_token_out   int32 [B, Nmax, top_k] (NULL when top_k = 0)
+ *   topk_logprob_out float32 [B, Nmax, top_k]: log q_u of those tokens
+ *   cand_parent_out, cand_token_out int32 [B, budget], cand_score_out
+ *                    float32 [B, budget] (NULL when budget = 0): the
+ *                    `budget` best candidates (u, v) among every node u and
+ *                    its top_k tokens, by path score path_logprob[u] +
+ *                    log q_u(v), larger first, ties to the lower (u, rank)
+ * Padding nodes and every node of a malformed tree get NaN (-1 for the
+ * integers), and a malformed tree raises JF_STATUS_BAD_TREE. The
+ * arithmetic is fp32; the selection orders by fp32 scores. The workspace
+ * is the one jf_workspace_bytes(shape) sizes. Returns as jf_tree_verify.
+ */
+JF_API int32_t jf_tree_score(const void *draft_logits, const int32_t *tree_tokens,
+                             const int32_t *parents, const int32_t *n_nodes, float temperature,
+                             int32_t top_k, int32_t budget, float *node_logprob_out,
+                             float *path_logprob_out, int32_t *topk_token_out,
+                             float *topk_logprob_out, int32_t *cand_parent_out,
+                             int32_t *cand_token_out, float *cand_score_out,
+                             const jf_shape *shape, void *workspace, size_t workspace_bytes,
+                             int32_t *status, jf_stream_t stream);
+
+/*
  * Accepted-path KV commit: the step after verification (the paper's section
  * 2.1 "Background": the prefix the target accepts extends the context). The
  * keys and values of the accepted nodes were computed by this tree's

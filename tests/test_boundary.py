@@ -69,7 +69,8 @@ def test_argmax_chunks_on_152_sms(rows, V, expect):
                                           (1, 152, 151936, 6)])
 def test_argmax_chunk_rule(lib, B, N, V, expect):
     """The verify region of the workspace holds one int2 per (row, chunk),
-    and the sampling region two float2 (target and draft): their growth from
+    the sampling region two float2 (target and draft) and the scoring
+    region 16 (value, index) pairs: their growth from
     a one-chunk vocabulary pins the chunk count they are sized for (256 SMs,
     the bound for any device's chunking)."""
     assert _argmax_chunks(B * N, V) == expect
@@ -77,7 +78,8 @@ def test_argmax_chunk_rule(lib, B, N, V, expect):
     base = jb.jf_workspace_bytes(jb.make_shape(B, 0, 0, 0, N, 0, 8))
     ws = jb.jf_workspace_bytes(jb.make_shape(B, 0, 0, 0, N, 0, V))
     rows = B * N
-    assert ws - base == (align(rows * expect * 8) + align(2 * rows * expect * 8)) - (align(rows * 8) + align(2 * rows * 8))
+    regions = lambda c: align(rows * c * 8) + align(2 * rows * c * 8) + align(rows * c * 16 * 8)
+    assert ws - base == regions(expect) - regions(1)
 
 
 A16 = 1 << 20            # fake 16-byte-aligned addresses: never dereferenced
@@ -233,3 +235,42 @@ def test_binding_refuses_strided_tensors(lib):
     with pytest.raises(ValueError):
         jb.jf_tree_verify(t, A16, A16, A16, A16, A16, None, good_shape(), 4, A16 * 2, workspace_bytes=1 << 30,
                           stream=0, check=False)
+
+
+def score(shape, top_k=4, budget=8, temperature=1.0, ws_bytes=None, **over):
+    args = dict(draft=A16, tokens=A16, parents=A16, n_nodes=A16, node=A16, path=A16, ttok=A16, tlp=A16,
+                cpar=A16, ctok=A16, cscore=A16, workspace=A16 * 2)
+    args.update(over)
+    if ws_bytes is None:
+        ws_bytes = jb.jf_workspace_bytes(shape)
+    return jb.jf_tree_score(args["draft"], args["tokens"], args["parents"], args["n_nodes"], temperature, top_k,
+                            budget, args["node"], args["path"], args["ttok"], args["tlp"], args["cpar"],
+                            args["ctok"], args["cscore"], shape, args["workspace"], ws_bytes, stream=0, check=False)
+
+
+@pytest.mark.parametrize("name", ["draft", "tokens", "parents", "n_nodes", "node", "path", "ttok", "tlp", "cpar",
+                                  "ctok", "cscore", "workspace"])
+def test_score_null_pointer(lib, name):
+    assert score(good_shape(), **{name: None}) == jb.JF_ERR_NULL
+
+
+def test_score_optional_outputs_may_be_null_when_unused(lib):
+    # nothing to report -> the optional outputs are not needed; the call then
+    # fails only at the device step on this machine (no GPU), not on NULLs
+    rc = score(good_shape(), top_k=0, budget=0, ttok=None, tlp=None, cpar=None, ctok=None, cscore=None)
+    assert rc not in (jb.JF_ERR_NULL, jb.JF_ERR_SHAPE, jb.JF_ERR_ALIGN, jb.JF_ERR_WORKSPACE)
+
+
+@pytest.mark.parametrize("kw", [dict(top_k=-1), dict(top_k=17), dict(budget=-1), dict(top_k=0, budget=1),
+                                dict(top_k=2, budget=64 * 2 + 1), dict(temperature=0.0),
+                                dict(temperature=float("nan")), dict(temperature=float("inf"))])
+def test_score_bad_arguments(lib, kw):
+    assert score(good_shape(), **kw) == jb.JF_ERR_SHAPE
+
+
+def test_score_bad_shape_alignment_workspace(lib):
+    assert score(good_shape(vocab=1001)) == jb.JF_ERR_SHAPE
+    assert score(good_shape(), draft=A16 + 2) == jb.JF_ERR_ALIGN
+    assert score(good_shape(), workspace=A16 + 16) == jb.JF_ERR_ALIGN
+    s = good_shape()
+    assert score(s, ws_bytes=jb.jf_workspace_bytes(s) - 1) == jb.JF_ERR_WORKSPACE

@@ -81,6 +81,9 @@ def _configure(lib: ctypes.CDLL) -> ctypes.CDLL:
         lib.jf_tree_verify_sample.argtypes = [P, P, P, P, P, ctypes.c_float, u64, u64, P, P, P, sp, i32, P, sz,
                                               P, P]
         lib.jf_tree_verify_sample.restype = i32
+        f32 = ctypes.c_float
+        lib.jf_tree_score.argtypes = [P, P, P, P, f32, i32, i32, P, P, P, P, P, P, P, sp, P, sz, P, P]
+        lib.jf_tree_score.restype = i32
     return lib
 
 
@@ -168,6 +171,24 @@ def jf_tree_verify_sample(target_logits, draft_logits, tree_tokens, parents, n_n
                                       int(workspace_bytes), _ptr(status), _stream(stream))
     if check and rc != JF_OK:
         raise JfError("jf_tree_verify_sample", rc)
+    return rc
+
+
+def jf_tree_score(draft_logits, tree_tokens, parents, n_nodes, temperature: float, top_k: int, budget: int,
+                  node_logprob_out, path_logprob_out, topk_token_out, topk_logprob_out, cand_parent_out,
+                  cand_token_out, cand_score_out, shape: JfShape, workspace, workspace_bytes: Optional[int] = None,
+                  status=None, stream=None, check: bool = True) -> int:
+    """Draft-side path scoring: node and path log-probabilities, each
+    node's top-k tokens and the budgeted expansion (see jf_tree.h)."""
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    rc = load().jf_tree_score(_ptr(draft_logits), _ptr(tree_tokens), _ptr(parents), _ptr(n_nodes),
+                              float(temperature), int(top_k), int(budget), _ptr(node_logprob_out),
+                              _ptr(path_logprob_out), _ptr(topk_token_out), _ptr(topk_logprob_out),
+                              _ptr(cand_parent_out), _ptr(cand_token_out), _ptr(cand_score_out), ctypes.byref(shape),
+                              _ptr(workspace), int(workspace_bytes), _ptr(status), _stream(stream))
+    if check and rc != JF_OK:
+        raise JfError("jf_tree_score", rc)
     return rc
 
 

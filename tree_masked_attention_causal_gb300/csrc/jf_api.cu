@@ -293,6 +293,52 @@ JF_API int32_t jf_tree_verify_sample(const void *target_logits, const void *draf
     return JF_OK;
 }
 
+JF_API int32_t jf_tree_score(const void *draft_logits, const int32_t *tree_tokens, const int32_t *parents,
+                             const int32_t *n_nodes, float temperature, int32_t top_k, int32_t budget,
+                             float *node_logprob_out, float *path_logprob_out, int32_t *topk_token_out,
+                             float *topk_logprob_out, int32_t *cand_parent_out, int32_t *cand_token_out,
+                             float *cand_score_out, const jf_shape *shape, void *workspace, size_t workspace_bytes,
+                             int32_t *status, jf_stream_t stream) {
+    if (!draft_logits || !tree_tokens || !parents || !n_nodes || !node_logprob_out || !path_logprob_out || !shape ||
+        !workspace)
+        return JF_ERR_NULL;
+    if (top_k > 0 && (!topk_token_out || !topk_logprob_out)) return JF_ERR_NULL;
+    if (budget > 0 && (!cand_parent_out || !cand_token_out || !cand_score_out)) return JF_ERR_NULL;
+    const int32_t sc = check_shape(shape, true, false);
+    if (sc != JF_OK) return sc;
+    if (!(temperature > 0.0f) || isinf(temperature)) return JF_ERR_SHAPE;
+    if (top_k < 0 || top_k > kScoreMaxK || budget < 0 || (budget > 0 && top_k == 0) ||
+        (long long)budget > (long long)shape->max_nodes * top_k)
+        return JF_ERR_SHAPE;
+    if (!aligned16(draft_logits) || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return JF_ERR_ALIGN;
+    if (workspace_bytes < jf_workspace_bytes(shape)) return JF_ERR_WORKSPACE;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return JF_ERR_CUDA;
+    const int sms = num_sms_cached(dev);
+    if (sms <= 0) return JF_ERR_CUDA;
+    const Layout L = layout_of(shape, sms);
+    ScoreArgs a{};
+    a.draft = reinterpret_cast<const __nv_bfloat16 *>(draft_logits);
+    a.tokens = tree_tokens;
+    a.parents = parents;
+    a.n_nodes = n_nodes;
+    a.node_lp = node_logprob_out;
+    a.path_lp = path_logprob_out;
+    a.topk_token = topk_token_out;
+    a.topk_lp = topk_logprob_out;
+    a.cand_parent = cand_parent_out;
+    a.cand_token = cand_token_out;
+    a.cand_score = cand_score_out;
+    a.status = status;
+    a.k2 = 1.4426950408889634f / temperature;
+    a.top_k = top_k;
+    a.budget = budget;
+    if (launch_score(L, a, reinterpret_cast<uint8_t *>(workspace), reinterpret_cast<cudaStream_t>(stream)) !=
+        cudaSuccess)
+        return JF_ERR_CUDA;
+    return JF_OK;
+}
+
 JF_API int32_t jf_tree_commit_kv(const void *tree_k, const void *tree_v, const int32_t *n_nodes,
                                  const int32_t *accept_len, const int32_t *accept_path, void *k_cache,
                                  void *v_cache, int32_t *prefix_lens, const jf_shape *shape, int32_t max_depth,

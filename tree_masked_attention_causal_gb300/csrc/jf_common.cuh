@@ -31,6 +31,7 @@ constexpr int kArgmaxVecs = 8;    // 16-byte loads in flight per thread
 constexpr int kArgmaxCtasPerSm = 4;  // resident argmax CTAs per SM (64 registers: no spills)
 constexpr int kArgmaxMaxChunk = 76800;  // target bf16 of one logits row per CTA (150 KB)
 constexpr int kArgmaxGranule = kArgmaxThreads * 8;  // chunks are whole vectors per thread
+constexpr int kScoreMaxK = 16;    // top-k of the path scoring, at most
 constexpr int kMaxSms = 256;      // SM count the workspace is sized for (the chunking uses the real one)
 // The limit of one wait. A test build shortens it (JF_WAIT_NS) to make a
 // wait run out; the drains at exit keep their own, longer limit.
@@ -67,6 +68,7 @@ struct Layout {
     size_t qtab_off, ml_off, opart_off;
     size_t amp_off;
     size_t lse_off;      // stochastic verify: (max, sum) per (target | draft, row, chunk)
+    size_t topk_off;     // path scoring: kScoreMaxK (value, index) per (row, chunk)
     size_t total;
 };
 
@@ -107,6 +109,7 @@ inline Layout make_layout(int B, int Nmax, int Hq, int Hkv, int D, int Pcap, int
     L.opart_off = take(2 * (size_t)L.max_pieces * kRows * D);   // fp16 rows, divided by l, scaled by 2^-e per half
     L.amp_off = take(sizeof(int2) * (size_t)B * Nmax * L.chunks);
     L.lse_off = take(2 * sizeof(float2) * (size_t)B * Nmax * L.chunks);
+    L.topk_off = take((sizeof(float) + sizeof(int)) * kScoreMaxK * (size_t)B * Nmax * L.chunks);
     L.total = off;
     return L;
 }
@@ -629,6 +632,17 @@ struct SampleArgs {
     int32_t max_depth;
 };
 cudaError_t launch_sample(const Layout &L, const SampleArgs &a, uint8_t *ws, int sms, cudaStream_t s);
+
+// Draft-side path scoring (jf_score.cu).
+struct ScoreArgs {
+    const __nv_bfloat16 *draft;
+    const int32_t *tokens, *parents, *n_nodes;
+    float *node_lp, *path_lp, *topk_lp, *cand_score;
+    int32_t *topk_token, *cand_parent, *cand_token, *status;
+    float k2;                 // log2(e) / temperature
+    int32_t top_k, budget;
+};
+cudaError_t launch_score(const Layout &L, const ScoreArgs &a, uint8_t *ws, cudaStream_t s);
 
 // Host-side launch bookkeeping (jf_api.cu): counts launches and records the
 // armed trace events around each one.
