@@ -285,6 +285,13 @@ class Calls:
         self.pl_slots = self.pl_saved.clone()
         self.c_alen = torch.empty_like(self.alen)
         self.c_path = torch.empty_like(self.path)
+        # the same prefix caches as 16-row pages of a shuffled pool
+        pg = synth.paged_layout(inp["k_cache"], inp["v_cache"], inp["prefix_lens"], 16, seed=w.seed)
+        pool_bytes = 2 * pg["k_pages"].numel() * 2
+        self.RP = min(G, max(2, math.ceil(3 * L2_BYTES / pool_bytes)))
+        self.pages = [dict(k=pg["k_pages"].to(dev), v=pg["v_pages"].to(dev)) for _ in range(self.RP)]
+        self.block_table = pg["block_table"].to(dev)
+        self.num_pages = pg["num_pages"]
         # stochastic verification: target and draft logits with trees whose
         # tokens a sampling draft proposed, rotated like the other inputs
         sinp = synth.make_sample_inputs(w)
@@ -328,6 +335,12 @@ class Calls:
         self.jb.jf_tree_commit_kv(c["tree_k"], c["tree_v"], c["n_nodes"], self.c_alen, self.c_path, self.kc, self.vc,
                                   self.pl_slots[i % self.G], self.shape_c, MAX_DEPTH, status=self.status)
 
+    def attn_paged(self, i):
+        c, pg = self.acopies[i % self.RA], self.pages[i % self.RP]
+        self.jb.jf_tree_attention_paged(c["q"], pg["k"], pg["v"], self.block_table, 16, self.num_pages,
+                                        c["prefix_lens"], c["tree_k"], c["tree_v"], c["parents"], c["n_nodes"],
+                                        self.out, self.shape, self.ws, status=self.status)
+
     def sample(self, i):
         c = self.scopies[i % self.RS]
         self.jb.jf_tree_verify_sample(c["target_logits"], c["draft_logits"], c["tokens"], c["parents"], c["n_nodes"],
@@ -354,6 +367,7 @@ class Calls:
             self.commit(i)
             self.sample(i)
             self.score(i)
+            self.attn_paged(i)
         self.torch.cuda.synchronize()
         assert int(self.status.item()) == 0, f"{self.w.name}: device status flag raised by the commit"
 
@@ -371,7 +385,7 @@ class Calls:
         rows = int(self.inp["planted_len"].sum())
         return 2 * 2 * rows * Hkv * d * 2 + 4 * self.B * (MAX_DEPTH + 4)
 
-    def rooflines(self, attn_ms, verify_ms, commit_ms, pk, synth, sample_ms=None, score_ms=None):
+    def rooflines(self, attn_ms, verify_ms, commit_ms, pk, synth, sample_ms=None, score_ms=None, paged_ms=None):
         inp, w = self.inp, self.w
         flops = synth.attention_flops(inp["parents"], inp["n_nodes"], inp["prefix_lens"], w.n_q_heads, w.head_dim)
         abytes = synth.attention_bytes(inp["prefix_lens"], inp["n_nodes"], w.n_q_heads, w.n_kv_heads, w.head_dim)
@@ -393,6 +407,9 @@ class Calls:
                 "sample_us": sample_ms * 1e3, "sample_bytes": 2 * vbytes,
                 "sample_gbs": 2 * vbytes / (sample_ms * 1e-3) / 1e9,
                 "sample_hbm_frac": 2 * vbytes / (sample_ms * 1e-3) / (pk["hbm_gbs"] * 1e9)}),
+            **({} if paged_ms is None else {
+                "attn_paged_us": paged_ms * 1e3,
+                "attn_paged_roofline_frac": max(t_flop, t_byte) / (paged_ms * 1e-3)}),
             **({} if score_ms is None else {
                 "score_us": score_ms * 1e3, "score_bytes": vbytes,
                 "score_gbs": vbytes / (score_ms * 1e-3) / 1e9,
@@ -446,7 +463,7 @@ def run_gpu(args, rank, world, local):
     graph = H.graph(H.step)
     launches_per_step = (jb.jf_kernel_launch_count() - launches0) / G
     g_attn, g_verify, g_commit, g_sample = H.graph(H.attn), H.graph(H.verify), H.graph(H.commit), H.graph(H.sample)
-    g_score = H.graph(H.score)
+    g_score, g_paged = H.graph(H.score), H.graph(H.attn_paged)
     max_kernels = 8
     events = [torch.cuda.Event(enable_timing=True) for _ in range(2 * max_kernels * G)]
     jb.jf_trace_kernels(events, max_kernels * G)
@@ -454,7 +471,7 @@ def run_gpu(args, rank, world, local):
     n_traced = jb.jf_trace_count()
     trace_names = [jb.jf_trace_name(k) for k in range(n_traced)]
     jb.jf_trace_kernels(None, 0)
-    for g in (graph, g_attn, g_verify, g_commit, g_sample, g_score, traced):      # untimed
+    for g in (graph, g_attn, g_verify, g_commit, g_sample, g_score, g_paged, traced):      # untimed
         g.replay()
     torch.cuda.synchronize()
 
@@ -462,16 +479,16 @@ def run_gpu(args, rank, world, local):
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize()
-        t_step, t_attn, t_verify, t_commit, t_sample, t_score = time_graphs(
-            [graph, g_attn, g_verify, g_commit, g_sample, g_score], M, torch)
+        t_step, t_attn, t_verify, t_commit, t_sample, t_score, t_paged = time_graphs(
+            [graph, g_attn, g_verify, g_commit, g_sample, g_score, g_paged], M, torch)
         traced.replay()
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
     clocks = clk.summary()
     assert int(H.status.item()) == 0, "device status flag raised in the timed region"
-    total_ms, attn_ms, verify_ms, commit_ms, sample_ms, score_ms = max_over_ranks(
-        [t_step, t_attn / K, t_verify / K, t_commit / K, t_sample / K, t_score / K], world, dev)
+    total_ms, attn_ms, verify_ms, commit_ms, sample_ms, score_ms, paged_ms = max_over_ranks(
+        [t_step, t_attn / K, t_verify / K, t_commit / K, t_sample / K, t_score / K, t_paged / K], world, dev)
 
     # per-kernel durations of the traced replay: each includes its launch
     # gap after the previous event, without programmatic overlap
@@ -533,7 +550,7 @@ def run_gpu(args, rank, world, local):
     e2e_ms = max_over_ranks([e0.elapsed_time(e1)], world, dev)[0]
     assert h_alen.tolist() == H.inp["planted_len"].tolist()
 
-    head = H.rooflines(attn_ms, verify_ms, commit_ms, pk, synth, sample_ms, score_ms)
+    head = H.rooflines(attn_ms, verify_ms, commit_ms, pk, synth, sample_ms, score_ms, paged_ms)
     head["step_us"] = total_ms * 1e3 / K
     traffic = stored_traffic()
     cpu = time_oracle(H.inp, target_s=args.cpu_seconds) if rank == 0 else None
@@ -546,7 +563,7 @@ def run_gpu(args, rank, world, local):
     if args.configs:
         Kc = min(K, args.config_steps)
         Gc = graph_size(Kc)
-        del graph, g_attn, g_verify, g_commit, g_sample, g_score, traced
+        del graph, g_attn, g_verify, g_commit, g_sample, g_score, g_paged, traced
         with ClockSampler(local) as clk2:
             for name, wc in synth.WORKLOADS.items():
                 if name == args.workload:
@@ -555,7 +572,8 @@ def run_gpu(args, rank, world, local):
                 else:
                     Hc = Calls(wc, dev, Gc, torch, jb, synth)
                     Hc.warm(3)
-                    gs = [Hc.graph(f) for f in (Hc.step, Hc.attn, Hc.verify, Hc.commit, Hc.sample, Hc.score)]
+                    gs = [Hc.graph(f) for f in (Hc.step, Hc.attn, Hc.verify, Hc.commit, Hc.sample, Hc.score,
+                                                Hc.attn_paged)]
                     for g in gs:
                         g.replay()
                     torch.cuda.synchronize()
@@ -564,7 +582,7 @@ def run_gpu(args, rank, world, local):
                     ts = time_graphs(gs, Kc // Gc, torch)
                     assert int(Hc.status.item()) == 0, f"{name}: device status flag raised"
                     ts = max_over_ranks([t / Kc for t in ts], world, dev)
-                    rec = Hc.rooflines(ts[1], ts[2], ts[3], pk, synth, ts[4], ts[5])
+                    rec = Hc.rooflines(ts[1], ts[2], ts[3], pk, synth, ts[4], ts[5], ts[6])
                     rec.update({"step_us": ts[0] * 1e3, "steps": Kc,
                                 "l2": f"inputs rotate over {Hc.R} device copies "
                                       f"({Hc.R * Hc.step_bytes / 2**20:.0f} MB); attention-only calls over "
@@ -591,10 +609,11 @@ def run_gpu(args, rank, world, local):
                           "note": "all replicas together; value and e2e are per step of one replica "
                                   "(the slowest rank)"},
             "attn_us": head["attn_us"], "verify_us": head["verify_us"], "commit_us": head["commit_us"],
-            "sample_us": head["sample_us"], "score_us": head["score_us"],
+            "sample_us": head["sample_us"], "score_us": head["score_us"], "attn_paged_us": head["attn_paged_us"],
             "call_timing": "graphs of back-to-back jf_tree_attention calls, of jf_tree_verify calls, of "
                            "jf_tree_commit_kv calls, of jf_tree_verify_sample calls (T = 1, a new Philox "
-                           "offset each) and of jf_tree_score calls (top 8, 64 candidates), K each, events on the "
+                           "offset each), of jf_tree_score calls (top 8, 64 candidates) and of "
+                           "jf_tree_attention_paged calls (16-row pages of a shuffled pool), K each, events on the "
                            "launch stream, same clock window as the steps",
             "kernel_us": {n: v * 1e3 for n, v in avg.items()},
             "kernel_timing": "event pair around each kernel in a traced copy of the step graph; each figure "

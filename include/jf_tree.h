@@ -152,6 +152,31 @@ JF_API int32_t jf_tree_attention(const void *q, const void *k_cache, const void 
                                  jf_stream_t stream);
 
 /*
+ * Tree attention over a paged prefix cache: jf_tree_attention with the
+ * prefix keys and values in fixed-size pages reached through a block table
+ * (the cache layout of paged serving engines), so that sequences share one
+ * page pool. Row p of sequence b's prefix, KV head h, is
+ *   k_pages[block_table[b, p / page_size], p % page_size, h, :]
+ * (v_pages alike). Everything else is as for jf_tree_attention.
+ *
+ *   k_pages, v_pages bf16 [num_pages, page_size, Hkv, d]
+ *   block_table      int32 [B, prefix_cap / page_size]; entries for pages
+ *                    past ceil(prefix_lens[b] / page_size) are never read
+ *   page_size        a power of two from 8 to 128 dividing shape->prefix_cap
+ *                    (else JF_ERR_SHAPE)
+ *   num_pages        pages in the pool, >= 1
+ * A used block-table entry outside [0, num_pages) makes the sequence
+ * malformed: NaN rows and JF_STATUS_BAD_TREE.
+ */
+JF_API int32_t jf_tree_attention_paged(const void *q, const void *k_pages, const void *v_pages,
+                                       const int32_t *block_table, int32_t page_size, int32_t num_pages,
+                                       const int32_t *prefix_lens, const void *tree_k,
+                                       const void *tree_v, const int32_t *parents,
+                                       const int32_t *n_nodes, void *out, const jf_shape *shape,
+                                       void *workspace, size_t workspace_bytes, int32_t *status,
+                                       jf_stream_t stream);
+
+/*
  * Greedy tree verification.
  *
  * am[b,i] = argmax_v logits[b,i,v] for i < n_nodes[b], the lowest index on

@@ -227,3 +227,29 @@ def tree_score(draft_logits, tokens, parents, n_nodes, temperature: float, top_k
     for key in ("cand_parent", "cand_token", "cand_score"):
         out[key] = out[key][:, :bud]
     return out
+
+
+def gather_pages(pages, block_table, prefix_lens, page_size: int, prefix_cap: int) -> np.ndarray:
+    """A paged cache [num_pages, page_size, Hkv, d] (bf16 bits) as the
+    contiguous [B, Hkv, prefix_cap, d] cache it stands for: row p of
+    sequence b, head h is pages[block_table[b, p // page_size], p % page_size,
+    h]. Rows at or past prefix_lens[b] are left 0 (never attended)."""
+    pg = _u16(pages)
+    tab = _i32(block_table)
+    pl = _i32(prefix_lens)
+    B = tab.shape[0]
+    Hkv, d = pg.shape[2], pg.shape[3]
+    out = np.zeros((B, Hkv, prefix_cap, d), dtype=np.uint16)
+    for b in range(B):
+        for p in range(int(pl[b])):
+            out[b, :, p, :] = pg[tab[b, p // page_size], p % page_size, :, :]
+    return out
+
+
+def tree_attention_paged(q, k_pages, v_pages, block_table, page_size: int, prefix_cap: int, prefix_lens, tree_k,
+                         tree_v, parents, n_nodes, scale: float = 0.0, sel=None) -> np.ndarray:
+    """Tree attention over a paged prefix cache: the pages gathered into the
+    contiguous cache they stand for, then tree_attention."""
+    kc = gather_pages(k_pages, block_table, prefix_lens, page_size, prefix_cap)
+    vc = gather_pages(v_pages, block_table, prefix_lens, page_size, prefix_cap)
+    return tree_attention(q, kc, vc, prefix_lens, tree_k, tree_v, parents, n_nodes, scale=scale, sel=sel)

@@ -274,3 +274,29 @@ def test_score_bad_shape_alignment_workspace(lib):
     assert score(good_shape(), workspace=A16 + 16) == jb.JF_ERR_ALIGN
     s = good_shape()
     assert score(s, ws_bytes=jb.jf_workspace_bytes(s) - 1) == jb.JF_ERR_WORKSPACE
+
+
+def paged(shape, page_size=16, num_pages=64, **over):
+    args = dict(q=A16, kp=A16, vp=A16, table=A16, prefix_lens=A16, tree_k=A16, tree_v=A16, parents=A16,
+                n_nodes=A16, out=A16, workspace=A16 * 2)
+    args.update(over)
+    return jb.jf_tree_attention_paged(args["q"], args["kp"], args["vp"], args["table"], page_size, num_pages,
+                                      args["prefix_lens"], args["tree_k"], args["tree_v"], args["parents"],
+                                      args["n_nodes"], args["out"], shape, args["workspace"], workspace_bytes=1 << 40,
+                                      stream=0, check=False)
+
+
+@pytest.mark.parametrize("name", ["q", "kp", "vp", "table", "prefix_lens", "tree_k", "tree_v", "parents", "n_nodes",
+                                  "out", "workspace"])
+def test_paged_null_pointer(lib, name):
+    assert paged(good_shape(prefix_cap=1024), **{name: None}) == jb.JF_ERR_NULL
+
+
+@pytest.mark.parametrize("ps,npages,cap", [(0, 64, 1024), (12, 64, 1024), (4, 64, 1024), (256, 64, 1024),
+                                           (64, 64, 1000), (16, 0, 1024)])
+def test_paged_bad_geometry(lib, ps, npages, cap):
+    assert paged(good_shape(prefix_cap=cap), page_size=ps, num_pages=npages) == jb.JF_ERR_SHAPE
+
+
+def test_paged_misaligned(lib):
+    assert paged(good_shape(prefix_cap=1024), kp=A16 + 8) == jb.JF_ERR_ALIGN

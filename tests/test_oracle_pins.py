@@ -442,3 +442,38 @@ def test_commit_then_attention_equals_chain_attention():
         got = oracle.tree_attention(q[:, i:i + 1], k2, v2, torch.full((B,), P + i, dtype=torch.int32),
                                     tk[:, i:i + 1], tv[:, i:i + 1], one, torch.ones(B, dtype=torch.int32))
         np.testing.assert_allclose(got[:, 0], ref[:, i], rtol=0, atol=1e-12)
+
+
+def test_gather_pages_picks_the_documented_element():
+    """Row p of sequence b, head h is pages[table[b, p // ps], p % ps, h]:
+    checked on a pool whose every element encodes its own coordinates."""
+    num_pages, ps, Hkv, d = 6, 4, 2, 3
+    pages = np.zeros((num_pages, ps, Hkv, d), dtype=np.uint16)
+    for ph in range(num_pages):
+        for r in range(ps):
+            for h in range(Hkv):
+                for c in range(d):
+                    pages[ph, r, h, c] = ph * 1000 + r * 100 + h * 10 + c
+    table = np.array([[4, 1, 5], [0, 3, -1]], dtype=np.int32)
+    lens = np.array([11, 6], dtype=np.int32)
+    out = oracle.gather_pages(pages, table, lens, ps, 12)
+    for b in range(2):
+        for p in range(12):
+            for h in range(Hkv):
+                want = [table[b, p // ps] * 1000 + (p % ps) * 100 + h * 10 + c for c in range(d)] if p < lens[b] \
+                    else [0] * d
+                assert out[b, h, p].tolist() == want
+
+
+def test_paged_layout_round_trip_and_attention():
+    c = random_case(11, B=3, N=9, Pcap=48, prefix=torch.tensor([48, 5, 0], dtype=torch.int32))
+    pg = synth.paged_layout(c["k_cache"], c["v_cache"], c["prefix_lens"], 8, seed=2)
+    kc = oracle.gather_pages(pg["k_pages"], pg["block_table"], c["prefix_lens"], 8, 48)
+    ref_k = c["k_cache"].view(torch.int16).numpy().view(np.uint16)
+    for b in range(3):
+        P = int(c["prefix_lens"][b])
+        np.testing.assert_array_equal(kc[b, :, :P], ref_k[b, :, :P])
+    a = oracle.tree_attention_paged(c["q"], pg["k_pages"], pg["v_pages"], pg["block_table"], 8, 48,
+                                    c["prefix_lens"], c["tree_k"], c["tree_v"], c["parents"], c["n_nodes"])
+    b_ = run_oracle(c)
+    np.testing.assert_array_equal(a, b_)

@@ -61,6 +61,8 @@ def _configure(lib: ctypes.CDLL) -> ctypes.CDLL:
         lib.jf_workspace_bytes.restype = sz
         lib.jf_tree_attention.argtypes = [P, P, P, P, P, P, P, P, P, sp, P, sz, P, P]
         lib.jf_tree_attention.restype = i32
+        lib.jf_tree_attention_paged.argtypes = [P, P, P, P, i32, i32, P, P, P, P, P, P, sp, P, sz, P, P]
+        lib.jf_tree_attention_paged.restype = i32
         lib.jf_tree_verify.argtypes = [P, P, P, P, P, P, P, sp, i32, P, sz, P, P]
         lib.jf_tree_verify.restype = i32
         lib.jf_status_string.argtypes = [i32]
@@ -139,6 +141,22 @@ def jf_tree_attention(q, k_cache, v_cache, prefix_lens, tree_k, tree_v, parents,
                                   _ptr(workspace), int(workspace_bytes), _ptr(status), _stream(stream))
     if check and rc != JF_OK:
         raise JfError("jf_tree_attention", rc)
+    return rc
+
+
+def jf_tree_attention_paged(q, k_pages, v_pages, block_table, page_size: int, num_pages: int, prefix_lens, tree_k,
+                            tree_v, parents, n_nodes, out, shape: JfShape, workspace,
+                            workspace_bytes: Optional[int] = None, status=None, stream=None,
+                            check: bool = True) -> int:
+    """Tree attention over a paged prefix cache (see jf_tree.h)."""
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    rc = load().jf_tree_attention_paged(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table), int(page_size),
+                                        int(num_pages), _ptr(prefix_lens), _ptr(tree_k), _ptr(tree_v), _ptr(parents),
+                                        _ptr(n_nodes), _ptr(out), ctypes.byref(shape), _ptr(workspace),
+                                        int(workspace_bytes), _ptr(status), _stream(stream))
+    if check and rc != JF_OK:
+        raise JfError("jf_tree_attention_paged", rc)
     return rc
 
 

@@ -175,15 +175,28 @@ JF_API const char *jf_status_string(int32_t code) {
     return "unknown status code";
 }
 
-JF_API int32_t jf_tree_attention(const void *q, const void *k_cache, const void *v_cache, const int32_t *prefix_lens,
-                                 const void *tree_k, const void *tree_v, const int32_t *parents,
-                                 const int32_t *n_nodes, void *out, const jf_shape *shape, void *workspace,
-                                 size_t workspace_bytes, int32_t *status, jf_stream_t stream) {
+// The attention call over a contiguous cache (page_size 0) or a paged one.
+static int32_t attention_call(const void *q, const void *k_cache, const void *v_cache, const int32_t *block_table,
+                              int32_t page_size, int32_t num_pages, const int32_t *prefix_lens, const void *tree_k,
+                              const void *tree_v, const int32_t *parents, const int32_t *n_nodes, void *out,
+                              const jf_shape *shape, void *workspace, size_t workspace_bytes, int32_t *status,
+                              jf_stream_t stream) {
     if (!q || !k_cache || !v_cache || !prefix_lens || !tree_k || !tree_v || !parents || !n_nodes || !out || !shape ||
-        !workspace)
+        !workspace || (page_size > 0 && !block_table))
         return JF_ERR_NULL;
     const int32_t sc = check_shape(shape, false, true);
     if (sc != JF_OK) return sc;
+    int page_lg = -1;
+    if (page_size > 0) {
+        page_lg = 0;
+        while ((1 << page_lg) < page_size) ++page_lg;
+        // a power of two from 8 to 128 (whole 1024-byte swizzle atoms, at most
+        // one tile), a whole number of pages per sequence, and page rows
+        // addressable in 32 bits
+        if ((1 << page_lg) != page_size || page_size < 8 || page_size > kBN || shape->prefix_cap % page_size ||
+            num_pages < 1 || (long long)num_pages * page_size > 0x7FFFFFFFll)
+            return JF_ERR_SHAPE;
+    }
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(tree_k) || !aligned16(tree_v) ||
         !aligned16(out) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return JF_ERR_ALIGN;
@@ -200,8 +213,14 @@ JF_API int32_t jf_tree_attention(const void *q, const void *k_cache, const void 
     AttnMaps maps;
     const uint64_t e2 = 2;   // bytes per bf16
     bool ok = encode3d(&maps.q, q, D, Hq, (uint64_t)B * N, e2 * D, e2 * D * Hq, 64, L.G, L.NB);
-    ok = ok && encode3d(&maps.k_cache, k_cache, D, Pcap, (uint64_t)B * Hkv, e2 * D, e2 * D * Pcap, 64, kBN, 1);
-    ok = ok && encode3d(&maps.v_cache, v_cache, D, Pcap, (uint64_t)B * Hkv, e2 * D, e2 * D * Pcap, 64, kBN, 1);
+    if (page_size > 0) {     // [num_pages, page_size, Hkv, d]: one box is one page of one head
+        const uint64_t rows = (uint64_t)num_pages * page_size;
+        ok = ok && encode3d(&maps.k_cache, k_cache, D, Hkv, rows, e2 * D, e2 * D * Hkv, 64, 1, page_size);
+        ok = ok && encode3d(&maps.v_cache, v_cache, D, Hkv, rows, e2 * D, e2 * D * Hkv, 64, 1, page_size);
+    } else {
+        ok = ok && encode3d(&maps.k_cache, k_cache, D, Pcap, (uint64_t)B * Hkv, e2 * D, e2 * D * Pcap, 64, kBN, 1);
+        ok = ok && encode3d(&maps.v_cache, v_cache, D, Pcap, (uint64_t)B * Hkv, e2 * D, e2 * D * Pcap, 64, kBN, 1);
+    }
     ok = ok && encode3d(&maps.tree_k, tree_k, D, Hkv, (uint64_t)B * N, e2 * D, e2 * D * Hkv, 64, 1, kBN);
     ok = ok && encode3d(&maps.tree_v, tree_v, D, Hkv, (uint64_t)B * N, e2 * D, e2 * D * Hkv, 64, 1, kBN);
     ok = ok && encode3d(&maps.out, out, D, Hq, (uint64_t)B * N, e2 * D, e2 * D * Hq, 64, L.G, L.NB);
@@ -219,11 +238,34 @@ JF_API int32_t jf_tree_attention(const void *q, const void *k_cache, const void 
     const float scale = shape->scale > 0.f ? shape->scale : 1.0f / sqrtf((float)D);
     args.scale_log2 = scale * 1.4426950408889634f;
     args.num_ctas = sms < kMaxCtas ? sms : kMaxCtas;
+    args.block_table = block_table;
+    args.page_lg = page_lg;
+    args.pages_per_seq = page_size > 0 ? Pcap / page_size : 0;
+    args.num_pages = page_size > 0 ? num_pages : 0;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (launch_tree_attention(L, maps, args, s) != cudaSuccess) return JF_ERR_CUDA;
     if (launch_split_combine(L, args, s) != cudaSuccess) return JF_ERR_CUDA;
     return JF_OK;
+}
+
+JF_API int32_t jf_tree_attention(const void *q, const void *k_cache, const void *v_cache, const int32_t *prefix_lens,
+                                 const void *tree_k, const void *tree_v, const int32_t *parents,
+                                 const int32_t *n_nodes, void *out, const jf_shape *shape, void *workspace,
+                                 size_t workspace_bytes, int32_t *status, jf_stream_t stream) {
+    return attention_call(q, k_cache, v_cache, nullptr, 0, 0, prefix_lens, tree_k, tree_v, parents, n_nodes, out,
+                          shape, workspace, workspace_bytes, status, stream);
+}
+
+JF_API int32_t jf_tree_attention_paged(const void *q, const void *k_pages, const void *v_pages,
+                                       const int32_t *block_table, int32_t page_size, int32_t num_pages,
+                                       const int32_t *prefix_lens, const void *tree_k, const void *tree_v,
+                                       const int32_t *parents, const int32_t *n_nodes, void *out,
+                                       const jf_shape *shape, void *workspace, size_t workspace_bytes,
+                                       int32_t *status, jf_stream_t stream) {
+    if (page_size <= 0) return JF_ERR_SHAPE;
+    return attention_call(q, k_pages, v_pages, block_table, page_size, num_pages, prefix_lens, tree_k, tree_v,
+                          parents, n_nodes, out, shape, workspace, workspace_bytes, status, stream);
 }
 
 JF_API int32_t jf_tree_verify(const void *logits, const int32_t *tree_tokens, const int32_t *parents,

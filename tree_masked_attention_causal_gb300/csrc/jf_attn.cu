@@ -124,6 +124,32 @@ __device__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
     return true;
 }
 
+// Prefix tile t of KV head kh of sequence b (keys t * 128 ..) into the
+// shared tile at dst: one box per 64 columns from the contiguous cache, or,
+// paged, one box per page and 64 columns, lane j loading page j. Pages past
+// the sequence's last one (the tile's ragged end, masked later) reload that
+// last page, so no block-table entry past the prefix is read. Called by the
+// whole warp after lane 0 has set the barrier's expected bytes.
+template <int D>
+__device__ __forceinline__ void load_prefix_tile(const CUtensorMap *map, const AttnArgs &a, const Layout &L,
+                                                 uint32_t dst, int b, int kh, int P, int t, uint32_t bar, int lane) {
+    using C = AttnCfg<D>;
+    if (a.page_lg < 0) {
+        if (lane == 0)
+            for (int dc = 0; dc < C::kBoxes; ++dc)
+                tma_load_3d(dst + dc * (kBN * 128), map, dc * 64, t * kBN, b * L.Hkv + kh, bar);
+        return;
+    }
+    const int lg = a.page_lg, per_tile = kBN >> lg;
+    if (lane < per_tile) {
+        const int last = max(0, ((P + (1 << lg) - 1) >> lg) - 1);
+        const int page = min((t << (7 - lg)) + lane, last);
+        const int phys = a.block_table[(size_t)b * a.pages_per_seq + page];
+        for (int dc = 0; dc < C::kBoxes; ++dc)
+            tma_load_3d(dst + dc * (kBN * 128) + (lane << lg) * 128, map, dc * 64, kh, phys << lg, bar);
+    }
+}
+
 template <int D>
 __device__ __forceinline__ void producer_loop(const AttnMaps &maps, const Layout &L, const AttnArgs &a,
                                               uint32_t sbase, uint32_t bars, ItemInfo *items_s,
@@ -172,16 +198,16 @@ __device__ __forceinline__ void producer_loop(const AttnMaps &maps, const Layout
             return true;
         }
 #endif
-        if (lane == 0) {
-            mbar_arrive_expect_tx(bar(C::B_K_FULL + ks), C::kTileBytes);
-            for (int dc = 0; dc < C::kBoxes; ++dc) {
-                const uint32_t dst = sbase + C::k_off + ks * C::kTileBytes + dc * (kBN * 128);
-                if (tree)
-                    tma_load_3d(dst, &maps.tree_k, dc * 64, info.kh, info.b * L.Nmax + (t - info.t_pre) * kBN,
-                                bar(C::B_K_FULL + ks));
-                else
-                    tma_load_3d(dst, &maps.k_cache, dc * 64, t * kBN, info.b * L.Hkv + info.kh, bar(C::B_K_FULL + ks));
-            }
+        if (lane == 0) mbar_arrive_expect_tx(bar(C::B_K_FULL + ks), C::kTileBytes);
+        __syncwarp();
+        const uint32_t dst = sbase + C::k_off + ks * C::kTileBytes;
+        if (tree) {
+            if (lane == 0)
+                for (int dc = 0; dc < C::kBoxes; ++dc)
+                    tma_load_3d(dst + dc * (kBN * 128), &maps.tree_k, dc * 64, info.kh,
+                                info.b * L.Nmax + (t - info.t_pre) * kBN, bar(C::B_K_FULL + ks));
+        } else {
+            load_prefix_tile<D>(&maps.k_cache, a, L, dst, info.b, info.kh, info.P, t, bar(C::B_K_FULL + ks), lane);
         }
         __syncwarp();
         ++kc;
@@ -305,17 +331,17 @@ __device__ __forceinline__ void v_producer_loop(const AttnMaps &maps, const Layo
                 const bool tree = t >= info.t_pre;
                 const int vs = vc % C::NV;
                 if (!mbar_wait(bar(C::B_V_EMPTY + vs), ((vc / C::NV) & 1) ^ 1, abort, a.status)) { ok = false; break; }
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(bar(C::B_V_FULL + vs), C::kTileBytes);
-                    for (int dc = 0; dc < C::kBoxes; ++dc) {
-                        const uint32_t dst = sbase + C::v_off + vs * C::kTileBytes + dc * (kBN * 128);
-                        if (tree)
-                            tma_load_3d(dst, &maps.tree_v, dc * 64, info.kh,
+                if (lane == 0) mbar_arrive_expect_tx(bar(C::B_V_FULL + vs), C::kTileBytes);
+                __syncwarp();
+                const uint32_t dst = sbase + C::v_off + vs * C::kTileBytes;
+                if (tree) {
+                    if (lane == 0)
+                        for (int dc = 0; dc < C::kBoxes; ++dc)
+                            tma_load_3d(dst + dc * (kBN * 128), &maps.tree_v, dc * 64, info.kh,
                                         info.b * L.Nmax + (t - info.t_pre) * kBN, bar(C::B_V_FULL + vs));
-                        else
-                            tma_load_3d(dst, &maps.v_cache, dc * 64, t * kBN, info.b * L.Hkv + info.kh,
-                                        bar(C::B_V_FULL + vs));
-                    }
+                } else {
+                    load_prefix_tile<D>(&maps.v_cache, a, L, dst, info.b, info.kh, info.P, t, bar(C::B_V_FULL + vs),
+                                        lane);
                 }
                 __syncwarp();
                 ++vc;

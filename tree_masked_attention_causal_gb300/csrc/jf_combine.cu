@@ -61,6 +61,13 @@ __global__ void __launch_bounds__(kCombineThreads, 4) split_combine_kernel(const
         const int p = a.parents[(size_t)b * L.Nmax + i];
         bad = (i == 0) ? (p != -1) : (p < 0 || p >= i);
     }
+    if (!bad && a.page_lg >= 0) {                          // every page the prefix uses is a real page
+        const int used = (P + (1 << a.page_lg) - 1) >> a.page_lg;
+        for (int j = i; !bad && j < used; j += blockDim.x) {
+            const int ph = a.block_table[(size_t)b * a.pages_per_seq + j];
+            bad = ph < 0 || ph >= a.num_pages;
+        }
+    }
     bad = __syncthreads_or(bad);
     pdl_wait_prior_grid();          // the attention grid is complete from here on
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;

@@ -605,6 +605,13 @@ struct AttnArgs {
     int32_t *status;
     float scale_log2;
     int32_t num_ctas;    // persistent grid size of the attention kernel
+    // Paged prefix cache (page_lg >= 0): page j of sequence b is physical
+    // page block_table[b * pages_per_seq + j] of a [num_pages, 2^page_lg,
+    // Hkv, d] array; the k_cache / v_cache maps then cover that array.
+    const int32_t *block_table;
+    int32_t page_lg;     // log2 of the page size, -1 for the contiguous cache
+    int32_t pages_per_seq;
+    int32_t num_pages;
 };
 
 cudaError_t launch_tree_attention(const Layout &L, const AttnMaps &m, const AttnArgs &a,

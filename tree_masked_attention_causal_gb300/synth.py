@@ -219,6 +219,39 @@ def make_logits(gen: torch.Generator, B: int, N: int, vocab: int,
     return logits
 
 
+def paged_layout(k_cache: torch.Tensor, v_cache: torch.Tensor, prefix_lens: torch.Tensor, page_size: int,
+                 seed: int = 0, spare: int = 3, spare_fill: float = float("nan")) -> Dict[str, object]:
+    """The same prefix caches as pages of a shared pool, in a shuffled order.
+
+      k_pages, v_pages  bf16 [num_pages, page_size, Hkv, d]: page j of
+                        sequence b holds rows j*page_size .. of its cache
+      block_table       int32 [B, Pcap / page_size]: the physical page of each
+                        used logical page; -1 past the prefix
+      num_pages         the used pages plus `spare` pages filled with
+                        spare_fill (never referenced)
+    """
+    B, Hkv, Pcap, d = k_cache.shape
+    assert Pcap % page_size == 0
+    per_seq = Pcap // page_size
+    used = [-(-int(prefix_lens[b]) // page_size) for b in range(B)]
+    num_pages = sum(used) + spare
+    gen = torch.Generator().manual_seed(seed)
+    perm = torch.randperm(num_pages, generator=gen).tolist()
+    k_pages = torch.full((num_pages, page_size, Hkv, d), spare_fill, dtype=torch.bfloat16)
+    v_pages = torch.full_like(k_pages, spare_fill)
+    table = torch.full((B, per_seq), -1, dtype=torch.int32)
+    nxt = 0
+    for b in range(B):
+        for j in range(used[b]):
+            phys = perm[nxt]
+            nxt += 1
+            table[b, j] = phys
+            rows = slice(j * page_size, (j + 1) * page_size)
+            k_pages[phys] = k_cache[b, :, rows].transpose(0, 1)
+            v_pages[phys] = v_cache[b, :, rows].transpose(0, 1)
+    return dict(k_pages=k_pages, v_pages=v_pages, block_table=table, num_pages=num_pages, page_size=page_size)
+
+
 # Draft logits of the sampling inputs are N(0, SAMPLE_SCALE^2); the
 # target's are the draft's plus SAMPLE_NOISE * N(0, 1), so that the target
 # agrees with the draft often but not always.
