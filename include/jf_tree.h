@@ -334,6 +334,24 @@ JF_API int32_t jf_tree_commit_kv(const void *tree_k, const void *tree_v, const i
                                  int32_t max_depth, int32_t *status, jf_stream_t stream);
 
 /*
+ * The accepted-path KV commit into a paged cache (the pool and block table
+ * of jf_tree_attention_paged): jf_tree_commit_kv with row p of sequence b
+ * stored at k_pages[block_table[b, p / page_size], p % page_size, h, :]
+ * (v_pages alike). The pages that receive rows P .. P + a - 1 must already
+ * be in the sequence's block table; a request is also malformed
+ * (JF_STATUS_BAD_TREE, nothing changes) if one of them lies outside
+ * [0, num_pages). The capacity is shape->prefix_cap (= block-table width x
+ * page_size); page_size and num_pages as for jf_tree_attention_paged.
+ */
+JF_API int32_t jf_tree_commit_kv_paged(const void *tree_k, const void *tree_v,
+                                       const int32_t *n_nodes, const int32_t *accept_len,
+                                       const int32_t *accept_path, void *k_pages, void *v_pages,
+                                       const int32_t *block_table, int32_t page_size,
+                                       int32_t num_pages, int32_t *prefix_lens,
+                                       const jf_shape *shape, int32_t max_depth, int32_t *status,
+                                       jf_stream_t stream);
+
+/*
  * Allocation-free variant of jf_tree_verify. The paper has no counterpart:
  * this entry point exists for callers that cannot allocate device memory.
  * Examples: code running inside a CUDA graph capture, a custom allocator

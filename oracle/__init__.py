@@ -67,6 +67,8 @@ def _load():
             lib.oracle_tree_verify_sample.restype = None
             lib.oracle_tree_score.argtypes = [P, P, P, P, i32, i32, i64, f64, i32, i32, P, P, P, P, P, P, P, P]
             lib.oracle_tree_score.restype = None
+            lib.oracle_commit_kv_paged.argtypes = [P, P, P, P, P, P, P, P, i32, i32, i32, P, i32, i32, i32, i32, i32, P]
+            lib.oracle_commit_kv_paged.restype = None
             _lib = lib
     return _lib
 
@@ -253,3 +255,20 @@ def tree_attention_paged(q, k_pages, v_pages, block_table, page_size: int, prefi
     kc = gather_pages(k_pages, block_table, prefix_lens, page_size, prefix_cap)
     vc = gather_pages(v_pages, block_table, prefix_lens, page_size, prefix_cap)
     return tree_attention(q, kc, vc, prefix_lens, tree_k, tree_v, parents, n_nodes, scale=scale, sel=sel)
+
+
+def commit_kv_paged(tree_k, tree_v, n_nodes, accept_len, accept_path, k_pages, v_pages, block_table,
+                    page_size: int, prefix_lens, max_depth: int):
+    """The KV commit into a paged cache. Returns (k_pages, v_pages) as
+    updated uint16 copies, prefix_lens and flags (int32)."""
+    lib = _load()
+    tk, tv = _u16(tree_k), _u16(tree_v)
+    B, N, Hkv, d = tk.shape
+    kp, vp = _u16(k_pages).copy(), _u16(v_pages).copy()
+    tab = _i32(block_table)
+    pl = _i32(prefix_lens).copy()
+    flags = np.empty(B, dtype=np.int32)
+    lib.oracle_commit_kv_paged(_ptr(tk), _ptr(tv), _ptr(_i32(n_nodes)), _ptr(_i32(accept_len)),
+                               _ptr(_i32(accept_path)), _ptr(kp), _ptr(vp), _ptr(tab), int(page_size), kp.shape[0],
+                               tab.shape[1], _ptr(pl), B, N, Hkv, d, int(max_depth), _ptr(flags))
+    return kp, vp, pl, flags

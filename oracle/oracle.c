@@ -630,3 +630,56 @@ void oracle_tree_score(const uint16_t *draft, const int32_t *tokens, const int32
     free(cu);
     free(cj);
 }
+
+/*
+ * The accepted-path KV commit into a paged cache: the same request as
+ * oracle_commit_kv, with row p of sequence b, head h stored at
+ * k_pages[block_table[b][p / page_size]][p % page_size][h] (v_pages alike),
+ * pages [num_pages, page_size, Hkv, d], block_table [B, pages_per_seq], the
+ * capacity pages_per_seq * page_size. A request is also malformed (flags 1)
+ * if a page holding one of rows P .. P + a - 1 is outside [0, num_pages).
+ */
+void oracle_commit_kv_paged(const uint16_t *tree_k, const uint16_t *tree_v, const int32_t *n_nodes,
+                            const int32_t *accept_len, const int32_t *accept_path, uint16_t *k_pages,
+                            uint16_t *v_pages, const int32_t *block_table, int32_t page_size, int32_t num_pages,
+                            int32_t pages_per_seq, int32_t *prefix_lens, int32_t B, int32_t Nmax, int32_t Hkv,
+                            int32_t d, int32_t max_depth, int32_t *flags)
+{
+    const int32_t Pcap = pages_per_seq * page_size;
+    for (int32_t b = 0; b < B; ++b) {
+        const int32_t a = accept_len[b], P = prefix_lens[b], n = n_nodes[b];
+        const int32_t *path = accept_path + (int64_t)b * (max_depth + 1);
+        const int32_t *table = block_table + (int64_t)b * pages_per_seq;
+        flags[b] = 0;
+        if (a == 0) continue;
+        int bad = n < 1 || n > Nmax || a < 0 || a > n || a > max_depth + 1 || P < 0 || P > Pcap;
+        for (int32_t k = 0; !bad && k < a; ++k)
+            if (path[k] < 0 || path[k] >= n) bad = 1;
+        if (!bad && P + a <= Pcap)
+            for (int32_t k = 0; k < a; ++k) {
+                const int32_t ph = table[(P + k) / page_size];
+                if (ph < 0 || ph >= num_pages) bad = 1;
+            }
+        if (bad) {
+            flags[b] = 1;
+            continue;
+        }
+        if (P + a > Pcap) {
+            flags[b] = 2;
+            continue;
+        }
+        for (int32_t k = 0; k < a; ++k) {
+            const int32_t row = P + k, node = path[k];
+            const int64_t page = table[row / page_size];
+            for (int32_t h = 0; h < Hkv; ++h) {
+                const int64_t src = (((int64_t)b * Nmax + node) * Hkv + h) * d;
+                const int64_t dst = ((page * page_size + row % page_size) * Hkv + h) * d;
+                for (int32_t e = 0; e < d; ++e) {
+                    k_pages[dst + e] = tree_k[src + e];
+                    v_pages[dst + e] = tree_v[src + e];
+                }
+            }
+        }
+        prefix_lens[b] = P + a;
+    }
+}

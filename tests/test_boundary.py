@@ -300,3 +300,20 @@ def test_paged_bad_geometry(lib, ps, npages, cap):
 
 def test_paged_misaligned(lib):
     assert paged(good_shape(prefix_cap=1024), kp=A16 + 8) == jb.JF_ERR_ALIGN
+
+
+def test_paged_commit_arguments(lib):
+    def call(shape, ps=16, npages=64, md=16, **over):
+        args = dict(tk=A16, tv=A16, n=A16, a=A16, p=A16, kp=A16, vp=A16, t=A16, pl=A16)
+        args.update(over)
+        return jb.jf_tree_commit_kv_paged(args["tk"], args["tv"], args["n"], args["a"], args["p"], args["kp"],
+                                          args["vp"], args["t"], ps, npages, args["pl"], shape, md, stream=0,
+                                          check=False)
+    s = good_shape(prefix_cap=1024)
+    for name in ("tk", "tv", "n", "a", "p", "kp", "vp", "t", "pl"):
+        assert call(s, **{name: None}) == jb.JF_ERR_NULL
+    for ps, npages in ((12, 64), (4, 64), (256, 64), (16, 0)):
+        assert call(s, ps=ps, npages=npages) == jb.JF_ERR_SHAPE
+    assert call(good_shape(prefix_cap=1000), ps=64) == jb.JF_ERR_SHAPE
+    assert call(s, md=-1) == jb.JF_ERR_SHAPE
+    assert call(s, kp=A16 + 8) == jb.JF_ERR_ALIGN

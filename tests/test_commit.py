@@ -132,3 +132,103 @@ def test_commit_then_attention_sees_the_committed_rows():
         out, st = run_attention(dev1, shape_of(one))
         assert st == 0
         assert_attention_close(out_f64(out), ref[:, i:i + 1], [(b, 0) for b in range(B)], f"node {i}", strict=True)
+
+
+def full_tables(pg, prefix_cap):
+    """Give every sequence a page for every row it may hold (its unused
+    entries get fresh pages at the end of the pool), as a serving engine
+    would before a commit."""
+    table = pg["block_table"].clone()
+    nxt = pg["num_pages"]
+    per_seq = table.shape[1]
+    for b in range(table.shape[0]):
+        for j in range(per_seq):
+            if table[b, j] < 0:
+                table[b, j] = nxt
+                nxt += 1
+    shp = pg["k_pages"].shape[1:]
+    kp = torch.cat([pg["k_pages"], torch.zeros((nxt - pg["num_pages"],) + tuple(shp), dtype=torch.bfloat16)])
+    vp = torch.cat([pg["v_pages"], torch.zeros((nxt - pg["num_pages"],) + tuple(shp), dtype=torch.bfloat16)])
+    return kp, vp, table, nxt
+
+
+@pytest.mark.parametrize("page_size", [8, 64])
+def test_paged_commit_matches_oracle(page_size):
+    """Verify, then commit into a paged pool: every page, the prefix lengths
+    and the flags against the oracle; one sequence without room."""
+    inp = small_inputs(63, B=5, N=40, Hq=8, Hkv=2, d=128, Pcap=128, vocab=8,
+                       prefixes=torch.tensor([100, 0, 125, 64, 128], dtype=torch.int32))
+    dev = to_dev(inp)
+    shape = shape_of(inp)
+    md = 16
+    a = torch.empty(5, dtype=torch.int32, device="cuda")
+    p = torch.empty(5, md + 1, dtype=torch.int32, device="cuda")
+    jb.jf_tree_verify(dev["logits"], dev["tokens"], dev["parents"], dev["n_nodes"], a, p, None, shape, md,
+                      new_workspace(shape))
+    pg = synth.paged_layout(inp["k_cache"], inp["v_cache"], inp["prefix_lens"], page_size, seed=9, spare_fill=0.0)
+    kp, vp, table, num_pages = full_tables(pg, 128)
+    kpd, vpd, pld = kp.cuda(), vp.cuda(), inp["prefix_lens"].cuda()
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    jb.jf_tree_commit_kv_paged(dev["tree_k"], dev["tree_v"], dev["n_nodes"], a, p, kpd, vpd, table.cuda(), page_size,
+                               num_pages, pld, shape, md, status=st)
+    torch.cuda.synchronize()
+    rk, rv, rpl, rfl = oracle.commit_kv_paged(inp["tree_k"], inp["tree_v"], inp["n_nodes"], a.cpu(), p.cpu(), kp, vp,
+                                              table, page_size, inp["prefix_lens"], md)
+    np.testing.assert_array_equal(pld.cpu().numpy(), rpl)
+    np.testing.assert_array_equal(_bits(kpd), rk)
+    np.testing.assert_array_equal(_bits(vpd), rv)
+    assert bool(int(st.item()) & jb.JF_STATUS_CACHE_FULL) == bool((rfl == 2).any())
+    assert (rfl == 2).any() and (rfl == 0).sum() >= 3
+
+
+def test_paged_chain_equals_contiguous_chain():
+    """Paged attention, commit into pages, paged attention again: bit for
+    bit what the contiguous calls give; a bad page flags its sequence."""
+    B, N, Hq, Hkv, d, Pcap = 3, 24, 8, 2, 128, 256
+    inp = small_inputs(64, B=B, N=N, Hq=Hq, Hkv=Hkv, d=d, Pcap=Pcap,
+                       prefixes=torch.tensor([100, 17, 200], dtype=torch.int32))
+    from helpers import run_attention
+    shape = shape_of(inp)
+    dev = to_dev(inp)
+    alen = torch.tensor([5, 3, 4], dtype=torch.int32)
+    path = torch.full((B, 17), -1, dtype=torch.int32)
+    for b in range(B):
+        node, chain = 0, [0]
+        while len(chain) < int(alen[b]):
+            kids = [c for c in range(N) if int(inp["parents"][b, c]) == node]
+            if not kids:
+                break
+            node = kids[0]
+            chain.append(node)
+        alen[b] = len(chain)
+        path[b, :len(chain)] = torch.tensor(chain)
+    # contiguous chain
+    kc, vc, plc = dev["k_cache"].clone(), dev["v_cache"].clone(), dev["prefix_lens"].clone()
+    jb.jf_tree_commit_kv(dev["tree_k"], dev["tree_v"], dev["n_nodes"], alen.cuda(), path.cuda(), kc, vc, plc, shape, 16)
+    dev2 = dict(dev)
+    dev2.update(k_cache=kc, v_cache=vc, prefix_lens=plc)
+    ref, _ = run_attention(dev2, shape)
+    # paged chain
+    pg = synth.paged_layout(inp["k_cache"], inp["v_cache"], inp["prefix_lens"], 16, seed=10)
+    kp, vp, table, num_pages = full_tables(pg, Pcap)
+    kpd, vpd, tabd, pld = kp.cuda(), vp.cuda(), table.cuda(), dev["prefix_lens"].clone()
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    jb.jf_tree_commit_kv_paged(dev["tree_k"], dev["tree_v"], dev["n_nodes"], alen.cuda(), path.cuda(), kpd, vpd, tabd,
+                               16, num_pages, pld, shape, 16, status=st)
+    out = torch.empty_like(dev["q"])
+    jb.jf_tree_attention_paged(dev["q"], kpd, vpd, tabd, 16, num_pages, pld, dev["tree_k"], dev["tree_v"],
+                               dev["parents"], dev["n_nodes"], out, shape, new_workspace(shape), status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    np.testing.assert_array_equal(pld.cpu().numpy(), plc.cpu().numpy())
+    np.testing.assert_array_equal(_bits(out), _bits(ref))
+    # a page outside the pool where sequence 1's rows would go
+    bad = tabd.clone()
+    bad[1, int(pld[1]) // 16] = num_pages + 7
+    pl_before = pld.clone()
+    st.zero_()
+    jb.jf_tree_commit_kv_paged(dev["tree_k"], dev["tree_v"], dev["n_nodes"], alen.cuda(), path.cuda(), kpd, vpd, bad,
+                               16, num_pages, pld, shape, 16, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & jb.JF_STATUS_BAD_TREE
+    assert int(pld[1]) == int(pl_before[1])

@@ -477,3 +477,42 @@ def test_paged_layout_round_trip_and_attention():
                                     c["prefix_lens"], c["tree_k"], c["tree_v"], c["parents"], c["n_nodes"])
     b_ = run_oracle(c)
     np.testing.assert_array_equal(a, b_)
+
+
+def test_paged_commit_equals_contiguous_commit():
+    """Committing into pages and gathering them back gives the cache the
+    contiguous commit gives, for the golden requests' flags as well."""
+    c = random_case(12, B=4, N=9, Pcap=48, prefix=torch.tensor([40, 5, 47, 0], dtype=torch.int32))
+    pg = synth.paged_layout(c["k_cache"], c["v_cache"], c["prefix_lens"], 8, seed=4, spare=2, spare_fill=0.0)
+    # give every sequence all its pages (the commit may grow into unused ones)
+    table = pg["block_table"].clone()
+    nxt = pg["num_pages"]
+    for b in range(4):
+        for j in range(6):
+            if table[b, j] < 0:
+                table[b, j] = nxt
+                nxt += 1
+    kp = torch.cat([pg["k_pages"], torch.zeros(nxt - pg["num_pages"], *pg["k_pages"].shape[1:], dtype=torch.bfloat16)])
+    vp = torch.cat([pg["v_pages"], torch.zeros_like(kp[pg["num_pages"]:])])
+    alen = torch.tensor([3, 2, 2, 1], dtype=torch.int32)
+    path = torch.tensor([[0, 1, 4, -1], [0, 2, -1, -1], [0, 3, -1, -1], [0, -1, -1, -1]], dtype=torch.int32)
+    path = torch.cat([path, torch.full((4, 13), -1, dtype=torch.int32)], 1)
+    kc, vc, pl, fl = oracle.commit_kv(c["tree_k"], c["tree_v"], c["n_nodes"], alen, path, c["k_cache"],
+                                      c["v_cache"], c["prefix_lens"], 16)
+    kp2, vp2, pl2, fl2 = oracle.commit_kv_paged(c["tree_k"], c["tree_v"], c["n_nodes"], alen, path, kp, vp, table, 8,
+                                                c["prefix_lens"], 16)
+    np.testing.assert_array_equal(pl2, pl)
+    np.testing.assert_array_equal(fl2, fl)
+    assert fl.tolist() == [0, 0, 2, 0]                   # 47 + 2 > 48: no room
+    kg = oracle.gather_pages(kp2, table, pl2, 8, 48)
+    vg = oracle.gather_pages(vp2, table, pl2, 8, 48)
+    for b in range(4):
+        P = int(pl2[b])
+        np.testing.assert_array_equal(kg[b, :, :P], kc[b, :, :P])
+        np.testing.assert_array_equal(vg[b, :, :P], vc[b, :, :P])
+    # a used page outside the pool makes the request malformed
+    bad = table.clone()
+    bad[0, 5] = nxt + 3
+    _, _, pl3, fl3 = oracle.commit_kv_paged(c["tree_k"], c["tree_v"], c["n_nodes"], alen, path, kp, vp, bad, 8,
+                                            c["prefix_lens"], 16)
+    assert fl3[0] == 1 and pl3[0] == 40

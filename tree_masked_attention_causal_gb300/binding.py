@@ -79,6 +79,8 @@ def _configure(lib: ctypes.CDLL) -> ctypes.CDLL:
         lib.jf_tree_verify_noalloc.restype = i32
         lib.jf_tree_commit_kv.argtypes = [P, P, P, P, P, P, P, P, sp, i32, P, P]
         lib.jf_tree_commit_kv.restype = i32
+        lib.jf_tree_commit_kv_paged.argtypes = [P, P, P, P, P, P, P, P, i32, i32, P, sp, i32, P, P]
+        lib.jf_tree_commit_kv_paged.restype = i32
         u64 = ctypes.c_uint64
         lib.jf_tree_verify_sample.argtypes = [P, P, P, P, P, ctypes.c_float, u64, u64, P, P, P, sp, i32, P, sz,
                                               P, P]
@@ -218,6 +220,19 @@ def jf_tree_commit_kv(tree_k, tree_v, n_nodes, accept_len, accept_path, k_cache,
                                   int(max_depth), _ptr(status), _stream(stream))
     if check and rc != JF_OK:
         raise JfError("jf_tree_commit_kv", rc)
+    return rc
+
+
+def jf_tree_commit_kv_paged(tree_k, tree_v, n_nodes, accept_len, accept_path, k_pages, v_pages, block_table,
+                            page_size: int, num_pages: int, prefix_lens, shape: JfShape, max_depth: int, status=None,
+                            stream=None, check: bool = True) -> int:
+    """Append each sequence's accepted path to its paged KV cache (see jf_tree.h)."""
+    rc = load().jf_tree_commit_kv_paged(_ptr(tree_k), _ptr(tree_v), _ptr(n_nodes), _ptr(accept_len),
+                                        _ptr(accept_path), _ptr(k_pages), _ptr(v_pages), _ptr(block_table),
+                                        int(page_size), int(num_pages), _ptr(prefix_lens), ctypes.byref(shape),
+                                        int(max_depth), _ptr(status), _stream(stream))
+    if check and rc != JF_OK:
+        raise JfError("jf_tree_commit_kv_paged", rc)
     return rc
 
 

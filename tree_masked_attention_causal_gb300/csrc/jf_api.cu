@@ -402,6 +402,33 @@ JF_API int32_t jf_tree_commit_kv(const void *tree_k, const void *tree_v, const i
     return JF_OK;
 }
 
+JF_API int32_t jf_tree_commit_kv_paged(const void *tree_k, const void *tree_v, const int32_t *n_nodes,
+                                       const int32_t *accept_len, const int32_t *accept_path, void *k_pages,
+                                       void *v_pages, const int32_t *block_table, int32_t page_size,
+                                       int32_t num_pages, int32_t *prefix_lens, const jf_shape *shape,
+                                       int32_t max_depth, int32_t *status, jf_stream_t stream) {
+    if (!tree_k || !tree_v || !n_nodes || !accept_len || !accept_path || !k_pages || !v_pages || !block_table ||
+        !prefix_lens || !shape)
+        return JF_ERR_NULL;
+    const int32_t sc = check_shape(shape, false, true);
+    if (sc != JF_OK) return sc;
+    if (max_depth < 0) return JF_ERR_SHAPE;
+    int page_lg = 0;
+    while (page_lg < 31 && (1 << page_lg) < page_size) ++page_lg;
+    if (page_size < 8 || page_size > kBN || (1 << page_lg) != page_size || shape->prefix_cap % page_size ||
+        num_pages < 1 || (long long)num_pages * page_size > 0x7FFFFFFFll)
+        return JF_ERR_SHAPE;
+    if (!aligned16(tree_k) || !aligned16(tree_v) || !aligned16(k_pages) || !aligned16(v_pages)) return JF_ERR_ALIGN;
+    const Layout L = layout_of(shape);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (launch_commit_kv(L, reinterpret_cast<const __nv_bfloat16 *>(tree_k),
+                         reinterpret_cast<const __nv_bfloat16 *>(tree_v), n_nodes, accept_len, accept_path,
+                         reinterpret_cast<__nv_bfloat16 *>(k_pages), reinterpret_cast<__nv_bfloat16 *>(v_pages),
+                         prefix_lens, max_depth, status, s, block_table, page_lg, num_pages) != cudaSuccess)
+        return JF_ERR_CUDA;
+    return JF_OK;
+}
+
 // ------------------------------------------------ allocation-free verify
 // Scratch for jf_tree_verify_noalloc: lives in the library's own device
 // memory, so the call needs no caller workspace and allocates nothing.

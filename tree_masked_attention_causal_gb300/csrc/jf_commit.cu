@@ -7,6 +7,10 @@
 // with the right positions, so committing them is a copy, and the prefix
 // length grows by the path length.
 //
+// The cache is contiguous ([B, Hkv, Pcap, d]) or paged ([num_pages,
+// page_size, Hkv, d] through a block table, as jf_tree_attention_paged
+// reads it).
+//
 // One block per sequence (so that reading and raising prefix_lens[b] cannot
 // race with another block), 512 threads. The block checks the request, then
 // copies a * Hkv key rows and as many value rows in 16-byte pieces: each
@@ -26,7 +30,8 @@ __global__ void __launch_bounds__(kCommitThreads)
                      const int32_t *__restrict__ n_nodes, const int32_t *__restrict__ accept_len,
                      const int32_t *__restrict__ accept_path, __nv_bfloat16 *__restrict__ k_cache,
                      __nv_bfloat16 *__restrict__ v_cache, int32_t *__restrict__ prefix_lens, int Nmax, int Hkv,
-                     int D, int Pcap, int max_depth, int32_t *status) {
+                     int D, int Pcap, int max_depth, int32_t *status, const int32_t *__restrict__ block_table,
+                     int page_lg, int pages_per_seq, int num_pages) {
     __shared__ int s_node[kMaxNodes + 1];
     const int b = blockIdx.x, tid = threadIdx.x;
     const int a = accept_len[b], P = prefix_lens[b], n = n_nodes[b];
@@ -42,6 +47,14 @@ __global__ void __launch_bounds__(kCommitThreads)
         else s_node[k] = node;
     }
     bad = __syncthreads_or(bad);
+    // paged: every page that receives a row must be a page of the pool
+    if (!bad && page_lg >= 0 && P + a <= Pcap) {
+        for (int k = tid; k < a; k += kCommitThreads) {
+            const int ph = block_table[(size_t)b * pages_per_seq + ((P + k) >> page_lg)];
+            if (ph < 0 || ph >= num_pages) bad = true;
+        }
+        bad = __syncthreads_or(bad);
+    }
     if (bad || P + a > Pcap) {
         if (tid == 0) set_status(status, bad ? JF_STATUS_BAD_TREE : JF_STATUS_CACHE_FULL);
         return;
@@ -57,7 +70,14 @@ __global__ void __launch_bounds__(kCommitThreads)
         r >>= 1;
         const int h = r % Hkv, k = r / Hkv;
         const size_t src = (((size_t)b * Nmax + s_node[k]) * Hkv + h) * D + e * 8;
-        const size_t dst = (((size_t)b * Hkv + h) * Pcap + P + k) * D + e * 8;
+        size_t dst;
+        if (page_lg < 0) {
+            dst = (((size_t)b * Hkv + h) * Pcap + P + k) * D + e * 8;
+        } else {                                      // [num_pages, page_size, Hkv, d]
+            const int row = P + k;
+            const size_t ph = (size_t)block_table[(size_t)b * pages_per_seq + (row >> page_lg)];
+            dst = (((ph << page_lg) + (row & ((1 << page_lg) - 1))) * Hkv + h) * D + e * 8;
+        }
         s = reinterpret_cast<const uint4 *>((kv ? tree_v : tree_k) + src);
         t = reinterpret_cast<uint4 *>((kv ? v_cache : k_cache) + dst);
     };
@@ -87,10 +107,13 @@ __global__ void __launch_bounds__(kCommitThreads)
 cudaError_t launch_commit_kv(const Layout &L, const __nv_bfloat16 *tree_k, const __nv_bfloat16 *tree_v,
                              const int32_t *n_nodes, const int32_t *accept_len, const int32_t *accept_path,
                              __nv_bfloat16 *k_cache, __nv_bfloat16 *v_cache, int32_t *prefix_lens, int32_t max_depth,
-                             int32_t *status, cudaStream_t s) {
+                             int32_t *status, cudaStream_t s, const int32_t *block_table, int32_t page_lg,
+                             int32_t num_pages) {
     trace_begin("commit_kv", s);
+    const int pages_per_seq = page_lg >= 0 ? L.Pcap >> page_lg : 0;
     commit_kv_kernel<<<L.B, kCommitThreads, 0, s>>>(tree_k, tree_v, n_nodes, accept_len, accept_path, k_cache, v_cache,
-                                                     prefix_lens, L.Nmax, L.Hkv, L.D, L.Pcap, max_depth, status);
+                                                     prefix_lens, L.Nmax, L.Hkv, L.D, L.Pcap, max_depth, status,
+                                                     block_table, page_lg, pages_per_seq, num_pages);
     cudaError_t e = cudaGetLastError();
     trace_end(s);
     return e;

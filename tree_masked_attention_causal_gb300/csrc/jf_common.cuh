@@ -617,10 +617,12 @@ struct AttnArgs {
 cudaError_t launch_tree_attention(const Layout &L, const AttnMaps &m, const AttnArgs &a,
                                   cudaStream_t s);
 cudaError_t launch_split_combine(const Layout &L, const AttnArgs &a, cudaStream_t s);
+// Paged when page_lg >= 0: the caches are [num_pages, 2^page_lg, Hkv, d] pools.
 cudaError_t launch_commit_kv(const Layout &L, const __nv_bfloat16 *tree_k, const __nv_bfloat16 *tree_v,
                              const int32_t *n_nodes, const int32_t *accept_len, const int32_t *accept_path,
                              __nv_bfloat16 *k_cache, __nv_bfloat16 *v_cache, int32_t *prefix_lens, int32_t max_depth,
-                             int32_t *status, cudaStream_t s);
+                             int32_t *status, cudaStream_t s, const int32_t *block_table = nullptr,
+                             int32_t page_lg = -1, int32_t num_pages = 0);
 cudaError_t launch_argmax(const Layout &L, const __nv_bfloat16 *logits, const int32_t *n_nodes,
                           uint8_t *ws, cudaStream_t s);
 cudaError_t launch_accept_walk(const Layout &L, const int32_t *tokens, const int32_t *parents,
