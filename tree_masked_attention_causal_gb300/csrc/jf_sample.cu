@@ -20,17 +20,19 @@
 //  lse_chunk_kernel    HBM-bound scan of both logits arrays, chunked like
 //                      the argmax: each CTA reduces its chunk of one row
 //                      to (max z, sum 2^((z - max) log2(e) / T)).
-//  sample_walk_kernel  a cluster of kSampleCluster CTAs per sequence,
-//                      launched programmatically after the scan. CTA 0
-//                      validates the tree, merges the row normalisers,
-//                      walks the tree and takes every decision; each pass
-//                      over the vocabulary (a residual mass, or the final
-//                      Gumbel-max sample) is split over the cluster's CTAs,
-//                      whose partial results CTA 0 reads through
-//                      distributed shared memory and combines in rank
-//                      order. The other CTAs only run the commands CTA 0
-//                      posts, so every CTA meets the same sequence of
-//                      cluster barriers.
+//  sample_walk_kernel  a cluster of 16 CTAs per sequence (8 when the
+//                      batch would not fit the SMs), launched
+//                      programmatically after the scan. CTA 0 validates the
+//                      tree, merges the row normalisers, walks the tree and
+//                      takes every decision; each pass over the vocabulary
+//                      (a residual mass, or the final Gumbel-max sample) is
+//                      split over the other CTAs, which store their partial
+//                      results into CTA 0 through distributed shared memory
+//                      for it to combine in rank order. Those CTAs draw the
+//                      Gumbel noise of their vocabulary slices into shared
+//                      memory while CTA 0 gathers the tree, and then only
+//                      run the commands CTA 0 posts, so every CTA meets the
+//                      same sequence of cluster barriers.
 //
 // Random numbers: Philox4x64-10 (Salmon, Moraes, Dror and Shaw, "Parallel
 // random numbers: as easy as 1, 2, 3", SC 2011) under key (seed, offset).
@@ -75,10 +77,12 @@ __device__ __forceinline__ uint32_t top23(uint64_t w) { return (uint32_t)(w >> 4
 __device__ __forceinline__ float uniform_of(uint32_t k) { return ((float)k + 0.5f) * 0x1p-23f; }
 
 // -ln(-ln U) for U = (k + 1/2) 2^-23: 1 - U = (2^23 - k - 1/2) 2^-23 is
-// exact, so -ln U = -log1p(-(1 - U)) keeps full precision near U = 1.
+// exact, so t = -ln U = -log1p(-(1 - U)) keeps full precision near U = 1;
+// t lies in (6e-8, 16.7), where the fast natural log's error (about 1e-6
+// absolute here) is far below the margins a sample's keys are told apart by.
 __device__ __forceinline__ float gumbel_of(uint32_t k) {
     const float one_minus = ((float)(0x800000u - k) - 0.5f) * 0x1p-23f;
-    return -logf(-log1pf(-one_minus));
+    return -__logf(-log1pf(-one_minus));
 }
 
 __device__ float accept_uniform(uint64_t seed, uint64_t offset, int b, int c) {
@@ -244,11 +248,16 @@ __device__ __forceinline__ bool beats(float a, int ia, float b, int ib) {
     return a > b || (a == b && ia >= 0 && (ib < 0 || ia < ib));
 }
 
-// The vectors (8 entries each) of the vocabulary that cluster CTA `rank` covers.
+// The vectors (8 entries each) of the vocabulary that cluster CTA `rank`
+// covers: CTA 0 walks the tree and takes none; the others share them.
 __device__ __forceinline__ void slice_of(int V, uint32_t rank, int &lo, int &hi) {
-    const int nv = V >> 3, kc = (int)cluster_size();
-    lo = (int)((long long)rank * nv / kc);
-    hi = (int)((long long)(rank + 1) * nv / kc);
+    const int nv = V >> 3, kw = (int)cluster_size() - 1;
+    if (rank == 0) {
+        lo = hi = 0;
+        return;
+    }
+    lo = (int)((long long)(rank - 1) * nv / kw);
+    hi = (int)((long long)rank * nv / kw);
 }
 
 __device__ __forceinline__ uint32_t dynamic_smem_bytes() {
@@ -412,12 +421,9 @@ __device__ void cluster_pass(WalkShared &sh, const SampleArgs &a, int V, int b, 
                              const float *lse, float &res_f, int &res_i) {
     post(sh, op, row, c, lse);
     cluster_sync_all();                                      // commands visible
-    float f = 0.f;
-    int i = 0;
-    run_slice(sh.cmd, a, V, b, 0, sh, f, i);
-    if (threadIdx.x == 0) {
-        sh.part_f[0] = f;
-        sh.part_i[0] = i;
+    if (threadIdx.x == 0) {                                  // CTA 0 has no slice of its own
+        sh.part_f[0] = op == kOpMass ? 0.f : -__int_as_float(0x7f800000);
+        sh.part_i[0] = -1;
     }
     cluster_sync_all();                                      // every partial is in place
     if (threadIdx.x == 0) {
@@ -513,7 +519,6 @@ __global__ void __launch_bounds__(kSampleThreads, 2)
         sh.zp[tid] = zp;
         sh.zq[tid] = zq;
     }
-    precompute_noise(a, V, b, 0);
     pdl_wait_prior_grid();
     int32_t *path_out = a.accept_path + (size_t)b * (a.max_depth + 1);
     float lse[4] = {0.f, 0.f, 0.f, 0.f};
@@ -653,8 +658,8 @@ cudaError_t launch_sample(const Layout &L, const SampleArgs &a, uint8_t *ws, int
         cudaGetLastError();                                  // a refused query leaves no error behind
     }
     const int kc = (big_ok && L.B * kSampleClusterBig <= sms) ? kSampleClusterBig : kSampleCluster;
-    // room for the Gumbel noise of one CTA's vocabulary slice, if it fits
-    const size_t noise = (size_t)((L.V / 8 + kc - 1) / kc) * 32;
+    // room for the Gumbel noise of one worker CTA's vocabulary slice, if it fits
+    const size_t noise = (size_t)((L.V / 8 + kc - 2) / (kc - 1)) * 32;
     const size_t dyn = noise <= kSampleNoiseMax ? noise : 0;
     static bool dyn_set = false;
     if (!dyn_set) {
