@@ -68,17 +68,17 @@ def test_argmax_chunks_on_152_sms(rows, V, expect):
                                           (2, 5, 151936, 75), (1, 16, 1024, 1), (4, 200, 262144, 4),
                                           (1, 152, 151936, 6)])
 def test_argmax_chunk_rule(lib, B, N, V, expect):
-    """The verify region of the workspace holds one int2 per (row, chunk),
-    the sampling region two float2 (target and draft) and the scoring
-    region 16 (value, index) pairs: their growth from
-    a one-chunk vocabulary pins the chunk count they are sized for (256 SMs,
-    the bound for any device's chunking)."""
+    """The verify region of the workspace holds one int2 per (row, chunk)
+    and the sampling region two float2 (target and draft; the scoring
+    shares it): their growth from a one-chunk vocabulary pins the chunk
+    count they are sized for (256 SMs, the bound for any device's
+    chunking)."""
     assert _argmax_chunks(B * N, V) == expect
     align = lambda x: -(-x // 256) * 256
     base = jb.jf_workspace_bytes(jb.make_shape(B, 0, 0, 0, N, 0, 8))
     ws = jb.jf_workspace_bytes(jb.make_shape(B, 0, 0, 0, N, 0, V))
     rows = B * N
-    regions = lambda c: align(rows * c * 8) + align(2 * rows * c * 8) + align(rows * c * 16 * 8)
+    regions = lambda c: align(rows * c * 8) + align(2 * rows * c * 8)
     assert ws - base == regions(expect) - regions(1)
 
 

@@ -138,3 +138,32 @@ def test_ties_padding_malformed_and_out_of_range():
     assert st == jb.JF_STATUS_BAD_TREE
     assert np.isneginf(g["node"][0, 3]) and np.isneginf(g["node"][0, 4])
     assert g["ttok"][0, 0, :7].tolist() == [5, 40000, 77823, 77824, 77829, 120000, V - 1]
+
+
+def test_topk_where_the_best_entries_crowd():
+    """Layouts that defeat a bound taken from per-thread maxima: one thread
+    holding 20 of a row's best entries in separate vectors, eight tied best
+    entries in one vector, a constant row, and a row of equal values with a
+    few larger ones (every entry then reaches the bound)."""
+    B, N, V = 1, 5, 151936
+    gen = torch.Generator().manual_seed(33)
+    z = torch.randn((B, N, V), generator=gen)
+    for j in range(20):                          # the vectors of one thread of the first chunk
+        z[0, 0, 8 * (37 + 256 * j) + (j % 8)] = 20.0 + 0.25 * j
+    z[0, 1, 8 * 1000: 8 * 1000 + 8] = 30.0       # one vector, eight ties
+    z[0, 1, [3, 90001, 150000, 77830, 12345, 54321, 111111, 8 * 1000 + 9]] = 29.0
+    z[0, 2] = 1.0                                # constant: the lowest indices
+    z[0, 3] = -60.0
+    z[0, 3, [17, 40000, 77824, 100000, V - 1]] = 3.0
+    z[0, 4, 8 * (200 + 256 * 3)] = 50.0          # one entry far above the rest
+    draft = z.to(torch.bfloat16)
+    parents = torch.tensor([[-1, 0, 1, 1, 0]], dtype=torch.int32)
+    tokens = torch.tensor([[0, 5, 7, V - 1, 77824]], dtype=torch.int32)
+    for k, budget in ((16, 0), (16, 30), (3, 7)):
+        g, r, st = compare(draft, tokens, parents, torch.tensor([N], dtype=torch.int32), 1.0, k, budget)
+        assert st == 0
+    g, r, st = compare(draft, tokens, parents, torch.tensor([N], dtype=torch.int32), 1.0, 16, 0)
+    assert g["ttok"][0, 0].tolist() == [8 * (37 + 256 * j) + (j % 8) for j in range(19, 3, -1)]
+    assert g["ttok"][0, 1, :8].tolist() == list(range(8000, 8008))
+    assert g["ttok"][0, 2].tolist() == list(range(16))
+    assert g["ttok"][0, 3].tolist() == [17, 40000, 77824, 100000, V - 1] + list(range(11))

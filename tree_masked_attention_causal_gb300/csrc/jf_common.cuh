@@ -67,8 +67,8 @@ struct Layout {
     int32_t chunks;      // argmax chunks per logits row
     size_t qtab_off, ml_off, opart_off;
     size_t amp_off;
-    size_t lse_off;      // stochastic verify: (max, sum) per (target | draft, row, chunk)
-    size_t topk_off;     // path scoring: kScoreMaxK (value, index) per (row, chunk)
+    size_t lse_off;      // stochastic verify: (max, sum) per (target | draft, row, chunk);
+                         // path scoring: (max, log2 sum) per row
     size_t total;
 };
 
@@ -109,7 +109,6 @@ inline Layout make_layout(int B, int Nmax, int Hq, int Hkv, int D, int Pcap, int
     L.opart_off = take(2 * (size_t)L.max_pieces * kRows * D);   // fp16 rows, divided by l, scaled by 2^-e per half
     L.amp_off = take(sizeof(int2) * (size_t)B * Nmax * L.chunks);
     L.lse_off = take(2 * sizeof(float2) * (size_t)B * Nmax * L.chunks);
-    L.topk_off = take((sizeof(float) + sizeof(int)) * kScoreMaxK * (size_t)B * Nmax * L.chunks);
     L.total = off;
     return L;
 }

@@ -41,7 +41,7 @@
 // counter (v / 4, b, 1, 0). A word w gives (floor(w / 2^41) + 1/2) 2^-23.
 // The sample is the v maximising ln r(v) - ln(-ln U(v)) over r(v) > 0,
 // the lowest index on ties.
-#include "jf_common.cuh"
+#include "jf_cluster.cuh"
 
 namespace jf {
 namespace {
@@ -192,34 +192,6 @@ struct Cmd {
     int op, row;
     float c, Mp, Lp, Mq, Lq, pad;
 };
-
-__device__ __forceinline__ uint32_t cluster_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-__device__ __forceinline__ uint32_t cluster_size() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
-    return r;
-}
-
-// Every thread of every CTA of the cluster; orders shared-memory writes
-// before it with reads after it, across the cluster.
-__device__ __forceinline__ void cluster_sync_all() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
-    return r;
-}
-
-__device__ __forceinline__ void st_cluster(uint32_t addr, uint32_t v) {
-    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
 
 struct WalkShared {
     Cmd cmd;                     // this CTA's command (written by CTA 0)

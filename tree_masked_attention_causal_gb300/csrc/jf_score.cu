@@ -11,21 +11,27 @@
 // path_lp[u] + log q_u(v), the best `budget` of them over the whole tree.
 //
 //  score_chunk_kernel  HBM-bound scan of the draft logits, chunked like the
-//                      argmax: each CTA reduces its chunk of one row to
-//                      (max z, sum 2^((z - max) log2(e) / T)) and, when
-//                      asked, its kScoreMaxK largest entries (the lower
-//                      index first on ties): a sorted list per thread,
-//                      merged across the block one winner at a time.
+//                      argmax (at most 4 chunks a row), the chunks of one
+//                      row forming one thread-block cluster. Each CTA
+//                      reduces its chunk to (max z, sum 2^((z - max)
+//                      log2(e) / T)) and, when asked, its kScoreMaxK
+//                      largest entries (the lower index first on ties):
+//                      while it reads, every entry at or above a running
+//                      bound on the chunk's kScoreMaxK-th entry (taken from
+//                      the threads' maxima) is kept in shared memory, and
+//                      at the end the few kept entries are ranked. CTA 0
+//                      of the cluster merges the chunks' normalisers and
+//                      lists and writes the row's top_k log-probabilities.
 //  score_tree_kernel   one block per sequence, one thread per node, a
 //                      programmatic dependent of the scan. Before the scan
 //                      completes it validates the tree and loads each
-//                      node's token logit; after, it merges its row's
-//                      chunks, sums the path by pointer jumping (8 rounds
-//                      cover 256 levels), writes the top-k, and selects the
-//                      budget best (node, rank) candidates by path score: a
-//                      radix select of the budget-th key, then a bitonic
-//                      sort of the selected ones, in shared memory.
-#include "jf_common.cuh"
+//                      node's token logit; after, it sums the path by
+//                      pointer jumping (8 rounds cover 256 levels) and
+//                      selects the budget best (node, rank) candidates by
+//                      path score: a radix select of the budget-th key,
+//                      then a bitonic sort of the selected ones, in shared
+//                      memory.
+#include "jf_cluster.cuh"
 
 namespace jf {
 namespace {
@@ -63,13 +69,10 @@ struct WarpTop {
     int thr_i;
 };
 
-// The elements of one vector per lane (8 bf16, indices idx0 ..) that clear
-// the bar (the list's last entry), inserted one at a time in (element,
-// lane) order. Once the list is full few vectors get here; it is out of
-// line, since the scan's loop runs faster with less code (measured: a
-// copy inlined at every call site, or a list filled from the first
-// vectors and a bar shared between warps, were slower).
-__device__ __noinline__ WarpTop warp_take(WarpTop t, uint4 vec, bool live, int idx0) {
+// The elements of one vector per lane (8 bf16, indices idx0 ..) that reach
+// floor_v and clear the bar (the list's last entry), inserted one at a
+// time in (element, lane) order. Out of line: few vectors get here.
+__device__ __noinline__ WarpTop warp_take(WarpTop t, uint4 vec, bool live, int idx0, float floor_v) {
     const unsigned full = 0xffffffffu;
     const int lane = threadIdx.x & 31;
 #pragma unroll 1
@@ -77,7 +80,7 @@ __device__ __noinline__ WarpTop warp_take(WarpTop t, uint4 vec, bool live, int i
         const uint32_t wj = (j >> 1) == 0 ? vec.x : (j >> 1) == 1 ? vec.y : (j >> 1) == 2 ? vec.z : vec.w;
         const float zj = __uint_as_float((j & 1) ? (wj & 0xFFFF0000u) : (wj << 16));
         const int ix = idx0 + j;
-        unsigned cand = __ballot_sync(full, live && ahead(zj, ix, t.thr_v, t.thr_i));
+        unsigned cand = __ballot_sync(full, live && zj >= floor_v && ahead(zj, ix, t.thr_v, t.thr_i));
         while (cand) {
             const int src = __ffs(cand) - 1;
             cand &= cand - 1;
@@ -103,56 +106,78 @@ __device__ __noinline__ WarpTop warp_take(WarpTop t, uint4 vec, bool live, int i
     return t;
 }
 
-// The kScoreMaxK best of two lists sorted by `ahead` into (lv, li): a
-// bitonic half-cleaner on lv ++ reverse(cv), then a bitonic merge of the
-// better half (static indices throughout, so the lists stay in registers).
-__device__ __forceinline__ void merge_top(float (&lv)[kScoreMaxK], int (&li)[kScoreMaxK], const float (&cv)[kScoreMaxK],
-                                          const int (&ci)[kScoreMaxK]) {
+// A bound T that the chunk's kScoreMaxK-th largest entry cannot be below:
+// the two largest thread maxima of every warp are distinct entries of the
+// chunk, kScoreMaxK of them over the block, so their minimum will do. Each
+// warp's pair only grows as the scan goes on, so a bound taken from older
+// values of some warps is still a bound.
+static_assert(2 * (kArgmaxThreads / 32) == kScoreMaxK, "two thread maxima per warp make the bound");
+
+// The largest of a vector's 8 bf16 entries (NaN only if all are NaN).
+__device__ __forceinline__ float vm_of(uint4 v) {
+    const float a = fmaxf(fmaxf(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xFFFF0000u)),
+                          fmaxf(__uint_as_float(v.y << 16), __uint_as_float(v.y & 0xFFFF0000u)));
+    const float b = fmaxf(fmaxf(__uint_as_float(v.z << 16), __uint_as_float(v.z & 0xFFFF0000u)),
+                          fmaxf(__uint_as_float(v.w << 16), __uint_as_float(v.w & 0xFFFF0000u)));
+    return fmaxf(a, b);
+}
+
+// The second largest of the warp's values (the largest counted once).
+__device__ __forceinline__ float warp_second(float x) {
+    const unsigned full = 0xffffffffu;
+    float m1 = x;
 #pragma unroll
-    for (int q = 0; q < kScoreMaxK; ++q) {
-        const float bv = cv[kScoreMaxK - 1 - q];
-        const int bi = ci[kScoreMaxK - 1 - q];
-        if (ahead(bv, bi, lv[q], li[q])) {
-            lv[q] = bv;
-            li[q] = bi;
-        }
-    }
+    for (int o = 16; o > 0; o >>= 1) m1 = fmaxf(m1, __shfl_xor_sync(full, m1, o));
+    const int first = __ffs(__ballot_sync(full, x == m1)) - 1;
+    float m2 = (int)(threadIdx.x & 31) == first ? -__builtin_huge_valf() : x;
 #pragma unroll
-    for (int stride = kScoreMaxK / 2; stride > 0; stride >>= 1) {
+    for (int o = 16; o > 0; o >>= 1) m2 = fmaxf(m2, __shfl_xor_sync(full, m2, o));
+    return m2;
+}
+
+// The scan's candidates: each thread keeps up to kThreadCands of its own
+// in a strided slot of shared memory, counting in a register.
+constexpr int kThreadCands = 8;
+constexpr int kScoreCap = kArgmaxThreads * kThreadCands;
+__shared__ float s_cand_v[kScoreCap];
+__shared__ int s_cand_i[kScoreCap];
+
+__device__ __forceinline__ float bound_of(const volatile float *sbound) {
+    float T = sbound[0];
 #pragma unroll
-        for (int q = 0; q < kScoreMaxK; ++q) {
-            if ((q & stride) == 0 && ahead(lv[q + stride], li[q + stride], lv[q], li[q])) {
-                const float tv = lv[q];
-                const int ti = li[q];
-                lv[q] = lv[q + stride];
-                li[q] = li[q + stride];
-                lv[q + stride] = tv;
-                li[q + stride] = ti;
-            }
-        }
-    }
+    for (int w = 1; w < kArgmaxThreads / 32; ++w) T = fminf(T, sbound[w]);
+    return T;
 }
 
 __global__ void __launch_bounds__(kArgmaxThreads)
     score_chunk_kernel(const __nv_bfloat16 *__restrict__ draft, const int32_t *__restrict__ n_nodes,
-                       float2 *__restrict__ lse_part, float *__restrict__ top_v, int *__restrict__ top_i, int Nmax,
-                       int V, int chunk, int chunks, float k2, int want_top) {
+                       float2 *__restrict__ row_lse, int32_t *__restrict__ topk_token, float *__restrict__ topk_lp,
+                       int K, int Nmax, int V, int chunk, float k2) {
     pdl_launch_dependents();
     const int row = blockIdx.y;
     const int b = row / Nmax, node = row - b * Nmax;
     const int n = n_nodes[b];
-    if (n < 1 || n > Nmax || node >= n) return;              // padding row
+    if (n < 1 || n > Nmax || node >= n) return;              // padding row (the whole cluster)
     const int tid = threadIdx.x;
     const int e0 = blockIdx.x * chunk;
     const int nvec = (min(V, e0 + chunk) - e0) >> 3;
     const uint4 *src = reinterpret_cast<const uint4 *>(draft + (size_t)row * V + e0);
     constexpr float kNegInf = -__builtin_huge_valf();
-    float2 acc = make_float2(kNegInf, 0.f);
-    const int lane = tid & 31;
+    const bool want_top = K > 0;
+    const int lane = tid & 31, warp = tid >> 5;
     const unsigned full = 0xffffffffu;
-    WarpTop wt{kNegInf, -1, kNegInf, -1};
-    // the loop bound is the same for the whole block, so every lane reaches
-    // every ballot; lanes past the chunk's end take part with live = false
+    __shared__ float2 sacc[kArgmaxThreads / 32];
+    __shared__ float sbound[kArgmaxThreads / 32];
+    __shared__ float swv[kArgmaxThreads / 32];
+    __shared__ int swi[kArgmaxThreads / 32];
+    __shared__ int s_over;
+    volatile float *vbound = sbound;
+    float2 acc = make_float2(kNegInf, 0.f);
+    // Candidates: the entries at or above the bound known when their vector
+    // is reduced, appended to shared memory. Every entry of the chunk's top
+    // kScoreMaxK is one, whatever the order the warps run in.
+    float T = kNegInf;
+    int ncand = 0;
     for (int k0b = 0; k0b < nvec; k0b += kArgmaxThreads * kArgmaxVecs) {
         const int k0 = k0b + tid;
         uint4 v[kArgmaxVecs];
@@ -161,12 +186,27 @@ __global__ void __launch_bounds__(kArgmaxThreads)
             const int k = k0 + u * kArgmaxThreads;
             if (k < nvec) v[u] = ld_stream(src + k);
         }
+        if (want_top && k0b > 0) {                            // raise this warp's part of the bound
+            const float m2 = warp_second(acc.x);                // (with the loads in flight)
+            if (lane == 0) vbound[warp] = m2;
+            T = bound_of(vbound);
+        }
+        if (want_top && k0b == 0) {                           // the first bound, from the first vectors
+            float tm = kNegInf;
+#pragma unroll
+            for (int u = 0; u < kArgmaxVecs; ++u)
+                if (k0 + u * kArgmaxThreads < nvec) tm = fmaxf(tm, vm_of(v[u]));
+            const float m2 = warp_second(tm);
+            if (lane == 0) vbound[warp] = m2;
+            if (tid == 0) s_over = 0;
+            __syncthreads();
+            T = bound_of(vbound);
+        }
 #pragma unroll
         for (int u = 0; u < kArgmaxVecs; ++u) {
             const int k = k0 + u * kArgmaxThreads;
-            const bool live = k < nvec;                       // warp-uniform loop: every lane takes the ballots
             float vm = kNegInf;
-            if (live) {
+            if (k < nvec) {
                 const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
                 float z[8];
 #pragma unroll
@@ -185,56 +225,168 @@ __global__ void __launch_bounds__(kArgmaxThreads)
 #pragma unroll
                 for (int j = 0; j < 8; ++j) s += ex2_approx((z[j] - acc.x) * k2);
                 acc.y += s;
+                if (want_top && vm >= T) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        if (z[j] >= T) {
+                            if (ncand < kThreadCands) {
+                                s_cand_v[ncand * kArgmaxThreads + tid] = z[j];
+                                s_cand_i[ncand * kArgmaxThreads + tid] = e0 + 8 * k + j;
+                            }
+                            ++ncand;
+                        }
+                    }
+                }
             }
-            // a vector whose largest entry reaches the bar may hold entries for the list
-            if (want_top && __any_sync(full, live && !(vm < wt.thr_v))) wt = warp_take(wt, v[u], live, e0 + 8 * k);
         }
     }
-    __shared__ float2 sacc[kArgmaxThreads / 32];
-    __shared__ float swv[kArgmaxThreads / 32];
-    __shared__ int swi[kArgmaxThreads / 32];
-    const int warp = tid >> 5;
+    const float my_max = acc.x;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
-        const float2 other = make_float2(__shfl_xor_sync(0xffffffffu, acc.x, o), __shfl_xor_sync(0xffffffffu, acc.y, o));
+        const float2 other = make_float2(__shfl_xor_sync(full, acc.x, o), __shfl_xor_sync(full, acc.y, o));
         acc = lse_merge(acc, other, k2);
     }
+    if (want_top && nvec > 0) {                               // this warp's final pair
+        const float m2 = warp_second(my_max);
+        if (lane == 0) vbound[warp] = m2;
+    }
+    if (want_top && ncand > kThreadCands) s_over = 1;
     if (lane == 0) sacc[warp] = acc;
     __syncthreads();
-    const size_t slot = (size_t)row * chunks + blockIdx.x;
+    // The row's chunks are one cluster: each CTA stores its (max, sum) and
+    // its kScoreMaxK best into CTA 0's shared memory, which then writes the
+    // row's normaliser and its top_k.
+    __shared__ float2 s_lse_all[kScoreMaxChunks];
+    __shared__ float s_all_v[kScoreMaxChunks * kScoreMaxK];
+    __shared__ int s_all_i[kScoreMaxChunks * kScoreMaxK];
+    const uint32_t crank = cluster_rank(), csize = cluster_size();
     if (tid == 0) {
         float2 t = sacc[0];
         for (int w2 = 1; w2 < kArgmaxThreads / 32; ++w2) t = lse_merge(t, sacc[w2], k2);
-        lse_part[slot] = t;
+        const uint32_t dst = map_to_rank(smem_u32(&s_lse_all[crank]), 0);
+        st_cluster(dst, __float_as_uint(t.x));
+        st_cluster(dst + 4, __float_as_uint(t.y));
     }
-    if (!want_top) return;
-    // the block's kScoreMaxK best: each round every warp offers the head of
-    // its list, the best offer is written out, and its warp drops its head
-    for (int r = 0; r < kScoreMaxK; ++r) {
-        if (lane == 0) {
-            swv[warp] = wt.ev;
-            swi[warp] = wt.ei;
-        }
+    T = want_top && nvec > 0 ? bound_of(vbound) : kNegInf;    // every warp's final pair
+    if (!want_top) {
+    } else if (nvec == 0 || s_over == 0) {
+        // only the candidates at or above the final bound can rank below
+        // kScoreMaxK: those are compacted, then each is ranked among them
+        __shared__ int s_keep;
+        __shared__ float s_kv[kScoreCap];
+        __shared__ int s_ki[kScoreCap];
+        if (tid == 0) s_keep = 0;
         __syncthreads();
-        float bv = swv[0];
-        int bi = swi[0], bw = 0;
-        for (int w2 = 1; w2 < kArgmaxThreads / 32; ++w2)
-            if (ahead(swv[w2], swi[w2], bv, bi)) {
-                bv = swv[w2];
-                bi = swi[w2];
-                bw = w2;
+        for (int q = 0; q < ncand; ++q) {                     // this thread's own
+            const float x = s_cand_v[q * kArgmaxThreads + tid];
+            if (x >= T) {
+                const int at = atomicAdd(&s_keep, 1);
+                s_kv[at] = x;
+                s_ki[at] = s_cand_i[q * kArgmaxThreads + tid];
             }
+        }
         __syncthreads();
-        if (tid == 0) {
-            top_v[slot * kScoreMaxK + r] = bv;
-            top_i[slot * kScoreMaxK + r] = bi;
+        const int keep = s_keep;
+        const uint32_t dst_v = map_to_rank(smem_u32(&s_all_v[crank * kScoreMaxK]), 0);
+        const uint32_t dst_i = map_to_rank(smem_u32(&s_all_i[crank * kScoreMaxK]), 0);
+        for (int t = tid; t < keep; t += kArgmaxThreads) {
+            const float x = s_kv[t];
+            const int xi = s_ki[t];
+            int rank = 0;
+#pragma unroll 4
+            for (int q = 0; q < keep; ++q) rank += ahead(s_kv[q], s_ki[q], x, xi) ? 1 : 0;
+            if (rank < kScoreMaxK) {
+                st_cluster(dst_v + 4 * rank, __float_as_uint(x));
+                st_cluster(dst_i + 4 * rank, (uint32_t)xi);
+            }
         }
-        if (warp == bw && bi >= 0) {                          // the winning warp drops its head
-            const float nv = __shfl_down_sync(full, wt.ev, 1);
-            const int ni = __shfl_down_sync(full, wt.ei, 1);
-            wt.ev = lane < kScoreMaxK - 1 ? nv : kNegInf;
-            wt.ei = lane < kScoreMaxK - 1 ? ni : -1;
+        if (tid >= keep && tid < kScoreMaxK) {                // fewer entries than the list holds
+            st_cluster(dst_v + 4 * tid, __float_as_uint(kNegInf));
+            st_cluster(dst_i + 4 * tid, (uint32_t)-1);
         }
+    } else {
+        // More candidates than shared memory keeps (many entries equal at
+        // the top of the chunk): a second pass over the vectors whose
+        // maximum reaches T fills a sorted list per warp.
+        WarpTop wt{kNegInf, -1, kNegInf, -1};
+        const bool mine = my_max >= T;
+        if (__any_sync(full, mine)) {
+            // the loop bound is the same for the whole warp, so every lane
+            // reaches every ballot; other lanes take part with live = false
+            for (int k0b = 0; k0b < nvec; k0b += kArgmaxThreads * kArgmaxVecs) {
+                const int k0 = k0b + tid;
+                uint4 v[kArgmaxVecs];
+#pragma unroll
+                for (int u = 0; u < kArgmaxVecs; ++u) {
+                    const int k = k0 + u * kArgmaxThreads;
+                    if (mine && k < nvec) v[u] = ld_stream(src + k);
+                }
+#pragma unroll
+                for (int u = 0; u < kArgmaxVecs; ++u) {
+                    const int k = k0 + u * kArgmaxThreads;
+                    const bool live = mine && k < nvec;
+                    const float vm = live ? vm_of(v[u]) : kNegInf;
+                    if (__any_sync(full, live && vm >= T && !(vm < wt.thr_v)))
+                        wt = warp_take(wt, v[u], live, e0 + 8 * k, T);
+                }
+            }
+        }
+        // the block's kScoreMaxK best: each round every warp offers the
+        // head of its list, the best offer is stored, and its warp drops
+        // its head
+        for (int r = 0; r < kScoreMaxK; ++r) {
+            if (lane == 0) {
+                swv[warp] = wt.ev;
+                swi[warp] = wt.ei;
+            }
+            __syncthreads();
+            float bv = swv[0];
+            int bi = swi[0], bw = 0;
+            for (int w2 = 1; w2 < kArgmaxThreads / 32; ++w2)
+                if (ahead(swv[w2], swi[w2], bv, bi)) {
+                    bv = swv[w2];
+                    bi = swi[w2];
+                    bw = w2;
+                }
+            __syncthreads();
+            if (tid == 0) {
+                st_cluster(map_to_rank(smem_u32(&s_all_v[crank * kScoreMaxK + r]), 0), __float_as_uint(bv));
+                st_cluster(map_to_rank(smem_u32(&s_all_i[crank * kScoreMaxK + r]), 0), (uint32_t)bi);
+            }
+            if (warp == bw && bi >= 0) {                      // the winning warp drops its head
+                const float nv = __shfl_down_sync(full, wt.ev, 1);
+                const int ni = __shfl_down_sync(full, wt.ei, 1);
+                wt.ev = lane < kScoreMaxK - 1 ? nv : kNegInf;
+                wt.ei = lane < kScoreMaxK - 1 ? ni : -1;
+            }
+        }
+    }
+    cluster_sync_all();
+    if (crank != 0) return;
+    // CTA 0: the row's normaliser (chunks merged in order) as (max, log2 sum)
+    float2 rl = s_lse_all[0];
+    for (uint32_t c = 1; c < csize; ++c) rl = lse_merge(rl, s_lse_all[c], k2);
+    const float l2 = log2f(rl.y);
+    if (tid == 0) row_lse[row] = make_float2(rl.x, l2);
+    if (!want_top) return;
+    // the row's top_k: each real entry of the chunks' lists ranked among them
+    const int total = (int)csize * kScoreMaxK;
+    const bool real = tid < total && s_all_i[tid] >= 0;
+    const int nreal = __syncthreads_count(real);
+    const float ln2 = 0.69314718055994531f;
+    if (real) {
+        const float x = s_all_v[tid];
+        const int xi = s_all_i[tid];
+        int rank = 0;
+        for (int q = 0; q < total; ++q) rank += (s_all_i[q] >= 0 && ahead(s_all_v[q], s_all_i[q], x, xi)) ? 1 : 0;
+        if (rank < K) {
+            topk_token[(size_t)row * K + rank] = xi;
+            topk_lp[(size_t)row * K + rank] = ((x - rl.x) * k2 - l2) * ln2;
+        }
+    }
+    if (tid >= nreal && tid < K) {                            // fewer entries than asked for
+        topk_token[(size_t)row * K + tid] = -1;
+        topk_lp[(size_t)row * K + tid] = __builtin_nanf("");
     }
 }
 
@@ -256,8 +408,7 @@ struct ScoreShared {
 };
 
 __global__ void __launch_bounds__(kScoreThreads)
-    score_tree_kernel(const Layout L, const ScoreArgs a, const float2 *__restrict__ lse_part,
-                      const float *__restrict__ top_v, const int *__restrict__ top_i, int chunks) {
+    score_tree_kernel(const Layout L, const ScoreArgs a, const float2 *__restrict__ row_lse) {
     extern __shared__ __align__(16) unsigned char s_raw[];
     ScoreShared &sh = *reinterpret_cast<ScoreShared *>(s_raw);
     const int b = blockIdx.x, i = threadIdx.x;
@@ -300,13 +451,11 @@ __global__ void __launch_bounds__(kScoreThreads)
         if (i == 0) set_status(a.status, JF_STATUS_BAD_TREE);
         return;
     }
-    // this node's row: its normaliser, merged from the chunks in order
+    // this node's row: its normaliser (max, log2 sum), from the scan
     if (i < n) {
-        const float2 *pr = lse_part + (seq + i) * chunks;
-        float2 acc = make_float2(kNegInf, 0.f);
-        for (int ch = 0; ch < chunks; ++ch) acc = lse_merge(acc, pr[ch], a.k2);
-        sh.ms[i][0] = acc.x;
-        sh.ms[i][1] = log2f(acc.y);
+        const float2 rl = row_lse[seq + i];
+        sh.ms[i][0] = rl.x;
+        sh.ms[i][1] = rl.y;
         sh.par[i] = p;
     }
     __syncthreads();
@@ -341,48 +490,23 @@ __global__ void __launch_bounds__(kScoreThreads)
         a.path_lp[seq + i] = path;
         if (i >= n) a.node_lp[seq + i] = kNaN;
     }
-    // this node's top-k: its chunks' lists (at most kScoreMaxChunks, each
-    // loaded whole with 16-byte loads) merged in chunk (index) order
-    float lv[kScoreMaxK];
-    int li[kScoreMaxK];
-#pragma unroll
-    for (int s = 0; s < kScoreMaxK; ++s) {
-        lv[s] = kNegInf;
-        li[s] = -1;
-    }
-    if (K > 0 && i < n) {
-        for (int ch = 0; ch < chunks; ++ch) {
-            const size_t slot = ((seq + i) * chunks + ch) * kScoreMaxK;
-            float cv[kScoreMaxK];
-            int ci[kScoreMaxK];
-#pragma unroll
-            for (int q = 0; q < kScoreMaxK / 4; ++q) {
-                const float4 v4 = *reinterpret_cast<const float4 *>(top_v + slot + 4 * q);
-                const int4 i4 = *reinterpret_cast<const int4 *>(top_i + slot + 4 * q);
-                cv[4 * q] = v4.x; cv[4 * q + 1] = v4.y; cv[4 * q + 2] = v4.z; cv[4 * q + 3] = v4.w;
-                ci[4 * q] = i4.x; ci[4 * q + 1] = i4.y; ci[4 * q + 2] = i4.z; ci[4 * q + 3] = i4.w;
-            }
-            merge_top(lv, li, cv, ci);
-        }
-    }
-    // outputs, and the expansion's candidates with an order-preserving key:
-    // larger score -> larger key, no candidate -> 0
-    const float m = i < n ? sh.ms[i][0] : 0.f, l2 = i < n ? sh.ms[i][1] : 0.f;
+    // this node's top-k, written by the scan (padding rows get none), and
+    // the expansion's candidates with an order-preserving key: larger score
+    // -> larger key, no candidate -> 0
     const bool want = a.budget > 0 && K > 0;
-#pragma unroll
-    for (int s = 0; s < kScoreMaxK; ++s) {
-        if (s < K && i < Nmax) {
-            const bool ok = i < n && li[s] >= 0;
-            const float v = ok ? ((lv[s] - m) * a.k2 - l2) * ln2 : kNaN;
-            a.topk_token[(seq + i) * K + s] = ok ? li[s] : -1;
-            a.topk_lp[(seq + i) * K + s] = v;
-            if (want) {
-                const float sc = path + v;
-                const uint32_t u = __float_as_uint(sc);
-                sh.cand_key[i * K + s] = (ok && sc == sc) ? ((u & 0x80000000u) ? ~u : (u | 0x80000000u)) : 0u;
-                sh.cand_s[i * K + s] = sc;
-                sh.cand_tok[i * K + s] = ok ? li[s] : -1;
-            }
+    for (int s = 0; s < K && i < Nmax; ++s) {
+        if (i >= n) {
+            a.topk_token[(seq + i) * K + s] = -1;
+            a.topk_lp[(seq + i) * K + s] = kNaN;
+        }
+        if (want) {
+            const int tok = i < n ? a.topk_token[(seq + i) * K + s] : -1;
+            const float v = tok >= 0 ? a.topk_lp[(seq + i) * K + s] : kNaN;
+            const float sc = path + v;
+            const uint32_t u = __float_as_uint(sc);
+            sh.cand_key[i * K + s] = (tok >= 0 && sc == sc) ? ((u & 0x80000000u) ? ~u : (u | 0x80000000u)) : 0u;
+            sh.cand_s[i * K + s] = sc;
+            sh.cand_tok[i * K + s] = tok;
         }
     }
     if (!want) return;
@@ -530,21 +654,28 @@ __global__ void __launch_bounds__(kScoreThreads)
 
 cudaError_t launch_score(const Layout &L, const ScoreArgs &a, uint8_t *ws, cudaStream_t s) {
     const int rows = L.B * L.Nmax;
-    // at most kScoreMaxChunks chunks a row, so that each node's merge loads
-    // a few whole lists (the argmax cuts more when rows are few)
+    // at most kScoreMaxChunks chunks a row, one cluster (the argmax cuts
+    // more when rows are few)
     int chunk = L.chunk, chunks = L.chunks;
     if (chunks > kScoreMaxChunks) {
         chunk = (int)align_up((size_t)ceil_div(L.V, kScoreMaxChunks), kArgmaxGranule);
         chunks = ceil_div(L.V, chunk);
     }
-    float2 *lse_part = reinterpret_cast<float2 *>(ws + L.lse_off);
-    float *top_v = reinterpret_cast<float *>(ws + L.topk_off);
-    int *top_i = reinterpret_cast<int *>(ws + L.topk_off + sizeof(float) * kScoreMaxK * (size_t)rows * L.chunks);
+    float2 *row_lse = reinterpret_cast<float2 *>(ws + L.lse_off);
     trace_begin("score_chunk", s);
-    score_chunk_kernel<<<dim3(chunks, rows), kArgmaxThreads, 0, s>>>(a.draft, a.n_nodes, lse_part, top_v, top_i,
-                                                                     L.Nmax, L.V, chunk, chunks, a.k2,
-                                                                     a.top_k > 0 ? 1 : 0);
-    cudaError_t e = cudaGetLastError();
+    cudaLaunchConfig_t cc{};
+    cc.gridDim = dim3(chunks, rows, 1);
+    cc.blockDim = dim3(kArgmaxThreads, 1, 1);
+    cc.stream = s;
+    cudaLaunchAttribute ca[1];
+    ca[0].id = cudaLaunchAttributeClusterDimension;
+    ca[0].val.clusterDim.x = chunks;
+    ca[0].val.clusterDim.y = 1;
+    ca[0].val.clusterDim.z = 1;
+    cc.attrs = ca;
+    cc.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cc, score_chunk_kernel, a.draft, a.n_nodes, row_lse, a.topk_token, a.topk_lp,
+                                       a.top_k, L.Nmax, L.V, chunk, a.k2);
     trace_end(s);
     if (e != cudaSuccess) return e;
     static bool smem_set = false;
@@ -565,8 +696,7 @@ cudaError_t launch_score(const Layout &L, const ScoreArgs &a, uint8_t *ws, cudaS
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, score_tree_kernel, L, a, static_cast<const float2 *>(lse_part),
-                           static_cast<const float *>(top_v), static_cast<const int *>(top_i), chunks);
+    e = cudaLaunchKernelEx(&cfg, score_tree_kernel, L, a, static_cast<const float2 *>(row_lse));
     trace_end(s);
     return e;
 }
