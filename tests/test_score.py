@@ -167,3 +167,18 @@ def test_topk_where_the_best_entries_crowd():
     assert g["ttok"][0, 1, :8].tolist() == list(range(8000, 8008))
     assert g["ttok"][0, 2].tolist() == list(range(16))
     assert g["ttok"][0, 3].tolist() == [17, 40000, 77824, 100000, V - 1] + list(range(11))
+
+
+def test_budget_when_thousands_of_candidates_tie():
+    """Constant draft rows on a 256-node star: the root's candidates lead
+    and the other 2040 are exactly equal, so the selection (ties to the
+    lower (node, rank)) takes more than a short list can hold."""
+    B, N, V = 1, 256, 4096
+    draft = torch.zeros((B, N, V), dtype=torch.bfloat16)
+    parents = torch.tensor([[-1] + [0] * (N - 1)], dtype=torch.int32)
+    tokens = torch.arange(N, dtype=torch.int32).reshape(1, N)
+    for k, budget in ((8, 64), (8, 256), (2, 100)):
+        g, r, st = compare(draft, tokens, parents, torch.tensor([N], dtype=torch.int32), 1.0, k, budget)
+        assert st == 0
+        np.testing.assert_array_equal(g["cpar"][0], r["cand_parent"][0])
+        np.testing.assert_array_equal(g["ctok"][0], r["cand_token"][0])

@@ -39,6 +39,7 @@ namespace {
 constexpr int kScoreThreads = 256;           // = kMaxNodes: one thread per node in the tree kernel
 constexpr int kScoreCands = kMaxNodes * kScoreMaxK;   // candidates of the expansion, at most
 constexpr int kScoreMaxChunks = 4;           // chunks a row in the scan, at most
+constexpr int kScoreFastCap = 128;           // expansion candidates ranked directly, at most
 
 __device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
     uint4 v;
@@ -511,6 +512,48 @@ __global__ void __launch_bounds__(kScoreThreads)
     }
     if (!want) return;
     __syncthreads();
+    auto before = [](uint32_t ka, int ca, uint32_t kb, int cb) { return ka > kb || (ka == kb && ca < cb); };
+    // Each selected candidate's place in the output is its rank among the
+    // selected: the number ahead of it (larger key, then lower (node,
+    // rank)). With few real candidates, every one is selected and ranked.
+    auto place = [&](int nsel) {
+        for (int e = i; e < nsel; e += kScoreThreads) {
+            const uint32_t key = sh.sel_key[e];
+            const int c = sh.sel_c[e];
+            int rank = 0;
+#pragma unroll 4
+            for (int f = 0; f < nsel; ++f) rank += before(sh.sel_key[f], sh.sel_c[f], key, c) ? 1 : 0;
+            if (rank < a.budget) {
+                const size_t o = (size_t)b * a.budget + rank;
+                a.cand_parent[o] = c / K;
+                a.cand_token[o] = sh.cand_tok[c];
+                a.cand_score[o] = sh.cand_s[c];
+            }
+        }
+        for (int r = nsel + i; r < a.budget; r += kScoreThreads) {   // fewer candidates than the budget
+            const size_t o = (size_t)b * a.budget + r;
+            a.cand_parent[o] = -1;
+            a.cand_token[o] = -1;
+            a.cand_score[o] = kNaN;
+        }
+    };
+    int mine_real = 0;
+    for (int s = 0; s < K && i < Nmax; ++s) mine_real += sh.cand_key[i * K + s] != 0u ? 1 : 0;
+    if (__syncthreads_count(mine_real > 0) * K <= kScoreFastCap) {   // at most kScoreFastCap real ones
+        if (i == 0) sh.n_sel = 0;
+        __syncthreads();
+        for (int s = 0; s < K && i < Nmax; ++s) {
+            const uint32_t key = sh.cand_key[i * K + s];
+            if (key != 0u) {
+                const int at = atomicAdd(&sh.n_sel, 1);
+                sh.sel_key[at] = key;
+                sh.sel_c[at] = i * K + s;
+            }
+        }
+        __syncthreads();
+        place(sh.n_sel);
+        return;
+    }
     // The budget-th largest key T by a radix select (four 8-bit digits,
     // shared-memory histograms); then every candidate above T, and those at
     // T in (node, rank) order until the budget is met, are compacted and
@@ -609,6 +652,10 @@ __global__ void __launch_bounds__(kScoreThreads)
     }
     __syncthreads();
     const int nsel = sh.n_sel;
+    if (nsel <= kScoreFastCap) {
+        place(nsel);
+        return;
+    }
     int C = 1;
     while (C < nsel) C <<= 1;
     for (int k = nsel + i; k < C; k += kScoreThreads) {
@@ -616,7 +663,6 @@ __global__ void __launch_bounds__(kScoreThreads)
         sh.sel_c[k] = 0x7FFFFFFF;
     }
     __syncthreads();
-    auto before = [](uint32_t ka, int ca, uint32_t kb, int cb) { return ka > kb || (ka == kb && ca < cb); };
     for (int size = 2; size <= C; size <<= 1) {
         for (int stride = size >> 1; stride > 0; stride >>= 1) {
             for (int t = i; t < C / 2; t += kScoreThreads) {
