@@ -246,8 +246,9 @@ JF_API int32_t jf_tree_verify(const void *logits, const int32_t *tree_tokens,
  *                    malformed tree
  *   max_depth        >= 0: the walk goes no deeper
  * The workspace is the one jf_workspace_bytes(shape) sizes. Each sequence
- * is walked by a cluster of 8 CTAs. Returns as jf_tree_verify; a malformed
- * tree raises JF_STATUS_BAD_TREE.
+ * is walked by a cluster of 16 CTAs (8 when B * 16 exceeds the SM count or
+ * the device refuses clusters of 16). Returns as jf_tree_verify; a
+ * malformed tree raises JF_STATUS_BAD_TREE.
  */
 JF_API int32_t jf_tree_verify_sample(const void *target_logits, const void *draft_logits,
                                      const int32_t *tree_tokens, const int32_t *parents,

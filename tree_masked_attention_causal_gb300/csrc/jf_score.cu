@@ -40,6 +40,7 @@ constexpr int kScoreThreads = 256;           // = kMaxNodes: one thread per node
 constexpr int kScoreCands = kMaxNodes * kScoreMaxK;   // candidates of the expansion, at most
 constexpr int kScoreMaxChunks = 4;           // chunks a row in the scan, at most
 constexpr int kScoreFastCap = 128;           // expansion candidates ranked directly, at most
+constexpr int kScoreKeepCap = 256;           // a chunk's candidates ranked directly, at most
 
 __device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
     uint4 v;
@@ -150,6 +151,72 @@ __device__ __forceinline__ float bound_of(const volatile float *sbound) {
     return T;
 }
 
+// The chunk's kScoreMaxK best by a second pass over the vectors whose
+// maximum reaches T: a sorted list per warp, then the block's best taken
+// from the warps' lists one at a time and stored at dst_v / dst_i (a CTA's
+// slot in its cluster's CTA 0). Called by the whole block; out of line, so
+// that the scan keeps its registers.
+__device__ __noinline__ void chunk_lists(const uint4 *src, int nvec, int e0, float T, float my_max, uint32_t dst_v,
+                                         uint32_t dst_i) {
+    constexpr float kNegInf = -__builtin_huge_valf();
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const unsigned full = 0xffffffffu;
+    __shared__ float swv[kArgmaxThreads / 32];
+    __shared__ int swi[kArgmaxThreads / 32];
+    WarpTop wt{kNegInf, -1, kNegInf, -1};
+    const bool mine = my_max >= T;
+    if (__any_sync(full, mine)) {
+        // the loop bound is the same for the whole warp, so every lane
+        // reaches every ballot; other lanes take part with live = false
+        for (int k0b = 0; k0b < nvec; k0b += kArgmaxThreads * kArgmaxVecs) {
+            const int k0 = k0b + tid;
+            uint4 v[kArgmaxVecs];
+#pragma unroll
+            for (int u = 0; u < kArgmaxVecs; ++u) {
+                const int k = k0 + u * kArgmaxThreads;
+                if (mine && k < nvec) v[u] = ld_stream(src + k);
+            }
+#pragma unroll
+            for (int u = 0; u < kArgmaxVecs; ++u) {
+                const int k = k0 + u * kArgmaxThreads;
+                const bool live = mine && k < nvec;
+                const float vm = live ? vm_of(v[u]) : kNegInf;
+                if (__any_sync(full, live && vm >= T && !(vm < wt.thr_v)))
+                    wt = warp_take(wt, v[u], live, e0 + 8 * k, T);
+            }
+        }
+    }
+    // the block's kScoreMaxK best: each round every warp offers the
+    // head of its list, the best offer is stored, and its warp drops
+    // its head
+    for (int r = 0; r < kScoreMaxK; ++r) {
+        if (lane == 0) {
+            swv[warp] = wt.ev;
+            swi[warp] = wt.ei;
+        }
+        __syncthreads();
+        float bv = swv[0];
+        int bi = swi[0], bw = 0;
+        for (int w2 = 1; w2 < kArgmaxThreads / 32; ++w2)
+            if (ahead(swv[w2], swi[w2], bv, bi)) {
+                bv = swv[w2];
+                bi = swi[w2];
+                bw = w2;
+            }
+        __syncthreads();
+        if (tid == 0) {
+            st_cluster(dst_v + 4 * r, __float_as_uint(bv));
+            st_cluster(dst_i + 4 * r, (uint32_t)bi);
+        }
+        if (warp == bw && bi >= 0) {                      // the winning warp drops its head
+            const float nv = __shfl_down_sync(full, wt.ev, 1);
+            const int ni = __shfl_down_sync(full, wt.ei, 1);
+            wt.ev = lane < kScoreMaxK - 1 ? nv : kNegInf;
+            wt.ei = lane < kScoreMaxK - 1 ? ni : -1;
+        }
+    }
+}
+
 __global__ void __launch_bounds__(kArgmaxThreads)
     score_chunk_kernel(const __nv_bfloat16 *__restrict__ draft, const int32_t *__restrict__ n_nodes,
                        float2 *__restrict__ row_lse, int32_t *__restrict__ topk_token, float *__restrict__ topk_lp,
@@ -169,8 +236,6 @@ __global__ void __launch_bounds__(kArgmaxThreads)
     const unsigned full = 0xffffffffu;
     __shared__ float2 sacc[kArgmaxThreads / 32];
     __shared__ float sbound[kArgmaxThreads / 32];
-    __shared__ float swv[kArgmaxThreads / 32];
-    __shared__ int swi[kArgmaxThreads / 32];
     __shared__ int s_over;
     volatile float *vbound = sbound;
     float2 acc = make_float2(kNegInf, 0.f);
@@ -269,13 +334,14 @@ __global__ void __launch_bounds__(kArgmaxThreads)
         st_cluster(dst + 4, __float_as_uint(t.y));
     }
     T = want_top && nvec > 0 ? bound_of(vbound) : kNegInf;    // every warp's final pair
-    if (!want_top) {
-    } else if (nvec == 0 || s_over == 0) {
-        // only the candidates at or above the final bound can rank below
-        // kScoreMaxK: those are compacted, then each is ranked among them
-        __shared__ int s_keep;
-        __shared__ float s_kv[kScoreCap];
-        __shared__ int s_ki[kScoreCap];
+    // only the candidates at or above the final bound can rank below
+    // kScoreMaxK: those are compacted, then (when few) each is ranked among
+    // them
+    __shared__ int s_keep;
+    __shared__ float s_kv[kScoreCap];
+    __shared__ int s_ki[kScoreCap];
+    const bool slots = want_top && (nvec == 0 || s_over == 0);
+    if (slots) {
         if (tid == 0) s_keep = 0;
         __syncthreads();
         for (int q = 0; q < ncand; ++q) {                     // this thread's own
@@ -287,9 +353,12 @@ __global__ void __launch_bounds__(kArgmaxThreads)
             }
         }
         __syncthreads();
-        const int keep = s_keep;
-        const uint32_t dst_v = map_to_rank(smem_u32(&s_all_v[crank * kScoreMaxK]), 0);
-        const uint32_t dst_i = map_to_rank(smem_u32(&s_all_i[crank * kScoreMaxK]), 0);
+    }
+    const int keep = slots ? s_keep : kScoreCap + 1;
+    const uint32_t dst_v = map_to_rank(smem_u32(&s_all_v[crank * kScoreMaxK]), 0);
+    const uint32_t dst_i = map_to_rank(smem_u32(&s_all_i[crank * kScoreMaxK]), 0);
+    if (!want_top) {
+    } else if (keep <= kScoreKeepCap) {
         for (int t = tid; t < keep; t += kArgmaxThreads) {
             const float x = s_kv[t];
             const int xi = s_ki[t];
@@ -306,61 +375,10 @@ __global__ void __launch_bounds__(kArgmaxThreads)
             st_cluster(dst_i + 4 * tid, (uint32_t)-1);
         }
     } else {
-        // More candidates than shared memory keeps (many entries equal at
-        // the top of the chunk): a second pass over the vectors whose
-        // maximum reaches T fills a sorted list per warp.
-        WarpTop wt{kNegInf, -1, kNegInf, -1};
-        const bool mine = my_max >= T;
-        if (__any_sync(full, mine)) {
-            // the loop bound is the same for the whole warp, so every lane
-            // reaches every ballot; other lanes take part with live = false
-            for (int k0b = 0; k0b < nvec; k0b += kArgmaxThreads * kArgmaxVecs) {
-                const int k0 = k0b + tid;
-                uint4 v[kArgmaxVecs];
-#pragma unroll
-                for (int u = 0; u < kArgmaxVecs; ++u) {
-                    const int k = k0 + u * kArgmaxThreads;
-                    if (mine && k < nvec) v[u] = ld_stream(src + k);
-                }
-#pragma unroll
-                for (int u = 0; u < kArgmaxVecs; ++u) {
-                    const int k = k0 + u * kArgmaxThreads;
-                    const bool live = mine && k < nvec;
-                    const float vm = live ? vm_of(v[u]) : kNegInf;
-                    if (__any_sync(full, live && vm >= T && !(vm < wt.thr_v)))
-                        wt = warp_take(wt, v[u], live, e0 + 8 * k, T);
-                }
-            }
-        }
-        // the block's kScoreMaxK best: each round every warp offers the
-        // head of its list, the best offer is stored, and its warp drops
-        // its head
-        for (int r = 0; r < kScoreMaxK; ++r) {
-            if (lane == 0) {
-                swv[warp] = wt.ev;
-                swi[warp] = wt.ei;
-            }
-            __syncthreads();
-            float bv = swv[0];
-            int bi = swi[0], bw = 0;
-            for (int w2 = 1; w2 < kArgmaxThreads / 32; ++w2)
-                if (ahead(swv[w2], swi[w2], bv, bi)) {
-                    bv = swv[w2];
-                    bi = swi[w2];
-                    bw = w2;
-                }
-            __syncthreads();
-            if (tid == 0) {
-                st_cluster(map_to_rank(smem_u32(&s_all_v[crank * kScoreMaxK + r]), 0), __float_as_uint(bv));
-                st_cluster(map_to_rank(smem_u32(&s_all_i[crank * kScoreMaxK + r]), 0), (uint32_t)bi);
-            }
-            if (warp == bw && bi >= 0) {                      // the winning warp drops its head
-                const float nv = __shfl_down_sync(full, wt.ev, 1);
-                const int ni = __shfl_down_sync(full, wt.ei, 1);
-                wt.ev = lane < kScoreMaxK - 1 ? nv : kNegInf;
-                wt.ei = lane < kScoreMaxK - 1 ? ni : -1;
-            }
-        }
+        // More candidates than the slots keep (many entries equal at the
+        // top of the chunk), or more than are worth ranking one by one (a
+        // chunk too short for the bound): the lists pass.
+        chunk_lists(src, nvec, e0, T, my_max, dst_v, dst_i);
     }
     cluster_sync_all();
     if (crank != 0) return;
