@@ -18,7 +18,8 @@
 // each rejection costs one pass over the vocabulary for the new mass.
 //
 //  lse_chunk_kernel    HBM-bound scan of both logits arrays, chunked like
-//                      the argmax: each CTA reduces its chunk of one row
+//                      the argmax (short chunks merged so that both arrays
+//                      fit one wave): each CTA reduces its chunk of one row
 //                      to (max z, sum 2^((z - max) log2(e) / T)).
 //  sample_walk_kernel  a cluster of 16 CTAs per sequence (8 when the
 //                      batch would not fit the SMs), launched
@@ -48,6 +49,7 @@ namespace {
 
 constexpr int kSampleCluster = 8;     // CTAs sharing one sequence's vocabulary passes
 constexpr int kSampleClusterBig = 16; // the same when the batch is small enough
+constexpr int kSampleShortChunk = 16384;  // argmax chunks shorter than this are merged for the scan
 constexpr size_t kSampleNoiseMax = 192 * 1024;  // dynamic shared memory for a slice's Gumbel noise
 constexpr int kSampleThreads = 512;
 constexpr int kSampleVecs = 4;        // 16-byte loads of each row in flight per thread
@@ -425,7 +427,7 @@ __device__ void cluster_pass(WalkShared &sh, const SampleArgs &a, int V, int b, 
 enum : int { kWalkMass = 0, kWalkDone = 1 };
 
 __global__ void __launch_bounds__(kSampleThreads, 2)
-    sample_walk_kernel(const Layout L, const SampleArgs a, const float2 *__restrict__ part) {
+    sample_walk_kernel(const Layout L, const SampleArgs a, const float2 *__restrict__ part, int chunks) {
     __shared__ WalkShared sh;
     const uint32_t rank = cluster_rank();
     const int b = blockIdx.y, tid = threadIdx.x;
@@ -508,10 +510,10 @@ __global__ void __launch_bounds__(kSampleThreads, 2)
     // every node row's normalisers, merged from the scan's chunks in chunk order
     for (int t = tid; t < 2 * n; t += kSampleThreads) {
         const int i = t >> 1, which = t & 1;
-        const float2 *pr = part + ((size_t)which * rows + seq + i) * L.chunks;
+        const float2 *pr = part + ((size_t)which * rows + seq + i) * chunks;
         float2 acc = make_float2(-__int_as_float(0x7f800000), 0.f);
 #pragma unroll 4
-        for (int ch = 0; ch < L.chunks; ++ch) acc = lse_merge(acc, pr[ch], a.k2);
+        for (int ch = 0; ch < chunks; ++ch) acc = lse_merge(acc, pr[ch], a.k2);
         sh.lse[i][2 * which] = acc.x;
         sh.lse[i][2 * which + 1] = log2f(acc.y);
     }
@@ -599,9 +601,27 @@ __global__ void __launch_bounds__(kSampleThreads, 2)
 cudaError_t launch_sample(const Layout &L, const SampleArgs &a, uint8_t *ws, int sms, cudaStream_t s) {
     const int rows = L.B * L.Nmax;
     float2 *part = reinterpret_cast<float2 *>(ws + L.lse_off);
+    // The scan covers two arrays. With few rows the argmax's chunks are
+    // short (a few thousand entries) and twice as many of them overrun one
+    // wave: then the argmax's rule for twice the rows (one wave of
+    // kArgmaxCtasPerSm CTAs per SM), never more chunks than the workspace
+    // holds. Long chunks stay as the argmax cuts them (measured: one chunk
+    // a row at the tree-256 shape, 0.84 of a wave, is slower than two).
+    int per_row = L.chunks;
+    if (L.V > 0 && rows > 0 && L.chunk < kSampleShortChunk) {
+        per_row = 1;
+        const long long rows2 = 2LL * rows;
+        const long long fill = (4LL * sms + rows2 - 1) / rows2;
+        const long long wave = (long long)kArgmaxCtasPerSm * sms / rows2;
+        const long long want = fill < wave ? fill : wave;
+        const long long most = L.chunks;
+        if (want > per_row) per_row = (int)(want < most ? want : most);
+    }
+    const int chunk = L.V > 0 ? (int)align_up((size_t)ceil_div(L.V, per_row), kArgmaxGranule) : kArgmaxGranule;
+    const int chunks = L.V > 0 ? ceil_div(L.V, chunk) : 1;
     trace_begin("lse_chunk", s);
-    lse_chunk_kernel<<<dim3(L.chunks, rows, 2), kArgmaxThreads, 0, s>>>(a.target, a.draft, a.n_nodes, part, L.Nmax,
-                                                                        L.V, L.chunk, L.chunks, a.k2);
+    lse_chunk_kernel<<<dim3(chunks, rows, 2), kArgmaxThreads, 0, s>>>(a.target, a.draft, a.n_nodes, part, L.Nmax,
+                                                                      L.V, chunk, chunks, a.k2);
     cudaError_t e = cudaGetLastError();
     trace_end(s);
     if (e != cudaSuccess) return e;
@@ -654,7 +674,7 @@ cudaError_t launch_sample(const Layout &L, const SampleArgs &a, uint8_t *ws, int
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    e = cudaLaunchKernelEx(&cfg, sample_walk_kernel, L, a, static_cast<const float2 *>(part));
+    e = cudaLaunchKernelEx(&cfg, sample_walk_kernel, L, a, static_cast<const float2 *>(part), chunks);
     trace_end(s);
     return e;
 }
