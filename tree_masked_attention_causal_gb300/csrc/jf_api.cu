@@ -375,7 +375,7 @@ JF_API int32_t jf_tree_score(const void *draft_logits, const int32_t *tree_token
     a.k2 = 1.4426950408889634f / temperature;
     a.top_k = top_k;
     a.budget = budget;
-    if (launch_score(L, a, reinterpret_cast<uint8_t *>(workspace), reinterpret_cast<cudaStream_t>(stream)) !=
+    if (launch_score(L, a, reinterpret_cast<uint8_t *>(workspace), sms, reinterpret_cast<cudaStream_t>(stream)) !=
         cudaSuccess)
         return JF_ERR_CUDA;
     return JF_OK;

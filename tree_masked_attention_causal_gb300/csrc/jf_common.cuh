@@ -650,7 +650,7 @@ struct ScoreArgs {
     float k2;                 // log2(e) / temperature
     int32_t top_k, budget;
 };
-cudaError_t launch_score(const Layout &L, const ScoreArgs &a, uint8_t *ws, cudaStream_t s);
+cudaError_t launch_score(const Layout &L, const ScoreArgs &a, uint8_t *ws, int sms, cudaStream_t s);
 
 // Host-side launch bookkeeping (jf_api.cu): counts launches and records the
 // armed trace events around each one.

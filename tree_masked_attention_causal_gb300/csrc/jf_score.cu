@@ -716,14 +716,20 @@ __global__ void __launch_bounds__(kScoreThreads)
 
 }  // namespace
 
-cudaError_t launch_score(const Layout &L, const ScoreArgs &a, uint8_t *ws, cudaStream_t s) {
+cudaError_t launch_score(const Layout &L, const ScoreArgs &a, uint8_t *ws, int sms, cudaStream_t s) {
     const int rows = L.B * L.Nmax;
     // at most kScoreMaxChunks chunks a row, one cluster (the argmax cuts
-    // more when rows are few)
+    // more when rows are few); one a row when the rows alone fill a wave,
+    // so that each row's closing work (ranking, the cluster merge) is done
+    // once
     int chunk = L.chunk, chunks = L.chunks;
     if (chunks > kScoreMaxChunks) {
         chunk = (int)align_up((size_t)ceil_div(L.V, kScoreMaxChunks), kArgmaxGranule);
         chunks = ceil_div(L.V, chunk);
+    }
+    if (L.V > 0 && rows >= kArgmaxCtasPerSm * sms) {
+        chunk = (int)align_up((size_t)L.V, kArgmaxGranule);
+        chunks = 1;
     }
     float2 *row_lse = reinterpret_cast<float2 *>(ws + L.lse_off);
     trace_begin("score_chunk", s);
