@@ -41,6 +41,8 @@ constexpr int kScoreCands = kMaxNodes * kScoreMaxK;   // candidates of the expan
 constexpr int kScoreMaxChunks = 4;           // chunks a row in the scan, at most
 constexpr int kScoreFastCap = 128;           // expansion candidates ranked directly, at most
 constexpr int kScoreKeepCap = 256;           // a chunk's candidates ranked directly, at most
+constexpr int kScoreTieCap = 256;            // candidates in the budget's bucket ranked directly, at most
+static_assert(kScoreTieCap <= kScoreThreads, "one tie candidate per thread");
 
 __device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
     uint4 v;
@@ -423,10 +425,11 @@ struct ScoreShared {
     uint32_t sel_key[kScoreCands];
     int sel_c[kScoreCands];
     int hist[kScoreThreads], tie_base[kScoreThreads];
-    int sel_digit, sel_rest, n_sel;
+    int sel_digit, sel_rest, n_sel, n_tie;
+    uint32_t red_min[kScoreThreads / 32], red_max[kScoreThreads / 32];
 };
 
-__global__ void __launch_bounds__(kScoreThreads)
+__global__ void __launch_bounds__(kScoreThreads, 1)
     score_tree_kernel(const Layout L, const ScoreArgs a, const float2 *__restrict__ row_lse) {
     extern __shared__ __align__(16) unsigned char s_raw[];
     ScoreShared &sh = *reinterpret_cast<ScoreShared *>(s_raw);
@@ -470,9 +473,25 @@ __global__ void __launch_bounds__(kScoreThreads)
         if (i == 0) set_status(a.status, JF_STATUS_BAD_TREE);
         return;
     }
-    // this node's row: its normaliser (max, log2 sum), from the scan
+    // Everything the scan wrote for this node, requested at once: its row's
+    // normaliser (max, log2 sum) and, for the expansion, its K entries (the
+    // scan wrote every one: NaN and -1 where a row has fewer).
+    const bool want = a.budget > 0 && K > 0;
+    int tok[kScoreMaxK];
+    float v[kScoreMaxK];
+    {
+        const bool node = want && i < n;
+        const int32_t *tp = a.topk_token + (seq + i) * K;
+        const float *vp = a.topk_lp + (seq + i) * K;
+#pragma unroll
+        for (int s = 0; s < kScoreMaxK; ++s) {
+            const bool ok = node && s < K;
+            tok[s] = ok ? __ldcg(tp + s) : -1;
+            v[s] = ok ? __ldcg(vp + s) : kNaN;
+        }
+    }
     if (i < n) {
-        const float2 rl = row_lse[seq + i];
+        const float2 rl = __ldcg(row_lse + seq + i);
         sh.ms[i][0] = rl.x;
         sh.ms[i][1] = rl.y;
         sh.par[i] = p;
@@ -491,18 +510,21 @@ __global__ void __launch_bounds__(kScoreThreads)
     float *cur = sh.lp, *nxt = sh.lp2;
     int *ca = sh.anc, *na = sh.anc2;
     for (int r = 0; r < 8; ++r) {
+        int up = -1;
         if (i < n) {
             const int j = ca[i];
             nxt[i] = j >= 0 ? cur[i] + cur[j] : cur[i];
-            na[i] = j >= 0 ? ca[j] : -1;
+            up = j >= 0 ? ca[j] : -1;
+            na[i] = up;
         }
-        __syncthreads();
+        const bool more = __syncthreads_or(up >= 0);
         float *t = cur;
         cur = nxt;
         nxt = t;
         int *ta = ca;
         ca = na;
         na = ta;
+        if (!more) break;                                      // every path is summed
     }
     const float path = i < n ? cur[i] : kNaN;
     if (i < Nmax) {
@@ -512,25 +534,44 @@ __global__ void __launch_bounds__(kScoreThreads)
     // this node's top-k, written by the scan (padding rows get none), and
     // the expansion's candidates with an order-preserving key: larger score
     // -> larger key, no candidate -> 0
-    const bool want = a.budget > 0 && K > 0;
-    for (int s = 0; s < K && i < Nmax; ++s) {
-        if (i >= n) {
+    if (i < Nmax && i >= n) {
+        for (int s = 0; s < K; ++s) {
             a.topk_token[(seq + i) * K + s] = -1;
             a.topk_lp[(seq + i) * K + s] = kNaN;
         }
-        if (want) {
-            const int tok = i < n ? a.topk_token[(seq + i) * K + s] : -1;
-            const float v = tok >= 0 ? a.topk_lp[(seq + i) * K + s] : kNaN;
-            const float sc = path + v;
-            const uint32_t u = __float_as_uint(sc);
-            sh.cand_key[i * K + s] = (tok >= 0 && sc == sc) ? ((u & 0x80000000u) ? ~u : (u | 0x80000000u)) : 0u;
-            sh.cand_s[i * K + s] = sc;
-            sh.cand_tok[i * K + s] = tok;
+    }
+    if (want && i < Nmax) {
+#pragma unroll
+        for (int s = 0; s < kScoreMaxK; ++s) {
+            if (s < K) {
+                const float sc = path + v[s];
+                const uint32_t u = __float_as_uint(sc);
+                sh.cand_key[i * K + s] = (tok[s] >= 0 && sc == sc) ? ((u & 0x80000000u) ? ~u : (u | 0x80000000u)) : 0u;
+                sh.cand_s[i * K + s] = sc;
+                sh.cand_tok[i * K + s] = tok[s];
+            }
         }
     }
     if (!want) return;
     __syncthreads();
     auto before = [](uint32_t ka, int ca, uint32_t kb, int cb) { return ka > kb || (ka == kb && ca < cb); };
+    // Appends (key, c) where pred holds, one shared-memory atomic per warp:
+    // at the front of sel_* (count n_sel) or from its back (count n_tie).
+    const int lane = i & 31;
+    auto append = [&](bool pred, bool back, uint32_t key, int c) {
+        const unsigned m = __ballot_sync(0xffffffffu, pred);
+        if (m == 0u) return;
+        const int first = __ffs(m) - 1;
+        int base = 0;
+        if (lane == first) base = atomicAdd(back ? &sh.n_tie : &sh.n_sel, __popc(m));
+        base = __shfl_sync(0xffffffffu, base, first);
+        if (pred) {
+            int at = base + __popc(m & ((1u << lane) - 1u));
+            if (back) at = kScoreCands - 1 - at;
+            sh.sel_key[at] = key;
+            sh.sel_c[at] = c;
+        }
+    };
     // Each selected candidate's place in the output is its rank among the
     // selected: the number ahead of it (larger key, then lower (node,
     // rank)). With few real candidates, every one is selected and ranked.
@@ -560,17 +601,110 @@ __global__ void __launch_bounds__(kScoreThreads)
     if (__syncthreads_count(mine_real > 0) * K <= kScoreFastCap) {   // at most kScoreFastCap real ones
         if (i == 0) sh.n_sel = 0;
         __syncthreads();
-        for (int s = 0; s < K && i < Nmax; ++s) {
-            const uint32_t key = sh.cand_key[i * K + s];
-            if (key != 0u) {
-                const int at = atomicAdd(&sh.n_sel, 1);
-                sh.sel_key[at] = key;
-                sh.sel_c[at] = i * K + s;
-            }
+        for (int s = 0; s < K; ++s) {
+            const uint32_t key = i < Nmax ? sh.cand_key[i * K + s] : 0u;
+            append(key != 0u, false, key, i * K + s);
         }
         __syncthreads();
         place(sh.n_sel);
         return;
+    }
+    if (a.budget <= kScoreFastCap) {
+        // One pass of 256 equal buckets over the keys' range: every
+        // candidate in a bucket above the budget-th key's bucket D is
+        // selected, and those in D are ranked among themselves for the rest
+        // (the selected then placed by rank). A crowded D (many equal keys)
+        // takes the radix selection below.
+        uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
+        for (int s = 0; s < K && i < Nmax; ++s) {
+            const uint32_t key = sh.cand_key[i * K + s];
+            if (key != 0u) {
+                kmin = min(kmin, key);
+                kmax = max(kmax, key);
+            }
+        }
+        kmin = __reduce_min_sync(0xffffffffu, kmin);
+        kmax = __reduce_max_sync(0xffffffffu, kmax);
+        if (lane == 0) {
+            sh.red_min[i >> 5] = kmin;
+            sh.red_max[i >> 5] = kmax;
+        }
+        sh.hist[i] = 0;                                        // 256 bins, one per thread
+        __syncthreads();
+        for (int w = 0; w < kScoreThreads / 32; ++w) {
+            kmin = min(kmin, sh.red_min[w]);
+            kmax = max(kmax, sh.red_max[w]);
+        }
+        const uint32_t range = kmax - kmin;                    // some candidate is real here
+        const int shift = max(0, 24 - __clz(range));           // (range >> shift) < 256
+        for (int s = 0; s < K && i < Nmax; ++s) {
+            const uint32_t key = sh.cand_key[i * K + s];
+            if (key != 0u) atomicAdd(&sh.hist[(key - kmin) >> shift], 1);
+        }
+        __syncthreads();
+        if (i < 32) {                                          // warp 0: the bucket holding rank budget
+            int cnt[8], sum = 0;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {                      // lane l takes bins 255 - 8l .. 248 - 8l
+                cnt[q] = sh.hist[255 - 8 * i - q];
+                sum += cnt[q];
+            }
+            int incl = sum;                                    // lanes before: higher buckets
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (i >= o) incl += y;
+            }
+            int before_me = incl - sum, found = -1, rest = 0;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                if (found < 0 && a.budget > before_me && a.budget <= before_me + cnt[q]) {
+                    found = 255 - 8 * i - q;
+                    rest = a.budget - before_me;
+                }
+                before_me += cnt[q];
+            }
+            const unsigned hit = __ballot_sync(0xffffffffu, found >= 0);
+            if (hit) {
+                const int src = __ffs(hit) - 1;
+                found = __shfl_sync(0xffffffffu, found, src);
+                rest = __shfl_sync(0xffffffffu, rest, src);
+            }
+            if (i == 0) {
+                sh.sel_digit = found;                          // -1: fewer candidates than the budget
+                sh.sel_rest = rest;
+                sh.n_sel = 0;
+                sh.n_tie = 0;
+            }
+        }
+        __syncthreads();
+        const int D = sh.sel_digit, need = sh.sel_rest;
+        // selected ones from the front of sel_*, bucket D's from the back
+        for (int s = 0; s < K; ++s) {
+            const uint32_t key = i < Nmax ? sh.cand_key[i * K + s] : 0u;
+            const int bk = (int)((key - kmin) >> shift);
+            append(key != 0u && (D < 0 || bk > D), false, key, i * K + s);
+            append(key != 0u && D >= 0 && bk == D, true, key, i * K + s);
+        }
+        __syncthreads();
+        const int ntie = sh.n_tie;
+        if (D < 0 || ntie <= kScoreTieCap) {                  // kScoreTieCap <= kScoreThreads: one each
+            uint32_t key = 0u;
+            int c = 0, rank = need;
+            if (D >= 0 && i < ntie) {
+                key = sh.sel_key[kScoreCands - 1 - i];
+                c = sh.sel_c[kScoreCands - 1 - i];
+                rank = 0;
+                for (int f = 0; f < ntie; ++f)
+                    rank += before(sh.sel_key[kScoreCands - 1 - f], sh.sel_c[kScoreCands - 1 - f], key, c) ? 1 : 0;
+            }
+            __syncthreads();                                   // the tie entries are read before any append
+            append(rank < need, false, key, c);
+            __syncthreads();
+            place(sh.n_sel);
+            return;
+        }
+        __syncthreads();
     }
     // The budget-th largest key T by a radix select (four 8-bit digits,
     // shared-memory histograms); then every candidate above T, and those at
