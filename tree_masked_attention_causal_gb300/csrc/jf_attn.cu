@@ -24,7 +24,8 @@
 //    equal contiguous range per CTA. A CTA walks its range as one or a few
 //    items (one per unit it touches). A unit covered by a single range is
 //    normalised and written as bf16 here. Every piece of a unit covered by
-//    several ranges writes fp32 (O, m, l) partials, which the combine kernel
+//    several ranges writes its rows O / l as fp16, scaled by 2^-e per half
+//    row, with (m, l, e) in fp32 beside them, which the combine kernel
 //    merges; the CTA where a unit starts records the unit's split plan.
 //  * One CTA per SM, 12 warps:
 //      warps 0-7  softmax: warp w owns TMEM lanes 32 (w % 4).. (rows) for
