@@ -626,16 +626,25 @@ cudaError_t launch_sample(const Layout &L, const SampleArgs &a, uint8_t *ws, int
     trace_end(s);
     if (e != cudaSuccess) return e;
     trace_begin("sample_walk", s);
-    // 16 CTAs a sequence when the device schedules clusters of 16 and the
-    // batch leaves SMs for them, else 8 (the portable size)
-    static int big_ok = -1;
-    if (big_ok < 0) {
-        big_ok = 0;
+    // Once per device: the walk's shared-memory opt-in, then whether the
+    // device schedules clusters of 16 of it (with that shared memory). 16
+    // CTAs a sequence when it does and the batch leaves SMs for them, else 8
+    // (the portable size).
+    static int clusters_of[64] = {0};                    // 0: not yet asked; else 8 or 16
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaGetLastError();
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (clusters_of[dev] == 0) {
+        if (cudaFuncSetAttribute(sample_walk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kSampleNoiseMax) != cudaSuccess)
+            return cudaGetLastError();
+        int ok16 = 0;
         if (cudaFuncSetAttribute(sample_walk_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
             cudaSuccess) {
             cudaLaunchConfig_t probe{};
             probe.gridDim = dim3(kSampleClusterBig, 1, 1);
             probe.blockDim = dim3(kSampleThreads, 1, 1);
+            probe.dynamicSmemBytes = kSampleNoiseMax;
             cudaLaunchAttribute ca[1];
             ca[0].id = cudaLaunchAttributeClusterDimension;
             ca[0].val.clusterDim.x = kSampleClusterBig;
@@ -645,21 +654,16 @@ cudaError_t launch_sample(const Layout &L, const SampleArgs &a, uint8_t *ws, int
             probe.numAttrs = 1;
             int clusters = 0;
             if (cudaOccupancyMaxActiveClusters(&clusters, sample_walk_kernel, &probe) == cudaSuccess && clusters > 0)
-                big_ok = 1;
+                ok16 = 1;
         }
         cudaGetLastError();                                  // a refused query leaves no error behind
+        clusters_of[dev] = ok16 ? kSampleClusterBig : kSampleCluster;
     }
-    const int kc = (big_ok && L.B * kSampleClusterBig <= sms) ? kSampleClusterBig : kSampleCluster;
+    const int kc = (clusters_of[dev] == kSampleClusterBig && L.B * kSampleClusterBig <= sms) ? kSampleClusterBig
+                                                                                            : kSampleCluster;
     // room for the Gumbel noise of one worker CTA's vocabulary slice, if it fits
     const size_t noise = (size_t)((L.V / 8 + kc - 2) / (kc - 1)) * 32;
     const size_t dyn = noise <= kSampleNoiseMax ? noise : 0;
-    static bool dyn_set = false;
-    if (!dyn_set) {
-        if (cudaFuncSetAttribute(sample_walk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kSampleNoiseMax) != cudaSuccess)
-            return cudaGetLastError();
-        dyn_set = true;
-    }
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(kc, L.B, 1);
     cfg.blockDim = dim3(kSampleThreads, 1, 1);

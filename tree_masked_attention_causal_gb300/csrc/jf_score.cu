@@ -882,12 +882,17 @@ cudaError_t launch_score(const Layout &L, const ScoreArgs &a, uint8_t *ws, int s
                                        a.top_k, L.Nmax, L.V, chunk, a.k2);
     trace_end(s);
     if (e != cudaSuccess) return e;
-    static bool smem_set = false;
-    if (!smem_set) {
+    // the tree kernel's shared-memory opt-in, once per device
+    static bool smem_set[64] = {false};
+    int dev = 0;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!smem_set[dev]) {
         e = cudaFuncSetAttribute(score_tree_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)sizeof(ScoreShared));
         if (e != cudaSuccess) return e;
-        smem_set = true;
+        smem_set[dev] = true;
     }
     trace_begin("score_tree", s);
     cudaLaunchConfig_t cfg{};
