@@ -182,3 +182,11 @@ def test_budget_when_thousands_of_candidates_tie():
         assert st == 0
         np.testing.assert_array_equal(g["cpar"][0], r["cand_parent"][0])
         np.testing.assert_array_equal(g["ctok"][0], r["cand_token"][0])
+
+
+def test_largest_direct_budget_and_top16_at_tree256():
+    """Top 16 and a budget of 128 (the largest the bucket selection takes)
+    on the Qwen3-8B tree-256 shape: 4096 candidates a sequence."""
+    inp = synth.make_sample_inputs(synth.WORKLOADS["qwen3_8b_tree256"])
+    _, _, st = compare(inp["draft_logits"], inp["tokens"], inp["parents"], inp["n_nodes"], 1.0, 16, 128)
+    assert st == 0
