@@ -49,7 +49,7 @@
 //  * Softmax per tile (one warp per row quadrant): one 128-column TMEM load
 //    for the row max, the running max handed over from the previous tile's
 //    owner, then ex2 on the MUFU pipe, bf16 packing and the P store in a
-//    rolled loop over 32-column chunks read again from TMEM; the scaling
+//    rolled loop over 64-column chunks read again from TMEM; the scaling
 //    and the row sums use packed f32x2 arithmetic. Instruction fetch is a
 //    first-order cost for this kernel, so the hot loop is kept small.
 //  * Online softmax in the exp2 domain, lazy rescale: O is rescaled only
@@ -515,7 +515,7 @@ __device__ __forceinline__ uint4 ancestor_bits(const int32_t *parents, int node,
 // the max, after the PV of the previous tile has completed.
 //
 // The warp reads the tile's whole 128-key row once for the row max, then
-// runs the exp pass over 32-column chunks read again from TMEM. The softmax
+// runs the exp pass over 64-column chunks read again from TMEM. The softmax
 // warpgroups get 216 registers per thread (setmaxnreg), the producer and
 // issuer warpgroup 72. P (bf16 pairs) goes back over the S columns 0-63 of
 // its buffer.
@@ -664,27 +664,27 @@ __device__ __forceinline__ void softmax_loop(const AttnMaps &maps, const Layout 
                 m_own = m_run;
             }
             const float neg_m = (m_run == kNegInf) ? 0.f : -m_run;
-            // exp pass in four rolled 32-key chunks, each read again from
+            // exp pass in two rolled 64-key chunks, each read again from
             // TMEM: one copy of the exp code keeps the hot loop small. The
             // scaling and the sums use packed f32x2 arithmetic (one
             // instruction per key pair).
             const uint64_t sl2x2 = f32x2(sl2, sl2), negm2 = f32x2(neg_m, neg_m);
             uint64_t lsum2 = f32x2(0.f, 0.f);
 #pragma unroll 1
-            for (int h = 0; h < 4; ++h) {
-                uint32_t sh[32];
-                tmem_ld32(t_s + 32 * h, sh);
-                uint32_t pv[16];
+            for (int h = 0; h < 2; ++h) {
+                uint32_t sh[64];
+                tmem_ld64(t_s + 64 * h, sh);
+                uint32_t pv[32];
                 uint64_t sum2[2] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f)};
 #pragma unroll
-                for (int c = 0; c < 32; c += 2) {
+                for (int c = 0; c < 64; c += 2) {
                     const float2 x = unpack_f32x2(fma_f32x2(f32x2(sh[c], sh[c + 1]), sl2x2, negm2));
                     const float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
                     sum2[(c >> 1) & 1] = add_f32x2(sum2[(c >> 1) & 1], f32x2(p0, p1));
                     pv[c >> 1] = pack_bf16x2(p0, p1);
                 }
                 lsum2 = add_f32x2(lsum2, add_f32x2(sum2[0], sum2[1]));
-                tmem_st16(t_s + 16 * h, pv);               // P of keys 32h.. -> S columns 16h..
+                tmem_st32(t_s + 32 * h, pv);               // P of keys 64h.. -> S columns 32h..
             }
             const float2 ls = unpack_f32x2(lsum2);
             l_own += ls.x + ls.y;
