@@ -125,17 +125,41 @@ __device__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
     return true;
 }
 
+// Block-table entries of a few consecutive prefix tiles of one sequence,
+// one page a lane: lane j holds page (t0 << (7 - page_lg)) + j, clamped to
+// the sequence's last page, so no entry past the prefix is read. One load
+// serves 32 pages (4 tiles of 16-row pages), and a producer issues it before
+// its wait on the ring stage so that the read overlaps the wait.
+struct PageWindow {
+    int b = -1, t0 = 0, phys = 0;
+    // Make tile t of sequence b (prefix length P) covered; whole warp.
+    __device__ __forceinline__ void cover(const AttnArgs &a, int b_, int P, int t, int lane) {
+        const int lg = a.page_lg, span = 32 >> (7 - lg);
+        if (b_ == b && t >= t0 && t < t0 + span) return;
+        const int last = max(0, ((P + (1 << lg) - 1) >> lg) - 1);
+        b = b_;
+        t0 = t;
+        phys = a.block_table[(size_t)b_ * a.pages_per_seq + min((t << (7 - lg)) + lane, last)];
+    }
+    // The physical page that lane loads for tile t (covered); whole warp.
+    __device__ __forceinline__ int page_of(const AttnArgs &a, int t, int lane) const {
+        return __shfl_sync(0xffffffffu, phys, (((t - t0) << (7 - a.page_lg)) + lane) & 31);
+    }
+};
+
 // Prefix tile t of KV head kh of sequence b (keys t * 128 ..) into the
 // shared tile at dst: one box per 64 columns from the contiguous cache, or,
-// paged, one box per page and 64 columns, lane j loading page j. Pages past
+// paged, one box per page and 64 columns, lane j loading page j, whose
+// physical number `phys` the caller took from its PageWindow. Pages past
 // the sequence's last one (the tile's ragged end, masked later) reload that
-// last page, so no block-table entry past the prefix is read. Called by the
-// whole warp after lane 0 has set the barrier's expected bytes.
-template <int D>
+// last page. Called by the whole warp after lane 0 has set the barrier's
+// expected bytes.
+template <int D, bool kPaged>
 __device__ __forceinline__ void load_prefix_tile(const CUtensorMap *map, const AttnArgs &a, const Layout &L,
-                                                 uint32_t dst, int b, int kh, int P, int t, uint32_t bar, int lane) {
+                                                 uint32_t dst, int b, int kh, int t, int phys, uint32_t bar,
+                                                 int lane) {
     using C = AttnCfg<D>;
-    if (a.page_lg < 0) {
+    if (!kPaged) {
         if (lane == 0)
             for (int dc = 0; dc < C::kBoxes; ++dc)
                 tma_load_3d(dst + dc * (kBN * 128), map, dc * 64, t * kBN, b * L.Hkv + kh, bar);
@@ -143,15 +167,12 @@ __device__ __forceinline__ void load_prefix_tile(const CUtensorMap *map, const A
     }
     const int lg = a.page_lg, per_tile = kBN >> lg;
     if (lane < per_tile) {
-        const int last = max(0, ((P + (1 << lg) - 1) >> lg) - 1);
-        const int page = min((t << (7 - lg)) + lane, last);
-        const int phys = a.block_table[(size_t)b * a.pages_per_seq + page];
         for (int dc = 0; dc < C::kBoxes; ++dc)
             tma_load_3d(dst + dc * (kBN * 128) + (lane << lg) * 128, map, dc * 64, kh, phys << lg, bar);
     }
 }
 
-template <int D>
+template <int D, bool kPaged>
 __device__ __forceinline__ void producer_loop(const AttnMaps &maps, const Layout &L, const AttnArgs &a,
                                               uint32_t sbase, uint32_t bars, ItemInfo *items_s,
                                               volatile int *abort) {
@@ -188,9 +209,12 @@ __device__ __forceinline__ void producer_loop(const AttnMaps &maps, const Layout
     bool ok = true;
     // K tile t of the current item into the next ring stage.
     int skipped = -1;                   // a load left out on purpose (stall-test build only)
+    PageWindow pw;
     auto issue_k = [&](const ItemInfo &info, int t) -> bool {
         const bool tree = t >= info.t_pre;
+        const bool paged = kPaged && !tree;
         const int ks = kc % C::NK;
+        if (paged) pw.cover(a, info.b, info.P, t, lane);
         if (!mbar_wait(bar(C::B_K_EMPTY + ks), ((kc / C::NK) & 1) ^ 1, abort, a.status)) return false;
 #ifdef JF_STALL_TEST
         if (kc == 0) {                  // never arrives: the first QK^T waits until its limit
@@ -208,7 +232,9 @@ __device__ __forceinline__ void producer_loop(const AttnMaps &maps, const Layout
                     tma_load_3d(dst + dc * (kBN * 128), &maps.tree_k, dc * 64, info.kh,
                                 info.b * L.Nmax + (t - info.t_pre) * kBN, bar(C::B_K_FULL + ks));
         } else {
-            load_prefix_tile<D>(&maps.k_cache, a, L, dst, info.b, info.kh, info.P, t, bar(C::B_K_FULL + ks), lane);
+            load_prefix_tile<D, kPaged>(&maps.k_cache, a, L, dst, info.b, info.kh, t,
+                                        paged ? pw.page_of(a, t, lane) : 0,
+                                        bar(C::B_K_FULL + ks), lane);
         }
         __syncwarp();
         ++kc;
@@ -315,7 +341,7 @@ __device__ __forceinline__ bool next_item(uint32_t bars, const ItemInfo *items_s
 // V producer: the V tiles of each item into the NV-stage ring. It runs apart
 // from the Q/K producer so that a K load never waits behind a V stage that a
 // slower PV still holds.
-template <int D>
+template <int D, bool kPaged>
 __device__ __forceinline__ void v_producer_loop(const AttnMaps &maps, const Layout &L, const AttnArgs &a,
                                                 uint32_t sbase, uint32_t bars, const ItemInfo *items_s,
                                                 volatile int *abort) {
@@ -325,12 +351,15 @@ __device__ __forceinline__ void v_producer_loop(const AttnMaps &maps, const Layo
     int ic = 0, vc = 0;
     ItemInfo info;
     bool ok = true;
+    PageWindow pw;
     while (ok && next_item<D>(bars, items_s, ic, info, abort, a.status)) {
         const int slot = (ic - 1) & 1;
         {
             for (int t = info.tb; t < info.te; ++t) {
                 const bool tree = t >= info.t_pre;
+                const bool paged = kPaged && !tree;
                 const int vs = vc % C::NV;
+                if (paged) pw.cover(a, info.b, info.P, t, lane);
                 if (!mbar_wait(bar(C::B_V_EMPTY + vs), ((vc / C::NV) & 1) ^ 1, abort, a.status)) { ok = false; break; }
                 if (lane == 0) mbar_arrive_expect_tx(bar(C::B_V_FULL + vs), C::kTileBytes);
                 __syncwarp();
@@ -341,8 +370,8 @@ __device__ __forceinline__ void v_producer_loop(const AttnMaps &maps, const Layo
                             tma_load_3d(dst + dc * (kBN * 128), &maps.tree_v, dc * 64, info.kh,
                                         info.b * L.Nmax + (t - info.t_pre) * kBN, bar(C::B_V_FULL + vs));
                 } else {
-                    load_prefix_tile<D>(&maps.v_cache, a, L, dst, info.b, info.kh, info.P, t, bar(C::B_V_FULL + vs),
-                                        lane);
+                    load_prefix_tile<D, kPaged>(&maps.v_cache, a, L, dst, info.b, info.kh, t,
+                                        paged ? pw.page_of(a, t, lane) : 0, bar(C::B_V_FULL + vs), lane);
                 }
                 __syncwarp();
                 ++vc;
@@ -815,7 +844,7 @@ __device__ __forceinline__ void softmax_loop(const AttnMaps &maps, const Layout 
     }
 }
 
-template <int D>
+template <int D, bool kPaged>
 __global__ void __launch_bounds__(kThreads, 1)
     tree_attention_kernel(const __grid_constant__ AttnMaps maps, const Layout L, const AttnArgs a) {
     using C = AttnCfg<D>;
@@ -885,13 +914,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp >= kSoftmaxWarps) {
         setmaxnreg_dec<kOtherRegs>();
         if (warp == kProducerWarp)
-            producer_loop<D>(maps, L, a, sbase, bars, items_s, abort);
+            producer_loop<D, kPaged>(maps, L, a, sbase, bars, items_s, abort);
         else if (warp == kQkWarp)
             qk_loop<D>(a, sbase, bars, items_s, tmem, abort);
         else if (warp == kPvWarp)
             pv_loop<D>(a, smem, sbase, bars, items_s, tmem, abort);
         else if (warp == kVProducerWarp)
-            v_producer_loop<D>(maps, L, a, sbase, bars, items_s, abort);
+            v_producer_loop<D, kPaged>(maps, L, a, sbase, bars, items_s, abort);
     } else {
         setmaxnreg_inc<kSoftmaxRegs>();
         softmax_loop<D>(maps, L, a, smem, bars, items_s, reinterpret_cast<float *>(smem + C::hand_off),
@@ -904,7 +933,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kQkWarp) tmem_dealloc(tmem, C::kTmemCols);
 }
 
-template <int D>
+template <int D, bool kPaged>
 cudaError_t launch_d(const Layout &L, const AttnMaps &m, const AttnArgs &a, cudaStream_t s) {
     using C = AttnCfg<D>;
     static_assert(C::smem_request <= 227 * 1024, "shared memory budget");
@@ -916,10 +945,10 @@ cudaError_t launch_d(const Layout &L, const AttnMaps &m, const AttnArgs &a, cuda
         // setmaxnreg hands out exactly the registers the block launched with;
         // a build with another per-thread count would make it wait forever.
         cudaFuncAttributes fa{};
-        e = cudaFuncGetAttributes(&fa, tree_attention_kernel<D>);
+        e = cudaFuncGetAttributes(&fa, tree_attention_kernel<D, kPaged>);
         if (e != cudaSuccess) return e;
         if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
-        e = cudaFuncSetAttribute(tree_attention_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(tree_attention_kernel<D, kPaged>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)C::smem_request);
         if (e != cudaSuccess) return e;
         configured_device = dev;
@@ -935,7 +964,7 @@ cudaError_t launch_d(const Layout &L, const AttnMaps &m, const AttnArgs &a, cuda
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     trace_begin("tree_attention", s);
-    e = cudaLaunchKernelEx(&cfg, tree_attention_kernel<D>, m, L, a);
+    e = cudaLaunchKernelEx(&cfg, tree_attention_kernel<D, kPaged>, m, L, a);
     if (e == cudaSuccess) e = cudaGetLastError();
     trace_end(s);
     return e;
@@ -944,7 +973,8 @@ cudaError_t launch_d(const Layout &L, const AttnMaps &m, const AttnArgs &a, cuda
 }  // namespace
 
 cudaError_t launch_tree_attention(const Layout &L, const AttnMaps &m, const AttnArgs &a, cudaStream_t s) {
-    return L.D == 128 ? launch_d<128>(L, m, a, s) : launch_d<64>(L, m, a, s);
+    if (a.page_lg >= 0) return L.D == 128 ? launch_d<128, true>(L, m, a, s) : launch_d<64, true>(L, m, a, s);
+    return L.D == 128 ? launch_d<128, false>(L, m, a, s) : launch_d<64, false>(L, m, a, s);
 }
 
 }  // namespace jf
