@@ -137,6 +137,15 @@ def test_long_ragged_prefixes_split_kv():
     check_attention(inp)
 
 
+def test_rotated_prefix_walk_ragged_with_nan_tails():
+    """Prefix K/V beyond half the L2 (167 MB here), where each unit walks its
+    prefix tiles from a rotated start: the ragged last tile of a prefix then
+    falls inside a piece, and the cache rows past it hold NaN."""
+    inp = small_inputs(10, B=3, N=24, Hq=32, Hkv=8, d=128, Pcap=24000,
+                       prefixes=torch.tensor([23999, 130, 16385], dtype=torch.int32), kv_fill=float("nan"))
+    check_attention(inp)
+
+
 @pytest.mark.parametrize("vscale", [1e5, 1e30])
 def test_values_beyond_fp16_in_split_units(vscale):
     """V far beyond fp16's largest value (65504), on prefixes long enough

@@ -71,8 +71,24 @@ namespace jf {
 namespace {
 
 struct ItemInfo {
-    int32_t valid, b, kh, qt, tb, te, t_pre, P, n, ns, slot, qtile, pad0, pad1, pad2, pad3;
+    int32_t valid, b, kh, qt, tb, te, t_pre, P, n, ns, slot, qtile, rot, pad1, pad2, pad3;
 };
+
+constexpr long long kRotateBytes = 64ll << 20;         // half the L2
+
+// The prefix tile that tile t (< t_pre) of an item stands for. When the
+// prefix K/V of the call exceed half the L2, a unit walks its prefix tiles
+// from `rot` on and wraps around, `rot` chosen so that the first range
+// boundary inside the unit falls on prefix tile 0. The pieces of the units
+// of one KV head then begin on the same few prefix tiles and move through
+// them side by side, so that L2 serves a tile to all of them after one DRAM
+// read instead of evicting it between their visits. (When the K/V fit in
+// L2 every tile is read from DRAM once anyway, and the rotation measured
+// slightly slower.) The online softmax does not depend on the order.
+__device__ __forceinline__ int prefix_tile(const ItemInfo &info, int t) {
+    const int p = t + info.rot;
+    return p >= info.t_pre ? p - info.t_pre : p;
+}
 
 template <int D>
 struct AttnCfg {
@@ -214,7 +230,8 @@ __device__ __forceinline__ void producer_loop(const AttnMaps &maps, const Layout
         const bool tree = t >= info.t_pre;
         const bool paged = kPaged && !tree;
         const int ks = kc % C::NK;
-        if (paged) pw.cover(a, info.b, info.P, t, lane);
+        const int pt = tree ? 0 : prefix_tile(info, t);
+        if (paged) pw.cover(a, info.b, info.P, pt, lane);
         if (!mbar_wait(bar(C::B_K_EMPTY + ks), ((kc / C::NK) & 1) ^ 1, abort, a.status)) return false;
 #ifdef JF_STALL_TEST
         if (kc == 0) {                  // never arrives: the first QK^T waits until its limit
@@ -232,8 +249,8 @@ __device__ __forceinline__ void producer_loop(const AttnMaps &maps, const Layout
                     tma_load_3d(dst + dc * (kBN * 128), &maps.tree_k, dc * 64, info.kh,
                                 info.b * L.Nmax + (t - info.t_pre) * kBN, bar(C::B_K_FULL + ks));
         } else {
-            load_prefix_tile<D, kPaged>(&maps.k_cache, a, L, dst, info.b, info.kh, t,
-                                        paged ? pw.page_of(a, t, lane) : 0,
+            load_prefix_tile<D, kPaged>(&maps.k_cache, a, L, dst, info.b, info.kh, pt,
+                                        paged ? pw.page_of(a, pt, lane) : 0,
                                         bar(C::B_K_FULL + ks), lane);
         }
         __syncwarp();
@@ -263,6 +280,19 @@ __device__ __forceinline__ void producer_loop(const AttnMaps &maps, const Layout
             info.P = P;
             info.n = n;
             info.t_pre = ceil_div(P, kBN);
+            // The first range boundary inside the unit's prefix tiles, if
+            // any, falls on prefix tile 0 (see prefix_tile): the first CTA
+            // whose range starts after S is the smallest c with
+            // c * total >= (S + 1) * C.
+            info.rot = 0;
+            if (info.t_pre > 1 && (long long)ps.kv_tiles * 2 * C::kTileBytes > kRotateBytes) {
+                const long long total = (long long)ps.n_ctas * ps.qt + ps.rt;
+                const int c1 = (int)(((long long)(S + 1) * ps.n_ctas + total - 1) / total);
+                if (c1 < ps.n_ctas) {
+                    const int s1 = range_start(c1, ps.qt, ps.rt, ps.n_ctas) - S;
+                    if (s1 < info.t_pre) info.rot = info.t_pre - s1;
+                }
+            }
             // Q and the first K tiles go out before the rest of the item's
             // bookkeeping, so that their latency overlaps it.
             const int qb = qc % C::NQ;
@@ -359,7 +389,8 @@ __device__ __forceinline__ void v_producer_loop(const AttnMaps &maps, const Layo
                 const bool tree = t >= info.t_pre;
                 const bool paged = kPaged && !tree;
                 const int vs = vc % C::NV;
-                if (paged) pw.cover(a, info.b, info.P, t, lane);
+                const int pt = tree ? 0 : prefix_tile(info, t);
+                if (paged) pw.cover(a, info.b, info.P, pt, lane);
                 if (!mbar_wait(bar(C::B_V_EMPTY + vs), ((vc / C::NV) & 1) ^ 1, abort, a.status)) { ok = false; break; }
                 if (lane == 0) mbar_arrive_expect_tx(bar(C::B_V_FULL + vs), C::kTileBytes);
                 __syncwarp();
@@ -370,8 +401,8 @@ __device__ __forceinline__ void v_producer_loop(const AttnMaps &maps, const Layo
                             tma_load_3d(dst + dc * (kBN * 128), &maps.tree_v, dc * 64, info.kh,
                                         info.b * L.Nmax + (t - info.t_pre) * kBN, bar(C::B_V_FULL + vs));
                 } else {
-                    load_prefix_tile<D, kPaged>(&maps.v_cache, a, L, dst, info.b, info.kh, t,
-                                        paged ? pw.page_of(a, t, lane) : 0, bar(C::B_V_FULL + vs), lane);
+                    load_prefix_tile<D, kPaged>(&maps.v_cache, a, L, dst, info.b, info.kh, pt,
+                                        paged ? pw.page_of(a, pt, lane) : 0, bar(C::B_V_FULL + vs), lane);
                 }
                 __syncwarp();
                 ++vc;
@@ -468,7 +499,7 @@ __device__ __forceinline__ void pv_loop(const AttnArgs &a, uint8_t *smem, uint32
             const int t = info.tb + j;
             int r0 = kBN;
             if (t < info.t_pre) {
-                if (t == info.t_pre - 1 && (info.P % kBN) != 0) r0 = info.P % kBN;
+                if (prefix_tile(info, t) == info.t_pre - 1 && (info.P % kBN) != 0) r0 = info.P % kBN;
             } else {
                 const int left = info.n - (t - info.t_pre) * kBN;
                 r0 = left < 0 ? 0 : (left < kBN ? left : kBN);
@@ -640,7 +671,7 @@ __device__ __forceinline__ void softmax_loop(const AttnMaps &maps, const Layout 
             const bool tree = t >= info.t_pre;
             uint4 mw = make_uint4(0u, 0u, 0u, 0u);         // ancestor bits of the tile's 128 keys
             if (tree && row_valid) mw = ancestor_bits(par_b, node, (t - info.t_pre) * kBN);
-            const int lim = (!tree && t == info.t_pre - 1) ? info.P - t * kBN : kBN;
+            const int lim = (!tree && prefix_tile(info, t) == info.t_pre - 1) ? info.P - (info.t_pre - 1) * kBN : kBN;
             const int sb = g % C::NS;
             const uint32_t t_s = t_row + sb * 128;
             // The running max so far, published by the previous tile's owner

@@ -182,6 +182,7 @@ struct PlanSeq {
     int lo, hi;         // this CTA's virtual range
     int b, P, n;        // the sequence holding virtual tile lo
     int seq_start;      // its first virtual tile
+    int kv_tiles;       // prefix tiles of all KV heads of all valid sequences
 };
 
 // Units with work in one KV head of a valid sequence.
@@ -196,7 +197,7 @@ __device__ inline PlanSeq plan_locate(const Layout &L, const int32_t *prefix_len
     PlanSeq r{};
     r.b = -1;
     int P0 = 0, n0 = 0;                              // this lane's sequence of the first 32
-    int tiles = 0, units = 0;
+    int tiles = 0, units = 0, kv = 0;
 #pragma unroll 1
     for (int b0 = 0; b0 < L.B; b0 += 32) {
         const int b = b0 + lane;
@@ -212,13 +213,16 @@ __device__ inline PlanSeq plan_locate(const Layout &L, const int32_t *prefix_len
         if (b < L.B && seq_valid(P, n, L)) {
             tiles += L.Hkv * head_tiles(P, n, L);
             units += L.Hkv * head_units(n, L);
+            kv += L.Hkv * ((P + kBN - 1) >> 7);
         }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         tiles += __shfl_xor_sync(0xffffffffu, tiles, o);
         units += __shfl_xor_sync(0xffffffffu, units, o);
+        kv += __shfl_xor_sync(0xffffffffu, kv, o);
     }
+    r.kv_tiles = kv;
     r.n_ctas = tiles > 0 ? plan_ctas(tiles, num_ctas) : 0;
     if (c >= r.n_ctas) return r;
     r.alpha = min(kSwitchTiles, tiles / r.n_ctas / 2);
