@@ -631,12 +631,20 @@ cudaError_t launch_sample(const Layout &L, const SampleArgs &a, uint8_t *ws, int
     // CTAs a sequence when it does and the batch leaves SMs for them, else 8
     // (the portable size).
     static int clusters_of[64] = {0};                    // 0: not yet asked; else 8 or 16
+    static size_t whole_sm[64] = {0};                    // dynamic shared memory that fills a block's opt-in limit
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return cudaGetLastError();
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (clusters_of[dev] == 0) {
+        cudaFuncAttributes fa{};
+        int optin = 0;
+        if (cudaFuncGetAttributes(&fa, sample_walk_kernel) != cudaSuccess ||
+            cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+            return cudaGetLastError();
+        const size_t whole = (size_t)optin > fa.sharedSizeBytes ? (size_t)optin - fa.sharedSizeBytes : 0;
+        whole_sm[dev] = whole > kSampleNoiseMax ? whole : kSampleNoiseMax;
         if (cudaFuncSetAttribute(sample_walk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kSampleNoiseMax) != cudaSuccess)
+                                 (int)whole_sm[dev]) != cudaSuccess)
             return cudaGetLastError();
         int ok16 = 0;
         if (cudaFuncSetAttribute(sample_walk_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
@@ -656,6 +664,23 @@ cudaError_t launch_sample(const Layout &L, const SampleArgs &a, uint8_t *ws, int
             if (cudaOccupancyMaxActiveClusters(&clusters, sample_walk_kernel, &probe) == cudaSuccess && clusters > 0)
                 ok16 = 1;
         }
+        // and whether clusters of 8 fit with a whole block's shared memory each
+        {
+            cudaLaunchConfig_t probe{};
+            probe.gridDim = dim3(kSampleCluster, 1, 1);
+            probe.blockDim = dim3(kSampleThreads, 1, 1);
+            probe.dynamicSmemBytes = whole_sm[dev];
+            cudaLaunchAttribute ca[1];
+            ca[0].id = cudaLaunchAttributeClusterDimension;
+            ca[0].val.clusterDim.x = kSampleCluster;
+            ca[0].val.clusterDim.y = 1;
+            ca[0].val.clusterDim.z = 1;
+            probe.attrs = ca;
+            probe.numAttrs = 1;
+            int clusters = 0;
+            if (cudaOccupancyMaxActiveClusters(&clusters, sample_walk_kernel, &probe) != cudaSuccess || clusters < 1)
+                whole_sm[dev] = 0;
+        }
         cudaGetLastError();                                  // a refused query leaves no error behind
         clusters_of[dev] = ok16 ? kSampleClusterBig : kSampleCluster;
     }
@@ -663,7 +688,16 @@ cudaError_t launch_sample(const Layout &L, const SampleArgs &a, uint8_t *ws, int
                                                                                             : kSampleCluster;
     // room for the Gumbel noise of one worker CTA's vocabulary slice, if it fits
     const size_t noise = (size_t)((L.V / 8 + kc - 2) / (kc - 1)) * 32;
-    const size_t dyn = noise <= kSampleNoiseMax ? noise : 0;
+    size_t dyn = noise <= kSampleNoiseMax ? noise : 0;
+    // With a cluster a sequence on most SMs (a batch), a walk CTA resident
+    // beside scan CTAs holds their share of the SM through the rest of the
+    // scan, which costs more than its early start gains (serving batch:
+    // 159 -> 148 µs per call). Asking for all the shared memory a block may
+    // have keeps it off every SM that still runs a scan CTA: the clusters
+    // start on SMs as the scan leaves them, their pre-wait work overlapping
+    // the scan's tail. A few clusters (one sequence) start at once; more
+    // than one wave of them at one CTA per SM keep two CTAs per SM.
+    if (L.B * kSampleClusterBig > sms && L.B * kc <= sms && noise <= whole_sm[dev]) dyn = whole_sm[dev];
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(kc, L.B, 1);
     cfg.blockDim = dim3(kSampleThreads, 1, 1);
