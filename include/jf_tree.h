@@ -141,6 +141,11 @@ JF_API size_t jf_workspace_bytes(const jf_shape *shape);
  *                256-byte aligned; its contents need no initialisation
  *   status       device int32 or NULL
  * Every bf16 pointer must be 16-byte aligned.
+ * Repeat calls on one device give bit-identical results. The order in which
+ * a row's keys are summed follows the work split over the SMs (and, when
+ * the prefix keys and values of the call exceed half the L2, a rotated
+ * order of the prefix tiles), so a device with another SM count may differ
+ * in the last bits.
  * Returns JF_OK, JF_ERR_NULL, JF_ERR_SHAPE, JF_ERR_ALIGN, JF_ERR_WORKSPACE
  * or JF_ERR_CUDA.
  */
