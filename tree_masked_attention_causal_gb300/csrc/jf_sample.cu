@@ -130,12 +130,18 @@ __global__ void __launch_bounds__(kArgmaxThreads, kArgmaxCtasPerSm)
     // the walk's clusters may start now: their work before the wait (the
     // tree, the Gumbel noise) overlaps this scan
     pdl_launch_dependents();
-    const int row = blockIdx.y, which = blockIdx.z;
-    const int b = row / Nmax, i = row - b * Nmax;
+    // Nodes from the last to the root, the sequences side by side and a
+    // node's target and draft chunks together: the walks' passes mostly read
+    // the rows of the roots and their first children, which are then the
+    // last ones read and still in L2.
+    const int nb = gridDim.y / Nmax;
+    const int i = Nmax - 1 - (int)blockIdx.y / nb, b = (int)blockIdx.y - (Nmax - 1 - i) * nb;
+    const int row = b * Nmax + i, which = blockIdx.x >= chunks ? 1 : 0;
+    const int ch = blockIdx.x - which * chunks;
     const int n = n_nodes[b];
     if (n < 1 || n > Nmax || i >= n) return;                 // padding row
     const int tid = threadIdx.x;
-    const int e0 = blockIdx.x * chunk;
+    const int e0 = ch * chunk;
     const int nvec = (min(V, e0 + chunk) - e0) >> 3;         // V % 8 == 0
     const uint4 *src = reinterpret_cast<const uint4 *>((which ? draft : target) + (size_t)row * V + e0);
     float2 acc = make_float2(-__int_as_float(0x7f800000), 0.f);
@@ -179,7 +185,7 @@ __global__ void __launch_bounds__(kArgmaxThreads, kArgmaxCtasPerSm)
         float2 t = sred[0];
         for (int w = 1; w < kArgmaxThreads / 32; ++w) t = lse_merge(t, sred[w], k2);
         const size_t rows = gridDim.y;
-        part[((size_t)which * rows + row) * chunks + blockIdx.x] = t;
+        part[((size_t)which * rows + row) * chunks + ch] = t;
     }
 }
 
@@ -620,7 +626,7 @@ cudaError_t launch_sample(const Layout &L, const SampleArgs &a, uint8_t *ws, int
     const int chunk = L.V > 0 ? (int)align_up((size_t)ceil_div(L.V, per_row), kArgmaxGranule) : kArgmaxGranule;
     const int chunks = L.V > 0 ? ceil_div(L.V, chunk) : 1;
     trace_begin("lse_chunk", s);
-    lse_chunk_kernel<<<dim3(chunks, rows, 2), kArgmaxThreads, 0, s>>>(a.target, a.draft, a.n_nodes, part, L.Nmax,
+    lse_chunk_kernel<<<dim3(2 * chunks, rows), kArgmaxThreads, 0, s>>>(a.target, a.draft, a.n_nodes, part, L.Nmax,
                                                                       L.V, chunk, chunks, a.k2);
     cudaError_t e = cudaGetLastError();
     trace_end(s);
