@@ -75,6 +75,9 @@ __device__ __forceinline__ bool ranks_before(float a, int ia, float b, int ib) {
 __global__ void __launch_bounds__(kArgmaxThreads, kArgmaxCtasPerSm)
     argmax_chunk_kernel(const __nv_bfloat16 *__restrict__ logits, const int32_t *__restrict__ n_nodes,
                         int2 *__restrict__ part, int Nmax, int V, int chunk, int chunks) {
+    // A programmatic dependent of whatever the stream ran before: nothing is
+    // read before that grid has completed, so only the launch overlaps it.
+    pdl_wait_prior_grid();
     const int row = blockIdx.y;
     const int b = row / Nmax, i = row - b * Nmax;
     const int n = n_nodes[b];
@@ -306,11 +309,20 @@ __global__ void __launch_bounds__(kMaxNodes)
 
 cudaError_t launch_argmax(const Layout &L, const __nv_bfloat16 *logits, const int32_t *n_nodes, uint8_t *ws,
                           cudaStream_t s) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(L.chunks, L.B * L.Nmax);
+    cfg.blockDim = dim3(kArgmaxThreads);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     trace_begin("argmax_chunk", s);
-    dim3 grid(L.chunks, L.B * L.Nmax);
-    argmax_chunk_kernel<<<grid, kArgmaxThreads, 0, s>>>(logits, n_nodes, reinterpret_cast<int2 *>(ws + L.amp_off),
-                                                        L.Nmax, L.V, L.chunk, L.chunks);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = cudaLaunchKernelEx(&cfg, argmax_chunk_kernel, logits, n_nodes,
+                                       reinterpret_cast<int2 *>(ws + L.amp_off), (int)L.Nmax, (int)L.V,
+                                       (int)L.chunk, (int)L.chunks);
+    if (e == cudaSuccess) e = cudaGetLastError();
     trace_end(s);
     return e;
 }
