@@ -32,6 +32,11 @@ __global__ void __launch_bounds__(kCommitThreads)
                      __nv_bfloat16 *__restrict__ v_cache, int32_t *__restrict__ prefix_lens, int Nmax, int Hkv,
                      int D, int Pcap, int max_depth, int32_t *status, const int32_t *__restrict__ block_table,
                      int page_lg, int pages_per_seq, int num_pages) {
+    // A programmatic dependent of the stream's previous kernel (normally the
+    // accept walk): nothing is read before that grid has completed. A
+    // follower may launch once this kernel has started.
+    pdl_wait_prior_grid();
+    pdl_launch_dependents();
     __shared__ int s_node[kMaxNodes + 1];
     const int b = blockIdx.x, tid = threadIdx.x;
     const int a = accept_len[b], P = prefix_lens[b], n = n_nodes[b];
@@ -111,10 +116,20 @@ cudaError_t launch_commit_kv(const Layout &L, const __nv_bfloat16 *tree_k, const
                              int32_t num_pages) {
     trace_begin("commit_kv", s);
     const int pages_per_seq = page_lg >= 0 ? L.Pcap >> page_lg : 0;
-    commit_kv_kernel<<<L.B, kCommitThreads, 0, s>>>(tree_k, tree_v, n_nodes, accept_len, accept_path, k_cache, v_cache,
-                                                     prefix_lens, L.Nmax, L.Hkv, L.D, L.Pcap, max_depth, status,
-                                                     block_table, page_lg, pages_per_seq, num_pages);
-    cudaError_t e = cudaGetLastError();
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(L.B, 1, 1);
+    cfg.blockDim = dim3(kCommitThreads, 1, 1);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, commit_kv_kernel, tree_k, tree_v, n_nodes, accept_len, accept_path,
+                                       k_cache, v_cache, prefix_lens, (int)L.Nmax, (int)L.Hkv, (int)L.D,
+                                       (int)L.Pcap, (int)max_depth, status, block_table, (int)page_lg,
+                                       pages_per_seq, (int)num_pages);
+    if (e == cudaSuccess) e = cudaGetLastError();
     trace_end(s);
     return e;
 }
