@@ -427,6 +427,7 @@ struct ScoreShared {
     int hist[kScoreThreads], tie_base[kScoreThreads];
     int sel_digit, sel_rest, n_sel, n_tie;
     uint32_t red_min[kScoreThreads / 32], red_max[kScoreThreads / 32];
+    int red_cnt[kScoreThreads / 32];
 };
 
 __global__ void __launch_bounds__(kScoreThreads, 1)
@@ -576,13 +577,23 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     // selected: the number ahead of it (larger key, then lower (node,
     // rank)). With few real candidates, every one is selected and ranked.
     auto place = [&](int nsel) {
-        for (int e = i; e < nsel; e += kScoreThreads) {
-            const uint32_t key = sh.sel_key[e];
-            const int c = sh.sel_c[e];
-            int rank = 0;
+        // `per` threads (neighbouring lanes) count the ranks of one candidate
+        // over interleaved parts of the list; the same number of rounds for
+        // every lane, so that the lanes of a group reduce together.
+        const int per = nsel <= kScoreThreads / 4 ? 4 : nsel <= kScoreThreads / 2 ? 2 : 1;
+        const int groups = kScoreThreads / per, part = i % per;
+        for (int e0 = 0; e0 < nsel; e0 += groups) {
+            const int e = e0 + i / per;
+            uint32_t key = 0u;
+            int c = 0, rank = 0;
+            if (e < nsel) {
+                key = sh.sel_key[e];
+                c = sh.sel_c[e];
 #pragma unroll 4
-            for (int f = 0; f < nsel; ++f) rank += before(sh.sel_key[f], sh.sel_c[f], key, c) ? 1 : 0;
-            if (rank < a.budget) {
+                for (int f = part; f < nsel; f += per) rank += before(sh.sel_key[f], sh.sel_c[f], key, c) ? 1 : 0;
+            }
+            for (int o = 1; o < per; o <<= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
+            if (e < nsel && part == 0 && rank < a.budget) {
                 const size_t o = (size_t)b * a.budget + rank;
                 a.cand_parent[o] = c / K;
                 a.cand_token[o] = sh.cand_tok[c];
@@ -679,12 +690,45 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         }
         __syncthreads();
         const int D = sh.sel_digit, need = sh.sel_rest;
-        // selected ones from the front of sel_*, bucket D's from the back
-        for (int s = 0; s < K; ++s) {
-            const uint32_t key = i < Nmax ? sh.cand_key[i * K + s] : 0u;
+        // Selected ones to the front of sel_*, bucket D's from the back, in
+        // (node, rank) order: each thread's two counts packed in one int,
+        // one block-wide exclusive scan gives every thread its offsets.
+        uint32_t selm = 0u, tiem = 0u;
+        for (int s = 0; s < K && i < Nmax; ++s) {
+            const uint32_t key = sh.cand_key[i * K + s];
             const int bk = (int)((key - kmin) >> shift);
-            append(key != 0u && (D < 0 || bk > D), false, key, i * K + s);
-            append(key != 0u && D >= 0 && bk == D, true, key, i * K + s);
+            if (key != 0u && (D < 0 || bk > D)) selm |= 1u << s;
+            if (key != 0u && D >= 0 && bk == D) tiem |= 1u << s;
+        }
+        const int cnt = __popc(selm) | (__popc(tiem) << 16);   // each below 2^16
+        int incl = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        if (lane == 31) sh.red_cnt[i >> 5] = incl;
+        __syncthreads();
+        int off = incl - cnt, tot = 0;
+        for (int w = 0; w < kScoreThreads / 32; ++w) {
+            const int t = sh.red_cnt[w];
+            off += w < (i >> 5) ? t : 0;
+            tot += t;
+        }
+        int os = off & 0xFFFF, ot = off >> 16;
+        for (int s = 0; s < K; ++s) {
+            if ((selm >> s) & 1u) {
+                sh.sel_key[os] = sh.cand_key[i * K + s];
+                sh.sel_c[os++] = i * K + s;
+            }
+            if ((tiem >> s) & 1u) {
+                sh.sel_key[kScoreCands - 1 - ot] = sh.cand_key[i * K + s];
+                sh.sel_c[kScoreCands - 1 - ot++] = i * K + s;
+            }
+        }
+        if (i == 0) {
+            sh.n_sel = tot & 0xFFFF;
+            sh.n_tie = tot >> 16;
         }
         __syncthreads();
         const int ntie = sh.n_tie;
