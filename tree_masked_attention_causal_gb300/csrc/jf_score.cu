@@ -541,13 +541,17 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             a.topk_lp[(seq + i) * K + s] = kNaN;
         }
     }
+    uint32_t ck[kScoreMaxK];                                   // this thread's keys, also in registers
+#pragma unroll
+    for (int s = 0; s < kScoreMaxK; ++s) ck[s] = 0u;
     if (want && i < Nmax) {
 #pragma unroll
         for (int s = 0; s < kScoreMaxK; ++s) {
             if (s < K) {
                 const float sc = path + v[s];
                 const uint32_t u = __float_as_uint(sc);
-                sh.cand_key[i * K + s] = (tok[s] >= 0 && sc == sc) ? ((u & 0x80000000u) ? ~u : (u | 0x80000000u)) : 0u;
+                ck[s] = (tok[s] >= 0 && sc == sc) ? ((u & 0x80000000u) ? ~u : (u | 0x80000000u)) : 0u;
+                sh.cand_key[i * K + s] = ck[s];
                 sh.cand_s[i * K + s] = sc;
                 sh.cand_tok[i * K + s] = tok[s];
             }
@@ -607,16 +611,48 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             a.cand_score[o] = kNaN;
         }
     };
-    int mine_real = 0;
-    for (int s = 0; s < K && i < Nmax; ++s) mine_real += sh.cand_key[i * K + s] != 0u ? 1 : 0;
-    if (__syncthreads_count(mine_real > 0) * K <= kScoreFastCap) {   // at most kScoreFastCap real ones
-        if (i == 0) sh.n_sel = 0;
+    // Thread i's candidates marked in selm to the front of sel_*, those in
+    // tiem to its back, in (node, rank) order: each thread's two counts
+    // packed in one int, one block-wide exclusive scan gives the offsets.
+    auto compact = [&](uint32_t selm, uint32_t tiem) {
+        const int cnt = __popc(selm) | (__popc(tiem) << 16);   // each below 2^16
+        int incl = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        if (lane == 31) sh.red_cnt[i >> 5] = incl;
         __syncthreads();
-        for (int s = 0; s < K; ++s) {
-            const uint32_t key = i < Nmax ? sh.cand_key[i * K + s] : 0u;
-            append(key != 0u, false, key, i * K + s);
+        int off = incl - cnt, tot = 0;
+        for (int w = 0; w < kScoreThreads / 32; ++w) {
+            const int t = sh.red_cnt[w];
+            off += w < (i >> 5) ? t : 0;
+            tot += t;
+        }
+        int os = off & 0xFFFF, ot = off >> 16;
+#pragma unroll
+        for (int s = 0; s < kScoreMaxK; ++s) {
+            if ((selm >> s) & 1u) {
+                sh.sel_key[os] = ck[s];
+                sh.sel_c[os++] = i * K + s;
+            }
+            if ((tiem >> s) & 1u) {
+                sh.sel_key[kScoreCands - 1 - ot] = ck[s];
+                sh.sel_c[kScoreCands - 1 - ot++] = i * K + s;
+            }
+        }
+        if (i == 0) {
+            sh.n_sel = tot & 0xFFFF;
+            sh.n_tie = tot >> 16;
         }
         __syncthreads();
+    };
+    uint32_t real = 0u;                                        // this thread's real candidates
+#pragma unroll
+    for (int s = 0; s < kScoreMaxK; ++s) real |= (s < K && ck[s] != 0u) ? 1u << s : 0u;
+    if (__syncthreads_count(real != 0u) * K <= kScoreFastCap) {      // at most kScoreFastCap real ones
+        compact(real, 0u);
         place(sh.n_sel);
         return;
     }
@@ -627,11 +663,11 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         // (the selected then placed by rank). A crowded D (many equal keys)
         // takes the radix selection below.
         uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
-        for (int s = 0; s < K && i < Nmax; ++s) {
-            const uint32_t key = sh.cand_key[i * K + s];
-            if (key != 0u) {
-                kmin = min(kmin, key);
-                kmax = max(kmax, key);
+#pragma unroll
+        for (int s = 0; s < kScoreMaxK; ++s) {
+            if ((real >> s) & 1u) {
+                kmin = min(kmin, ck[s]);
+                kmax = max(kmax, ck[s]);
             }
         }
         kmin = __reduce_min_sync(0xffffffffu, kmin);
@@ -648,10 +684,9 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         }
         const uint32_t range = kmax - kmin;                    // some candidate is real here
         const int shift = max(0, 24 - __clz(range));           // (range >> shift) < 256
-        for (int s = 0; s < K && i < Nmax; ++s) {
-            const uint32_t key = sh.cand_key[i * K + s];
-            if (key != 0u) atomicAdd(&sh.hist[(key - kmin) >> shift], 1);
-        }
+#pragma unroll
+        for (int s = 0; s < kScoreMaxK; ++s)
+            if ((real >> s) & 1u) atomicAdd(&sh.hist[(ck[s] - kmin) >> shift], 1);
         __syncthreads();
         if (i < 32) {                                          // warp 0: the bucket holding rank budget
             int cnt[8], sum = 0;
@@ -690,47 +725,15 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         }
         __syncthreads();
         const int D = sh.sel_digit, need = sh.sel_rest;
-        // Selected ones to the front of sel_*, bucket D's from the back, in
-        // (node, rank) order: each thread's two counts packed in one int,
-        // one block-wide exclusive scan gives every thread its offsets.
+        // selected ones to the front of sel_*, bucket D's to the back
         uint32_t selm = 0u, tiem = 0u;
-        for (int s = 0; s < K && i < Nmax; ++s) {
-            const uint32_t key = sh.cand_key[i * K + s];
-            const int bk = (int)((key - kmin) >> shift);
-            if (key != 0u && (D < 0 || bk > D)) selm |= 1u << s;
-            if (key != 0u && D >= 0 && bk == D) tiem |= 1u << s;
-        }
-        const int cnt = __popc(selm) | (__popc(tiem) << 16);   // each below 2^16
-        int incl = cnt;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += y;
+        for (int s = 0; s < kScoreMaxK; ++s) {
+            const int bk = (int)((ck[s] - kmin) >> shift);
+            if (((real >> s) & 1u) && (D < 0 || bk > D)) selm |= 1u << s;
+            if (((real >> s) & 1u) && D >= 0 && bk == D) tiem |= 1u << s;
         }
-        if (lane == 31) sh.red_cnt[i >> 5] = incl;
-        __syncthreads();
-        int off = incl - cnt, tot = 0;
-        for (int w = 0; w < kScoreThreads / 32; ++w) {
-            const int t = sh.red_cnt[w];
-            off += w < (i >> 5) ? t : 0;
-            tot += t;
-        }
-        int os = off & 0xFFFF, ot = off >> 16;
-        for (int s = 0; s < K; ++s) {
-            if ((selm >> s) & 1u) {
-                sh.sel_key[os] = sh.cand_key[i * K + s];
-                sh.sel_c[os++] = i * K + s;
-            }
-            if ((tiem >> s) & 1u) {
-                sh.sel_key[kScoreCands - 1 - ot] = sh.cand_key[i * K + s];
-                sh.sel_c[kScoreCands - 1 - ot++] = i * K + s;
-            }
-        }
-        if (i == 0) {
-            sh.n_sel = tot & 0xFFFF;
-            sh.n_tie = tot >> 16;
-        }
-        __syncthreads();
+        compact(selm, tiem);
         const int ntie = sh.n_tie;
         if (D < 0 || ntie <= kScoreTieCap) {                  // kScoreTieCap <= kScoreThreads: one each
             uint32_t key = 0u;
