@@ -418,6 +418,8 @@ struct ScoreShared {
     int anc[kMaxNodes], anc2[kMaxNodes];
     float ms[kMaxNodes][2];      // row max, log2 sum
     // the expansion's candidates (node * K + rank): order key, score, token
+    // stored rank-major: candidate (node u, rank s) at s * kScoreThreads + u,
+    // so that a thread's entries fall in distinct banks
     uint32_t cand_key[kScoreCands];
     float cand_s[kScoreCands];
     int cand_tok[kScoreCands];
@@ -551,9 +553,9 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
                 const float sc = path + v[s];
                 const uint32_t u = __float_as_uint(sc);
                 ck[s] = (tok[s] >= 0 && sc == sc) ? ((u & 0x80000000u) ? ~u : (u | 0x80000000u)) : 0u;
-                sh.cand_key[i * K + s] = ck[s];
-                sh.cand_s[i * K + s] = sc;
-                sh.cand_tok[i * K + s] = tok[s];
+                sh.cand_key[s * kScoreThreads + i] = ck[s];
+                sh.cand_s[s * kScoreThreads + i] = sc;
+                sh.cand_tok[s * kScoreThreads + i] = tok[s];
             }
         }
     }
@@ -600,8 +602,9 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             if (e < nsel && part == 0 && rank < a.budget) {
                 const size_t o = (size_t)b * a.budget + rank;
                 a.cand_parent[o] = c / K;
-                a.cand_token[o] = sh.cand_tok[c];
-                a.cand_score[o] = sh.cand_s[c];
+                const int at = (c % K) * kScoreThreads + c / K;
+                a.cand_token[o] = sh.cand_tok[at];
+                a.cand_score[o] = sh.cand_s[at];
             }
         }
         for (int r = nsel + i; r < a.budget; r += kScoreThreads) {   // fewer candidates than the budget
@@ -757,15 +760,15 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     // shared-memory histograms); then every candidate above T, and those at
     // T in (node, rank) order until the budget is met, are compacted and
     // sorted (bitonic) best first: larger score, then lower (node, rank).
-    const int total = Nmax * K;
     uint32_t prefix = 0, mask = 0;
     int want_rank = a.budget;                                  // 1-based rank of T among the candidates
     for (int pass = 0; pass < 4; ++pass) {
         const int shift = 24 - 8 * pass;
         sh.hist[i] = 0;                                        // 256 bins, one per thread
         __syncthreads();
-        for (int c = i; c < total; c += kScoreThreads) {
-            const uint32_t key = sh.cand_key[c];
+#pragma unroll
+        for (int s = 0; s < kScoreMaxK; ++s) {
+            const uint32_t key = ck[s];
             if (key != 0u && (key & mask) == prefix) atomicAdd(&sh.hist[(key >> shift) & 255u], 1);
         }
         __syncthreads();
@@ -816,7 +819,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     int my_ties = 0;
     if (!short_list)
         for (int s = 0; s < K; ++s)
-            if (i < Nmax && sh.cand_key[i * K + s] == T) ++my_ties;
+            if (i < Nmax && sh.cand_key[s * kScoreThreads + i] == T) ++my_ties;
     // exclusive prefix of ties over threads (node order)
     sh.hist[i] = my_ties;
     __syncthreads();
@@ -840,7 +843,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     __syncthreads();
     int tie_rank = sh.tie_base[i];
     for (int s = 0; s < K && i < Nmax; ++s) {
-        const uint32_t key = sh.cand_key[i * K + s];
+        const uint32_t key = sh.cand_key[s * kScoreThreads + i];
         bool take = key != 0u && (short_list || key > T);
         if (!short_list && key == T) take = tie_rank++ < want_rank;
         if (take) {
@@ -885,8 +888,9 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         if (r < nsel) {
             const int c = sh.sel_c[r];
             a.cand_parent[o] = c / K;
-            a.cand_token[o] = sh.cand_tok[c];
-            a.cand_score[o] = sh.cand_s[c];
+            const int at = (c % K) * kScoreThreads + c / K;
+            a.cand_token[o] = sh.cand_tok[at];
+            a.cand_score[o] = sh.cand_s[at];
         } else {
             a.cand_parent[o] = -1;
             a.cand_token[o] = -1;
