@@ -80,24 +80,34 @@ __global__ void __launch_bounds__(kArgmaxThreads, kArgmaxCtasPerSm)
     pdl_wait_prior_grid();
     const int row = blockIdx.y;
     const int b = row / Nmax, i = row - b * Nmax;
+    const int tid = threadIdx.x;
+    const int e0 = blockIdx.x * chunk;
+    const int nvec = (min(V, e0 + chunk) - e0) >> 3;         // V % 8 == 0
+    const uint4 *src = reinterpret_cast<const uint4 *>(logits + (size_t)row * V + e0);
+    // The first vectors go out before the row is known to be real: a
+    // padding row's logits exist too, and the latency of n_nodes overlaps
+    // theirs.
+    uint4 v[kArgmaxVecs];
+#pragma unroll
+    for (int u = 0; u < kArgmaxVecs; ++u) {
+        const int k = tid + u * kArgmaxThreads;
+        if (k < nvec) v[u] = ld_stream(src + k);
+    }
     const int n = n_nodes[b];
     if (n < 1 || n > Nmax || i >= n) {                       // padding row
         pdl_launch_dependents();
         return;
     }
-    const int tid = threadIdx.x;
-    const int e0 = blockIdx.x * chunk;
-    const int nvec = (min(V, e0 + chunk) - e0) >> 3;         // V % 8 == 0
-    const uint4 *src = reinterpret_cast<const uint4 *>(logits + (size_t)row * V + e0);
     float best = -__int_as_float(0x7f800000);
     int best_k = -1;
     uint4 best_v = make_uint4(0u, 0u, 0u, 0u);              // the vector that holds it
     for (int k0 = tid; k0 < nvec; k0 += kArgmaxThreads * kArgmaxVecs) {
-        uint4 v[kArgmaxVecs];
+        if (k0 != tid) {
 #pragma unroll
-        for (int u = 0; u < kArgmaxVecs; ++u) {
-            const int k = k0 + u * kArgmaxThreads;
-            if (k < nvec) v[u] = ld_stream(src + k);
+            for (int u = 0; u < kArgmaxVecs; ++u) {
+                const int k = k0 + u * kArgmaxThreads;
+                if (k < nvec) v[u] = ld_stream(src + k);
+            }
         }
 #pragma unroll
         for (int u = 0; u < kArgmaxVecs; ++u) {
