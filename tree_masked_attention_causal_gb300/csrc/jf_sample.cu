@@ -141,19 +141,28 @@ __global__ void __launch_bounds__(kArgmaxThreads, kArgmaxCtasPerSm)
     const int i = Nmax - 1 - (int)blockIdx.y / nb, b = (int)blockIdx.y - (Nmax - 1 - i) * nb;
     const int row = b * Nmax + i, which = blockIdx.x >= chunks ? 1 : 0;
     const int ch = blockIdx.x - which * chunks;
-    const int n = n_nodes[b];
-    if (n < 1 || n > Nmax || i >= n) return;                 // padding row
     const int tid = threadIdx.x;
     const int e0 = ch * chunk;
     const int nvec = (min(V, e0 + chunk) - e0) >> 3;         // V % 8 == 0
     const uint4 *src = reinterpret_cast<const uint4 *>((which ? draft : target) + (size_t)row * V + e0);
+    // The first vectors go out before the row is known to be real (a
+    // padding row's logits exist too): n_nodes's latency overlaps theirs.
+    uint4 v[kArgmaxVecs];
+#pragma unroll
+    for (int u = 0; u < kArgmaxVecs; ++u) {
+        const int k = tid + u * kArgmaxThreads;
+        if (k < nvec) v[u] = ld_stream(src + k);
+    }
+    const int n = n_nodes[b];
+    if (n < 1 || n > Nmax || i >= n) return;                 // padding row
     float2 acc = make_float2(-__int_as_float(0x7f800000), 0.f);
     for (int k0 = tid; k0 < nvec; k0 += kArgmaxThreads * kArgmaxVecs) {
-        uint4 v[kArgmaxVecs];
+        if (k0 != tid) {
 #pragma unroll
-        for (int u = 0; u < kArgmaxVecs; ++u) {
-            const int k = k0 + u * kArgmaxThreads;
-            if (k < nvec) v[u] = ld_stream(src + k);
+            for (int u = 0; u < kArgmaxVecs; ++u) {
+                const int k = k0 + u * kArgmaxThreads;
+                if (k < nvec) v[u] = ld_stream(src + k);
+            }
         }
 #pragma unroll
         for (int u = 0; u < kArgmaxVecs; ++u) {
